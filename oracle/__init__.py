@@ -1,0 +1,181 @@
+"""CPU oracle for the quantised attention path -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the package's smoke() check and bench.py's CPU-baseline / reference leg
+may import this package.  It shares no code with the CUDA library: the arithmetic lives
+in `sage_oracle.c` (plain C, fp64 loops) and, for tiny cases, in `brute.py` (numpy).
+
+`build()` compiles `sage_oracle.c` with gcc into `oracle/_build/liboracle.so`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sage_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+MUTATIONS = {"none": 0, "no_smooth": 1, "rescale_sign": 2, "scale_255": 3, "key_index": 4,
+             "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, -O2, OpenMP, no FMA contraction, no fast-math)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            P, I = ctypes.c_void_p, ctypes.c_int64
+            L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_decode.restype = ctypes.c_double
+            L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+            L.oracle_e4m3_encode.restype = ctypes.c_uint8
+            L.oracle_set_mutation.argtypes = [ctypes.c_int]
+            L.oracle_k_mean.argtypes = [P, I, I, I, I, I, P]
+            L.oracle_quant_q.argtypes = [P, I, I, I, I, I, P, P]
+            L.oracle_quant_k.argtypes = [P, I, I, I, I, I, P, P, P]
+            L.oracle_quant_v.argtypes = [P, I, I, I, I, I, P, P]
+            L.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, I, I, I, P]
+            L.oracle_attn_sq.argtypes = [P, P, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, P]
+            L.oracle_attn_exact.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double,
+                                            P, I, P]
+            L.oracle_num_threads.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def set_mutation(name: str) -> None:
+    """Plants one deliberate mistake in the oracle (tests of the pins only)."""
+    lib().oracle_set_mutation(MUTATIONS[name])
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+def pad128(n: int) -> int:
+    return (n + 127) // 128 * 128
+
+
+def _view_args(x: torch.Tensor):
+    """A bf16 [N, H, D] CPU view with unit channel stride -> (base pointer, st, sh, keepalive)."""
+    assert x.dtype == torch.bfloat16 and x.device.type == "cpu" and x.dim() == 3
+    assert x.stride(2) == 1
+    return x.data_ptr(), x.stride(0), x.stride(1)
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(x)))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(lib().oracle_e4m3_decode(int(c)))
+
+
+def e4m3_table() -> np.ndarray:
+    """Decoded value of every code 0..255 (NaN for the two NaN codes)."""
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def k_mean(k: torch.Tensor) -> np.ndarray:
+    n, h, d = k.shape
+    mu = np.zeros((h, d), np.float32)
+    p, st, sh = _view_args(k)
+    lib().oracle_k_mean(p, n, h, d, st, sh, _ptr(mu))
+    return mu
+
+
+def quant_q(q: torch.Tensor):
+    n, h, d = q.shape
+    np_ = pad128(n)
+    codes = np.zeros((h, np_, d), np.int8)
+    scales = np.zeros((h, np_ // 128), np.float32)
+    p, st, sh = _view_args(q)
+    lib().oracle_quant_q(p, n, h, d, st, sh, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quant_k(k: torch.Tensor, mu: np.ndarray):
+    n, h, d = k.shape
+    np_ = pad128(n)
+    codes = np.zeros((h, np_, d), np.int8)
+    scales = np.zeros((h, np_ // 64), np.float32)
+    mu = np.ascontiguousarray(mu, dtype=np.float32)
+    p, st, sh = _view_args(k)
+    lib().oracle_quant_k(p, n, h, d, st, sh, _ptr(mu), _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quant_v(v: torch.Tensor):
+    n, h, d = v.shape
+    np_ = pad128(n)
+    codes = np.zeros((h, d, np_), np.uint8)
+    scales = np.zeros((h, d), np.float32)
+    p, st, sh = _view_args(v)
+    lib().oracle_quant_v(p, n, h, d, st, sh, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+class Quantized:
+    """Steps 1-4 of the oracle for one set of inputs."""
+
+    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+        self.n, self.h, self.d = q.shape
+        self.k_mean = k_mean(k)
+        self.q_codes, self.q_scales = quant_q(q)
+        self.k_codes, self.k_scales = quant_k(k, self.k_mean)
+        self.v_codes, self.v_scales = quant_v(v)
+
+
+def qk_int32(qz: Quantized, head: int, i0: int, j0: int, rows: int, cols: int) -> np.ndarray:
+    out = np.zeros((rows, cols), np.int32)
+    lib().oracle_qk_int32(_ptr(qz.q_codes), _ptr(qz.k_codes), qz.n, qz.h, qz.d, head, i0, j0,
+                          rows, cols, _ptr(out))
+    return out
+
+
+def attn_sq(qz: Quantized, sm_scale: float, rows, tile: int = 128) -> np.ndarray:
+    """Same-quantisation attention O_sq for query `rows` (all heads): [len(rows), H, D] fp64."""
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((len(rows), qz.h, qz.d), np.float64)
+    lib().oracle_attn_sq(_ptr(qz.q_codes), _ptr(qz.q_scales), _ptr(qz.k_codes), _ptr(qz.k_scales),
+                         _ptr(qz.v_codes), _ptr(qz.v_scales), qz.n, qz.h, qz.d, float(sm_scale),
+                         _ptr(rows), len(rows), int(tile), _ptr(out))
+    return out
+
+
+def attn_exact(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_scale: float, rows) -> np.ndarray:
+    """Exact fp64 softmax attention O_exact for query `rows` (all heads): [len(rows), H, D]."""
+    n, h, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((len(rows), h, d), np.float64)
+    pq, qst, qsh = _view_args(q)
+    pk, kst, ksh = _view_args(k)
+    pv, vst, vsh = _view_args(v)
+    lib().oracle_attn_exact(pq, pk, pv, n, h, d, qst, qsh, kst, ksh, vst, vsh, float(sm_scale),
+                            _ptr(rows), len(rows), _ptr(out))
+    return out

@@ -1,0 +1,325 @@
+/*
+ * sage_oracle.c -- plain, slow, obviously-correct CPU oracle for SageAttention2-style
+ * quantised attention.  TEST INFRASTRUCTURE ONLY: it is linked by the tests, by the
+ * package's smoke() check and by the CPU-baseline leg of bench.py, never by the product
+ * path.  It shares no source, header or table with the CUDA library.
+ *
+ * What it computes, in the order of the quantised attention call timed in
+ * "gb10-sampling-component-profile-1344x768-124f-seed440420.json"
+ * (key attention_internal_p50_milliseconds.sage2: framework_and_k_smoothing_estimate,
+ * qk_quantize, v_quantize, attention_forward):
+ *
+ *   1. K mean       mu[h,c] = mean over tokens of K[t,h,c]                 oracle_k_mean
+ *   2. Q quantise   per (head, 128-row block) symmetric INT8, fp32 scale   oracle_quant_q
+ *   3. K quantise   K~ = K - mu, per (head, 64-row block) INT8             oracle_quant_k
+ *   4. V quantise   per (head, channel) FP8 E4M3, fp32 scale               oracle_quant_v
+ *   5. S = Qc Kc^T  exact integer dot products                             oracle_qk_int32
+ *   6-8. softmax(S * s_q * s_k * sm_scale) with P held in E4M3, times V    oracle_attn_sq
+ *   9. exact fp64 softmax attention of the bf16 inputs                     oracle_attn_exact
+ *
+ * The shapes are those of the attention call profiled in
+ * "gb10-sage2-p0-interleave-softmax-latency.json" (q_shape [1, 37810, 56, 128]).
+ * Readings where the pages are silent (the summation order of the mean, division rather
+ * than reciprocal multiplication, the clamp at +-127, the static 448 scale of P, ...) are
+ * stated at each function.
+ *
+ * Inputs are bf16 bit patterns (uint16) addressed as data[t*st + h*sh + c]: a strided
+ * [N, H, D] view with unit channel stride.  Code buffers use N_pad = ceil(N/128)*128 rows,
+ * and the pad rows hold code 0.
+ *
+ * Build: plain C99, no fast-math, no FMA contraction (-ffp-contract=off), OpenMP optional.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Test hook: a nonzero value plants one deliberate mistake (see the MUT_* list) so that
+ * the tests can show that the pins catch it.  Always 0 outside those tests. */
+enum { MUT_NONE = 0, MUT_NO_SMOOTH = 1, MUT_RESCALE_SIGN = 2, MUT_SCALE_255 = 3,
+       MUT_KEY_INDEX = 4, MUT_V_SCALE_CHANNEL = 5, MUT_DROP_LAST_KEY = 6,
+       MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8 };
+static int g_mutation = 0;
+void oracle_set_mutation(int m) { g_mutation = m; }
+
+static inline float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static inline int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
+
+/* ------------------------------------------------------------------------------------
+ * FP8 E4M3 (OCP 8-bit floating point specification, E4M3 variant): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 encodes subnormals m * 2^-9; there
+ * are no infinities and S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.110b * 2^8 = 448.  Encoding rounds to nearest with ties to even and saturates finite
+ * values beyond 448 to +-448 ("satfinite").
+ * ---------------------------------------------------------------------------------- */
+double oracle_e4m3_decode(uint8_t c) {
+  int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return s ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(double x) {
+  uint8_t s = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return (uint8_t)(s | 0x7F);
+  if (a > 448.0) a = 448.0;                    /* satfinite */
+  if (a == 0.0) return s;
+  int e2;
+  frexp(a, &e2);                               /* a in [2^(e2-1), 2^e2) */
+  int E = e2 - 1;                              /* unbiased exponent of a */
+  if (E < -6) E = -6;                          /* subnormals share the 2^-6 binade's spacing */
+  double q = ldexp(1.0, E - 3);                /* spacing of E4M3 values in this binade */
+  double n = nearbyint(a / q);                 /* a/q exact; ties to even */
+  if (g_mutation == MUT_E4M3_TRUNC) n = floor(a / q);
+  if (n >= 16.0) { E += 1; n = 8.0; }          /* carried into the next binade */
+  /* n*2^(E-3): for E = -6 the code is n itself (n < 8 subnormal, n = 8.. normal with
+   * exponent field 1); otherwise exponent field E+7 and mantissa n-8. */
+  uint8_t mag = (E == -6) ? (uint8_t)n : (uint8_t)(((E + 7) << 3) | ((int)n - 8));
+  return (uint8_t)(s | mag);
+}
+
+/* ------------------------------------------------------------------------------------
+ * 1. K mean.  The pages fold it into "framework_and_k_smoothing_estimate" and give no
+ * order of summation.  Reading used here (and in the CUDA path, so that the INT8 K codes
+ * can be compared bit for bit): tokens are split into consecutive chunks of 128; each
+ * chunk is summed in fp32 in ascending token order starting from 0; the chunk sums are
+ * added in fp64 in ascending chunk order; the fp64 total is divided by N in fp64 and
+ * rounded once to fp32.
+ * ---------------------------------------------------------------------------------- */
+void oracle_k_mean(const uint16_t* k, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                   float* mu) {
+  int64_t nchunk = (n + 127) / 128;
+  for (int64_t hh = 0; hh < h; ++hh) {
+    for (int64_t c = 0; c < d; ++c) {
+      double total = 0.0;
+      for (int64_t ch = 0; ch < nchunk; ++ch) {
+        float part = 0.0f;
+        int64_t t1 = (ch + 1) * 128 < n ? (ch + 1) * 128 : n;
+        for (int64_t t = ch * 128; t < t1; ++t) part = part + bf16_to_f32(k[t * st + hh * sh + c]);
+        total += (double)part;
+      }
+      double denom = (g_mutation == MUT_MEAN_N_PAD) ? (double)pad128(n) : (double)n;
+      mu[hh * d + c] = (float)(total / denom);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------------------
+ * Symmetric INT8 quantisation of one block (rows [r0, r1) of one head, all D channels).
+ * scale = fl32(amax / 127); code = clamp(round_half_even(fl32(x / scale)), -127, 127),
+ * with IEEE fp32 division.  An all-zero block has scale 0 and codes 0.  Pad rows (>= N)
+ * are not part of the block's max and get code 0.
+ * ---------------------------------------------------------------------------------- */
+static float quant_block_i8(const float* x, int64_t rows, int64_t d, int8_t* codes) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < rows * d; ++i) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  float scale = (g_mutation == MUT_SCALE_255) ? amax / 255.0f : amax / 127.0f;
+  for (int64_t i = 0; i < rows * d; ++i) {
+    if (scale == 0.0f) { codes[i] = 0; continue; }
+    float y = x[i] / scale;
+    float r = rintf(y);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    codes[i] = (int8_t)r;
+  }
+  return scale;
+}
+
+/* 2. Q: one scale per (head, 128-row block). codes [H][N_pad][D], scales [H][N_pad/128]. */
+void oracle_quant_q(const uint16_t* q, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                    int8_t* codes, float* scales) {
+  int64_t np = pad128(n), nb = np / 128;
+  float* buf = (float*)malloc(sizeof(float) * 128 * d);
+  memset(codes, 0, (size_t)(h * np * d));
+  for (int64_t hh = 0; hh < h; ++hh)
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t r0 = b * 128, r1 = r0 + 128 < n ? r0 + 128 : n;
+      for (int64_t t = r0; t < r1; ++t)
+        for (int64_t c = 0; c < d; ++c) buf[(t - r0) * d + c] = bf16_to_f32(q[t * st + hh * sh + c]);
+      scales[hh * nb + b] = quant_block_i8(buf, r1 - r0, d, codes + (hh * np + r0) * d);
+    }
+  free(buf);
+}
+
+/* 3. K smoothing then quantisation: K~ = fl32(K - mu) (one fp32 subtraction), one scale per
+ * (head, 64-row block). codes [H][N_pad][D], scales [H][N_pad/64]. */
+void oracle_quant_k(const uint16_t* k, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                    const float* mu, int8_t* codes, float* scales) {
+  int64_t np = pad128(n), nb = np / 64;
+  float* buf = (float*)malloc(sizeof(float) * 64 * d);
+  memset(codes, 0, (size_t)(h * np * d));
+  for (int64_t hh = 0; hh < h; ++hh)
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t r0 = b * 64, r1 = r0 + 64 < n ? r0 + 64 : n;
+      if (r1 <= r0) { scales[hh * nb + b] = 0.0f; continue; }
+      for (int64_t t = r0; t < r1; ++t)
+        for (int64_t c = 0; c < d; ++c) {
+          float m = (g_mutation == MUT_NO_SMOOTH) ? 0.0f : mu[hh * d + c];
+          buf[(t - r0) * d + c] = bf16_to_f32(k[t * st + hh * sh + c]) - m;
+        }
+      scales[hh * nb + b] = quant_block_i8(buf, r1 - r0, d, codes + (hh * np + r0) * d);
+    }
+  free(buf);
+}
+
+/* 4. V: one scale per (head, channel), scale = fl32(amax over tokens / 448), code =
+ * E4M3(fl32(v / scale)); written transposed as [H][D][N_pad] (keys contiguous). */
+void oracle_quant_v(const uint16_t* v, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                    uint8_t* codes, float* scales) {
+  int64_t np = pad128(n);
+  memset(codes, 0, (size_t)(h * d * np));
+  for (int64_t hh = 0; hh < h; ++hh)
+    for (int64_t c = 0; c < d; ++c) {
+      float amax = 0.0f;
+      for (int64_t t = 0; t < n; ++t) {
+        float a = fabsf(bf16_to_f32(v[t * st + hh * sh + c]));
+        if (a > amax) amax = a;
+      }
+      float scale = amax / 448.0f;
+      int64_t sc = (g_mutation == MUT_V_SCALE_CHANNEL) ? (c + 1) % d : c;
+      scales[hh * d + sc] = scale;
+      for (int64_t t = 0; t < n; ++t) {
+        if (scale == 0.0f) continue;
+        float y = bf16_to_f32(v[t * st + hh * sh + c]) / scale;
+        codes[(hh * d + c) * np + t] = oracle_e4m3_encode((double)y);
+      }
+    }
+}
+
+/* 5. S[i][j] = sum_c qc[h][i0+i][c] * kc[h][j0+j][c], exact in int64, stored as int32
+ * (|S| <= 128 * 127^2 < 2^31). */
+void oracle_qk_int32(const int8_t* qc, const int8_t* kc, int64_t n, int64_t h, int64_t d,
+                     int64_t head, int64_t i0, int64_t j0, int64_t rows, int64_t cols,
+                     int32_t* out) {
+  int64_t np = pad128(n);
+  (void)h;
+  for (int64_t i = 0; i < rows; ++i)
+    for (int64_t j = 0; j < cols; ++j) {
+      int64_t acc = 0;
+      const int8_t* a = qc + (head * np + i0 + i) * d;
+      const int8_t* b = kc + (head * np + j0 + j) * d;
+      for (int64_t c = 0; c < d; ++c) acc += (int64_t)a[c] * (int64_t)b[c];
+      out[i * cols + j] = (int32_t)acc;
+    }
+}
+
+/* ------------------------------------------------------------------------------------
+ * 6-8. Same-quantisation attention for selected query rows (all heads).
+ *   s_ij = S_ij * s_q[h, i/128] * s_k[h, j/64] * sm_scale            (fp64)
+ *   p_ij = exp(s_ij - m_i)                                             (fp64)
+ *   P8_ij = E4M3(448 * p_ij) / 448       (static scale 448: p <= 1 never overflows)
+ *   l_i  = sum_j p_ij                    (unquantised p)
+ *   O_ic = (sum_j P8_ij * E4M3val(vc[h,c,j])) * s_v[h,c] / l_i
+ * tile == 0: m_i is the row's global max (one pass).
+ * tile  > 0: keys are visited in tiles of `tile`; m_i is the running max up to the current
+ *   tile, P8 is formed against it, and whenever m_i rises the partial sums (O and l) are
+ *   multiplied by exp(m_old - m_new) in fp64 -- an exact rescale on every increase, the
+ *   schedule of an online-softmax kernel that holds P in E4M3.
+ * out[r][h][c] (fp64).
+ * ---------------------------------------------------------------------------------- */
+void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const float* ks,
+                    const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
+                    double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
+                    double* out) {
+  int64_t np = pad128(n), nbq = np / 128, nbk = np / 64;
+  int64_t nkeys = (g_mutation == MUT_DROP_LAST_KEY) ? n - 1 : n;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t rh = 0; rh < nrows * h; ++rh) {
+    int64_t r = rh / h, hh = rh % h, i = rows[r];
+    double* o = (double*)calloc((size_t)d, sizeof(double));
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    const int8_t* a = qc + (hh * np + i) * d;
+    double sq = (double)qs[hh * nbq + i / 128];
+    for (int64_t j = 0; j < nkeys; ++j) {
+      int64_t jj = (g_mutation == MUT_KEY_INDEX) ? (j ^ 1) % n : j;
+      const int8_t* b = kc + (hh * np + jj) * d;
+      int64_t acc = 0;
+      for (int64_t c = 0; c < d; ++c) acc += (int64_t)a[c] * (int64_t)b[c];
+      s[j] = (double)acc * sq * (double)ks[hh * nbk + j / 64] * sm_scale;
+    }
+    double m = -INFINITY, l = 0.0;
+    int64_t tw = tile > 0 ? tile : nkeys;
+    if (tile <= 0)
+      for (int64_t j = 0; j < nkeys; ++j) if (s[j] > m) m = s[j];
+    for (int64_t j0 = 0; j0 < nkeys; j0 += tw) {
+      int64_t j1 = j0 + tw < nkeys ? j0 + tw : nkeys;
+      if (tile > 0) {
+        double mt = -INFINITY;
+        for (int64_t j = j0; j < j1; ++j) if (s[j] > mt) mt = s[j];
+        if (mt > m) {
+          if (m != -INFINITY) {
+            double alpha = (g_mutation == MUT_RESCALE_SIGN) ? exp(mt - m) : exp(m - mt);
+            for (int64_t c = 0; c < d; ++c) o[c] *= alpha;
+            l *= alpha;
+          }
+          m = mt;
+        }
+      }
+      for (int64_t j = j0; j < j1; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        double p8 = oracle_e4m3_decode(oracle_e4m3_encode(448.0 * p));
+        if (p8 == 0.0) continue;
+        for (int64_t c = 0; c < d; ++c)
+          o[c] += p8 * oracle_e4m3_decode(vc[(hh * d + c) * np + j]);
+      }
+    }
+    for (int64_t c = 0; c < d; ++c)
+      out[(r * h + hh) * d + c] = o[c] * (double)vs[hh * d + c] / (448.0 * l);
+    free(o);
+    free(s);
+  }
+}
+
+/* 9. Exact attention of the bf16 inputs in fp64: O = softmax(sm_scale * q k^T) v, no
+ * smoothing, no quantisation.  out[r][h][c]. */
+void oracle_attn_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t n,
+                       int64_t h, int64_t d, int64_t qst, int64_t qsh, int64_t kst, int64_t ksh,
+                       int64_t vst, int64_t vsh, double sm_scale, const int64_t* rows,
+                       int64_t nrows, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t rh = 0; rh < nrows * h; ++rh) {
+    int64_t r = rh / h, hh = rh % h, i = rows[r];
+    double* qi = (double*)malloc(sizeof(double) * (size_t)d);
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    double* o = (double*)calloc((size_t)d, sizeof(double));
+    for (int64_t c = 0; c < d; ++c) qi[c] = bf16_to_f32(q[i * qst + hh * qsh + c]);
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+      double acc = 0.0;
+      for (int64_t c = 0; c < d; ++c) acc += qi[c] * (double)bf16_to_f32(k[j * kst + hh * ksh + c]);
+      s[j] = sm_scale * acc;
+      if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      double p = exp(s[j] - m);
+      l += p;
+      for (int64_t c = 0; c < d; ++c) o[c] += p * (double)bf16_to_f32(v[j * vst + hh * vsh + c]);
+    }
+    for (int64_t c = 0; c < d; ++c) out[(r * h + hh) * d + c] = o[c] / l;
+    free(qi);
+    free(s);
+    free(o);
+  }
+}
+
+/* Threads OpenMP will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

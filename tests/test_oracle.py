@@ -1,0 +1,365 @@
+"""Pins of the CPU oracle against facts fixed by the formats and the mathematics.
+
+Each test names what it pins.  Nothing here runs on a GPU.
+"""
+import fractions
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+from video_diffusion_transformer_sage_gb300 import synth
+
+
+def rel_l2(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def small_inputs(n=300, h=2, d=64, layout="qkv", seed=5, n_outlier=2, rms=False, bias_var=4.0):
+    return synth.make_inputs(synth.custom(n, h, d, layout, seed, k_bias_var=bias_var,
+                                          n_outlier=n_outlier, rms_norm=rms))
+
+
+# ---------------------------------------------------------------- E4M3 (OCP FP8 format)
+
+def test_e4m3_decode_closed_forms(oracle_lib):
+    # largest finite, smallest subnormal, smallest normal, one, NaN, negative zero
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0x3C) == 1.5
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+    z = oracle.e4m3_decode(0x80)
+    assert z == 0.0 and math.copysign(1.0, z) < 0
+    assert oracle.e4m3_decode(0xFE) == -448.0
+
+
+def test_e4m3_roundtrip_all_codes(oracle_lib):
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c, hex(c)
+
+
+def test_e4m3_midpoints_ties_to_even(oracle_lib):
+    vals = brute.e4m3_values()
+    for i in range(len(vals) - 1):
+        mid = 0.5 * (vals[i] + vals[i + 1])
+        want = i if i % 2 == 0 else i + 1
+        assert oracle.e4m3_encode(mid) == want, (i, mid)
+        assert oracle.e4m3_encode(-mid) == (want | 0x80)
+
+
+def test_e4m3_matches_torch_float8_cast(oracle_lib):
+    """torch's float8_e4m3fn cast rounds to nearest-even within range (a library routine)."""
+    g = torch.Generator().manual_seed(0)
+    x = torch.cat([torch.randn(4000, generator=g, dtype=torch.float64) * s
+                   for s in (1e-3, 1e-2, 0.1, 1.0, 10.0, 100.0)])
+    vals = torch.tensor(brute.e4m3_values(), dtype=torch.float64)
+    mids = 0.5 * (vals[:-1] + vals[1:])
+    x = torch.cat([x, mids, -mids, vals, -vals]).clamp(-448.0, 448.0)
+    ref = x.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([oracle.e4m3_encode(float(v)) for v in x.to(torch.float32).tolist()], np.uint8)
+    # torch keeps the sign of zero; so does the oracle
+    assert (ref == ours).all()
+
+
+def test_e4m3_saturates(oracle_lib):
+    assert oracle.e4m3_encode(448.0) == 0x7E
+    assert oracle.e4m3_encode(463.9) == 0x7E
+    assert oracle.e4m3_encode(1e6) == 0x7E
+    assert oracle.e4m3_encode(-500.0) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -11) == 0x00     # below half the smallest subnormal
+    assert oracle.e4m3_encode(2.0 ** -10 * 1.0001) == 0x01
+
+
+def test_e4m3_brute_agrees(oracle_lib):
+    g = np.random.default_rng(1)
+    x = np.concatenate([g.standard_normal(20000) * s for s in (1e-3, 0.1, 1, 30, 300)])
+    ours = np.array([oracle.e4m3_encode(float(v)) for v in x], np.uint8)
+    assert (ours == brute.e4m3_encode(x)).all()
+
+
+# ---------------------------------------------------------------- K mean (smoothing)
+
+def test_k_mean_constant_column_exact(oracle_lib):
+    inp = small_inputs(n=1000, h=2, d=64, layout="nhd")
+    k = inp.k.clone()
+    k[:, 0, :] = 0.375
+    k[:, 1, 5] = -3.0
+    mu = oracle.k_mean(k)
+    assert (mu[0] == np.float32(0.375)).all()
+    assert mu[1, 5] == np.float32(-3.0)
+
+
+def test_k_mean_vs_exact_rational(oracle_lib):
+    """mu is within the fp32 chunk-summation error bound of the exact rational mean."""
+    inp = small_inputs(n=4100, h=3, d=64, layout="qkv")
+    mu = oracle.k_mean(inp.k)
+    kf = inp.k.float().numpy().astype(np.float64)
+    n = kf.shape[0]
+    u = 2.0 ** -24
+    for hh, c in [(0, 0), (1, 17), (2, 63), (0, 31)]:
+        col = kf[:, hh, c]
+        exact = sum((fractions.Fraction(float(x)) for x in col), fractions.Fraction(0)) / n
+        bound = 127 * u * np.abs(col).sum() / n + 2 * u * abs(float(exact)) + 1e-30
+        assert abs(float(mu[hh, c]) - float(exact)) <= bound
+
+
+def test_smoothing_invariance_of_softmax():
+    """softmax(q (k - mu)^T) == softmax(q k^T) row by row, so O_exact needs no mean correction."""
+    g = np.random.default_rng(2)
+    q, k, v = g.standard_normal((3, 50, 2, 32))
+    mu = g.standard_normal((2, 32)) * 3
+    a = brute.attn_exact(q, k, v, 0.2)
+    b = brute.attn_exact(q, k - mu[None], v, 0.2)
+    assert np.abs(a - b).max() < 1e-12
+
+
+# ---------------------------------------------------------------- INT8 / E4M3 quantisation
+
+@pytest.mark.parametrize("layout", ["nhd", "qkv", "hnd"])
+def test_quant_matches_brute(oracle_lib, layout):
+    inp = small_inputs(n=300, h=2, d=64, layout=layout)
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    qf = inp.q.float().numpy().transpose(1, 0, 2)
+    kf = (inp.k.float().numpy() - qz.k_mean[None]).astype(np.float32).transpose(1, 0, 2)
+    vf = inp.v.float().numpy().transpose(1, 0, 2)
+    bq, bqs = brute.quant_int8_blocks(np.ascontiguousarray(qf), 128)
+    bk, bks = brute.quant_int8_blocks(np.ascontiguousarray(kf), 64)
+    bv, bvs = brute.quant_v(np.ascontiguousarray(vf))
+    assert (bq == qz.q_codes).all() and (bqs == qz.q_scales).all()
+    assert (bk == qz.k_codes).all() and (bks == qz.k_scales).all()
+    assert (bv == qz.v_codes).all() and (bvs == qz.v_scales).all()
+
+
+def test_int8_error_bound_and_range(oracle_lib):
+    inp = synth.make_inputs("tails")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    n = inp.q.shape[0]
+    for codes, scales, block, x in (
+            (qz.q_codes, qz.q_scales, 128, inp.q.float().numpy()),
+            (qz.k_codes, qz.k_scales, 64, inp.k.float().numpy() - qz.k_mean[None])):
+        xs = x.transpose(1, 0, 2)                                  # [H, N, D]
+        s = np.repeat(scales, block, axis=1)[:, :n, None].astype(np.float64)
+        deq = codes[:, :n].astype(np.float64) * s
+        assert (np.abs(deq - xs) <= s * 0.5 * (1 + 2e-5) + 1e-30).all()
+        assert np.abs(codes).max() <= 127
+        # every nonzero block holds a code of magnitude 127 (its max element)
+        nb = scales.shape[1]
+        cb = np.abs(codes.astype(np.int32)).reshape(codes.shape[0], nb, block, -1).max(axis=(2, 3))
+        assert ((cb == 127) | (scales == 0)).all()
+        assert (codes[:, n:] == 0).all()
+
+
+def test_v_quant_error_bound(oracle_lib):
+    inp = small_inputs(n=500, h=2, d=64, layout="nhd")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    v = inp.v.float().numpy().astype(np.float64)       # [N, H, D]
+    dec = brute.e4m3_decode(qz.v_codes[:, :, :500])   # [H, D, N]
+    deq = dec * qz.v_scales[:, :, None]
+    vt = v.transpose(1, 2, 0)
+    # half an E4M3 ulp at the value's magnitude: ulp = 2^(floor(log2|y|) - 3), >= 2^-9
+    y = np.abs(vt / qz.v_scales[:, :, None])
+    ulp = np.where(y < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(y, 1e-30))) - 3))
+    assert (np.abs(deq - vt) <= 0.5 * ulp * qz.v_scales[:, :, None] * (1 + 1e-6)).all()
+    assert (np.abs(dec).max(axis=2) == 448.0).all()
+
+
+def test_all_zero_block(oracle_lib):
+    inp = small_inputs(n=256, h=1, d=64, layout="nhd")
+    q = inp.q.clone()
+    q[:128] = 0
+    codes, scales = oracle.quant_q(q)
+    assert scales[0, 0] == 0 and (codes[0, :128] == 0).all() and scales[0, 1] > 0
+
+
+# ---------------------------------------------------------------- integer S and attention
+
+def test_qk_int32_matches_integer_matmul(oracle_lib):
+    inp = small_inputs(n=300, h=2, d=64)
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    S = oracle.qk_int32(qz, 1, 128, 64, 100, 200)
+    ref = qz.q_codes[1, 128:228].astype(np.int64) @ qz.k_codes[1, 64:264].astype(np.int64).T
+    assert (S == ref).all()
+    # worst case magnitude fits: all +-127
+    qz.q_codes[0, :128] = 127
+    qz.k_codes[0, :128] = -127
+    S = oracle.qk_int32(qz, 0, 0, 0, 4, 4)
+    assert (S == -127 * 127 * 64).all()
+
+
+def test_attn_exact_matches_brute(oracle_lib):
+    inp = small_inputs(n=200, h=2, d=64, layout="qkv")
+    rows = list(range(200))
+    a = oracle.attn_exact(inp.q, inp.k, inp.v, 0.125, rows)
+    b = brute.attn_exact(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), 0.125)
+    assert np.abs(a - b).max() < 1e-12
+
+
+def test_attn_exact_rows_sum_to_one(oracle_lib):
+    inp = small_inputs(n=300, h=2, d=64, layout="nhd")
+    v = torch.ones_like(inp.v)
+    o = oracle.attn_exact(inp.q, inp.k, v, 0.125, [0, 7, 299])
+    assert np.abs(o - 1.0).max() < 1e-12
+
+
+def test_constant_keys_give_mean_of_v(oracle_lib):
+    inp = small_inputs(n=300, h=2, d=64, layout="nhd")
+    k = torch.empty_like(inp.k)
+    k[:] = inp.k[3]
+    o = oracle.attn_exact(inp.q, k, inp.v, 0.125, [0, 150])
+    mean_v = inp.v.double().mean(dim=0).numpy()
+    assert np.abs(o - mean_v[None]).max() < 1e-12
+    # the quantised path: K~ = 0 -> all codes 0 -> uniform P8 -> O_sq = mean of dequantised V
+    qz = oracle.Quantized(inp.q, k, inp.v)
+    assert (qz.k_codes == 0).all()
+    osq = oracle.attn_sq(qz, 0.125, [0, 150], tile=128)
+    vdeq = brute.e4m3_decode(qz.v_codes[:, :, :300]) * qz.v_scales[:, :, None]
+    assert np.abs(osq - vdeq.mean(axis=2)[None]).max() < 1e-12
+
+
+def test_one_hot_query_selects_value(oracle_lib):
+    n, h, d = 200, 1, 64
+    inp = small_inputs(n=n, h=h, d=d, layout="nhd", n_outlier=0)
+    q = torch.zeros_like(inp.q)
+    q[:, 0, 0] = 8.0
+    k = torch.zeros_like(inp.k)
+    k[:, 0, 0] = torch.linspace(-1, 1, n).to(torch.bfloat16)
+    k[77, 0, 0] = 4.0
+    o = oracle.attn_exact(q, k, inp.v, 1.0, [5])
+    assert np.abs(o[0, 0] - inp.v[77, 0].double().numpy()).max() < 1e-6
+
+
+def test_attn_sq_matches_brute_global(oracle_lib):
+    inp = small_inputs(n=300, h=2, d=64, layout="qkv")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    rows = list(range(300))
+    a = oracle.attn_sq(qz, 0.125, rows, tile=0)
+    b = brute.attn_sq_global(qz.q_codes, qz.q_scales, qz.k_codes, qz.k_scales, qz.v_codes,
+                             qz.v_scales, 300, 0.125)
+    assert np.abs(a - b).max() < 1e-12
+
+
+def test_attn_sq_single_tile_equals_global(oracle_lib):
+    inp = small_inputs(n=128, h=2, d=64, layout="nhd")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    rows = list(range(128))
+    a = oracle.attn_sq(qz, 0.125, rows, tile=128)
+    b = oracle.attn_sq(qz, 0.125, rows, tile=0)
+    assert (a == b).all()
+
+
+def _tiled_exact_case_error() -> float:
+    """Scores that are integer multiples of ln 2 make every p an exact power of two, which
+    E4M3 holds exactly, so tiled mode (with its rescales on each rise of the running max)
+    must equal global mode and the closed form sum_j 2^k_j v_j / sum_j 2^k_j.  Returns the
+    largest deviation from either."""
+    n, d = 384, 64
+    inp = small_inputs(n=n, h=1, d=d, layout="nhd")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    g = np.random.default_rng(3)
+    kexp = g.integers(-6, 1, size=n)                 # exponents in [-6, 0]
+    kexp[: n // 3] -= 2                             # first tile lower: max rises later
+    kexp[n - 5] = 1                                 # global max in the last tile
+    qz.q_codes[:] = 0
+    qz.q_codes[0, :n, 0] = 1
+    qz.k_codes[:] = 0
+    qz.k_codes[0, :n, 0] = kexp
+    qz.q_scales[:] = 1.0
+    qz.k_scales[:] = 1.0
+    rows = [0, 5, 200]
+    t = oracle.attn_sq(qz, math.log(2.0), rows, tile=128)
+    gl = oracle.attn_sq(qz, math.log(2.0), rows, tile=0)
+    w = 2.0 ** (kexp - kexp.max())
+    vdeq = brute.e4m3_decode(qz.v_codes[0, :, :n]) * qz.v_scales[0][:, None]   # [D, N]
+    closed = (vdeq @ w) / w.sum()
+    return max(np.abs(t - gl).max(), np.abs(t[:, 0] - closed[None]).max())
+
+
+def test_attn_sq_tiled_rescale_exact_case(oracle_lib):
+    assert _tiled_exact_case_error() < 1e-12
+
+
+def test_attn_sq_method_gap_to_exact(oracle_lib):
+    """Same-quantisation attention stays near exact attention; on N(0,1) values E4M3 V and
+    P each cost about 2.5 % relative L2 (3 mantissa bits), which bounds the method's gap."""
+    inp = synth.make_inputs("tiny")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    rows = synth.sample_rows(1024, 64, 0)
+    sm = 1 / math.sqrt(128)
+    t = oracle.attn_sq(qz, sm, rows, tile=128)
+    gl = oracle.attn_sq(qz, sm, rows, tile=0)
+    e = oracle.attn_exact(inp.q, inp.k, inp.v, sm, rows)
+    assert rel_l2(t, e) < 5e-2 and rel_l2(gl, e) < 5e-2
+    assert rel_l2(t, gl) < 4e-2
+
+
+def test_page_shapes_golden():
+    """Tile counts of the pages' attention call, printed on the pages."""
+    import json, os
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_shapes.json")))
+    _, n, h, d = gold["q_shape"]["value"]
+    segs = gold["segments"]["value"]
+    assert segs[-1][1] == n == gold["packed_tokens"]["value"] == synth.WORKLOADS["video"].n_tokens
+    assert sum(e - s for s, e, _ in segs) == n
+    assert tuple(map(tuple, segs)) == synth.VIDEO_SEGMENTS
+    cta_q = gold["scheduler"]["value"]["cta_q"]
+    assert oracle.pad128(n) // cta_q * h == gold["scheduler"]["value"]["grid_ctas"]
+    assert abs(synth.WORKLOADS["video"].flops - 40.989e12) / 40.989e12 < 1e-4
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _pins_pass(inp) -> bool:
+    """A quick battery of the pins above; False as soon as one fails."""
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    n = inp.q.shape[0]
+    kf = (inp.k.float().numpy() - brute_k_mean_exactish(inp.k)[None]).astype(np.float32)
+    bk, bks = brute.quant_int8_blocks(np.ascontiguousarray(kf.transpose(1, 0, 2)), 64)
+    if not ((bk == qz.k_codes).mean() > 0.999):
+        return False
+    bq, bqs = brute.quant_int8_blocks(np.ascontiguousarray(inp.q.float().numpy().transpose(1, 0, 2)), 128)
+    if not ((bq == qz.q_codes).all() and (bqs == qz.q_scales).all()):
+        return False
+    bv, bvs = brute.quant_v(np.ascontiguousarray(inp.v.float().numpy().transpose(1, 0, 2)))
+    if not ((bv == qz.v_codes).all() and (bvs == qz.v_scales).all()):
+        return False
+    rows = list(range(n))
+    gl = oracle.attn_sq(qz, 0.125, rows, tile=0)
+    g = brute.attn_sq_global(qz.q_codes, qz.q_scales, qz.k_codes, qz.k_scales, qz.v_codes,
+                             qz.v_scales, n, 0.125)
+    if not np.abs(gl - g).max() < 1e-12:
+        return False
+    if not _tiled_exact_case_error() < 1e-12:
+        return False
+    e = oracle.attn_exact(inp.q, inp.k, inp.v, 0.125, rows)
+    b = brute.attn_exact(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), 0.125)
+    return np.abs(e - b).max() < 1e-12
+
+
+def brute_k_mean_exactish(k: torch.Tensor) -> np.ndarray:
+    """fp64 mean rounded to fp32 (agrees with the oracle's mean to within an ulp or so)."""
+    return k.double().mean(dim=0).float().numpy()
+
+
+def test_pins_pass_unmutated(oracle_lib):
+    inp = small_inputs(n=400, h=2, d=64, layout="qkv", bias_var=16.0)
+    assert _pins_pass(inp)
+
+
+@pytest.mark.parametrize("mutation", [m for m in oracle.MUTATIONS if m != "none"])
+def test_planted_mistake_is_caught(oracle_lib, mutation):
+    inp = small_inputs(n=400, h=2, d=64, layout="qkv", bias_var=16.0)
+    try:
+        oracle.set_mutation(mutation)
+        caught = not _pins_pass(inp)
+    finally:
+        oracle.set_mutation("none")
+    assert caught, mutation
