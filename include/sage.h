@@ -1,0 +1,173 @@
+/*
+ * sage.h -- C ABI of the GB300 (sm_103a) quantised-attention library `libsage_gb300.so`.
+ *
+ * The library computes SageAttention2-style non-causal multi-head attention over one
+ * packed token sequence: per-head K mean smoothing, symmetric INT8 quantisation of Q
+ * (one scale per head and 128-row block) and of K - mean (per head and 64-row block),
+ * FP8 E4M3 quantisation of V (per head and channel), then a fused kernel that forms the
+ * exact integer QK^T on the tensor cores, runs an fp32 online softmax, multiplies E4M3 P
+ * by E4M3 V with fp32 accumulation and writes bf16 O.
+ *
+ * Page references: the call is the Sage2 attention of block 24 profiled in
+ * "gb10-sampling-component-profile-1344x768-124f-seed440420.json"
+ * (attention_internal_p50_milliseconds.sage2: qk_quantize, v_quantize, attention_forward,
+ * framework_and_k_smoothing_estimate) at q_shape [1, 37810, 56, 128]
+ * ("gb10-sage2-p0-interleave-softmax-latency.json", key q_shape), and it reads Q, K, V as
+ * strided NHD views of the token-major QKV projection with no transposed copies and
+ * writes a contiguous NHD output that the next projection reads as [N, H*D]
+ * ("gb10-sage-strided-nhd-summary-1344x768-124f-seed440420.json", key dataflow).
+ *
+ * General rules for every entry point:
+ *  - All pointers are DEVICE pointers unless a parameter says "host".  The caller owns
+ *    every buffer (inputs, outputs, code buffers, workspace); the library allocates no
+ *    device memory and keeps no per-call state.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy default stream)
+ *    and the call returns without waiting, except sage_check_device_status.
+ *  - Arguments are checked before anything is launched; a failed check returns a status
+ *    and launches nothing.  Nothing aborts or throws.  SAGE_ERR_CUDA wraps a failed launch
+ *    (cudaGetLastError after the launch).
+ *  - Batch is 1 (the pages' call has batch 1).  head_dim must be 64 or 128.  Q, K and V
+ *    must agree in n_tokens, n_heads and head_dim.
+ *  - N_pad = ceil(n_tokens / 128) * 128.  Code buffers hold N_pad rows; pad rows get code 0.
+ */
+#ifndef SAGE_GB300_H
+#define SAGE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sage_status {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, mismatched shapes */
+  SAGE_ERR_ALIGNMENT = 2,       /* pointer not 16-byte aligned or stride not a multiple of 8 elements */
+  SAGE_ERR_UNSUPPORTED = 3,     /* head_dim not in {64, 128}; sizes beyond the int32 index range */
+  SAGE_ERR_WORKSPACE = 4,       /* workspace pointer null or smaller than required */
+  SAGE_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed */
+  SAGE_ERR_DEVICE_TIMEOUT = 6   /* a bounded device-side wait expired (see sage_check_device_status) */
+} sage_status;
+
+/* A bf16 [n_tokens, n_heads, head_dim] view with unit channel stride: element (t, h, c)
+ * lives at ((const uint16_t*)data)[t * stride_token + h * stride_head + c].
+ * data must be 16-byte aligned and both strides multiples of 8 elements (16 bytes), so
+ * that every (t, h) row can be read with 16-byte vector loads.  Examples: a contiguous
+ * NHD tensor has strides (H*D, D); a Q/K/V slice of a token-major [N, 3*H*D] projection
+ * buffer has strides (3*H*D, D); an HND-contiguous tensor has strides (D, N*D). */
+typedef struct sage_view {
+  const void* data;
+  int64_t n_tokens;
+  int64_t n_heads;
+  int64_t head_dim;
+  int64_t stride_token;
+  int64_t stride_head;
+} sage_view;
+
+/* Quantised operands produced by sage_smooth_quant_qk / sage_quant_v and consumed by
+ * sage_attn_fwd_quantized.  Layouts (all row-major):
+ *   q_codes  [H][N_pad][D]  INT8 codes in [-127, 127] held as IEEE fp16 (uint16 bits).
+ *            sm_103a has no 8-bit integer MMA kind; every integer |c| <= 2048 is exact
+ *            in fp16, and the fp16 MMA with fp32 accumulation reproduces the integer dot
+ *            products exactly (|QK^T| <= 128 * 127^2 < 2^21).
+ *   q_scales [H][N_pad/128] fp32
+ *   k_codes  [H][N_pad][D]  as q_codes, codes of K - k_mean
+ *   k_scales [H][N_pad/64]  fp32
+ *   k_mean   [H][D]         fp32
+ *   v_codes  [H][D][N_pad]  FP8 E4M3 bytes, keys contiguous (the K-major B operand of P.V)
+ *   v_scales [H][D]         fp32
+ * All of these pointers must be 16-byte aligned. */
+typedef struct sage_quantized {
+  uint16_t* q_codes;
+  float* q_scales;
+  uint16_t* k_codes;
+  float* k_scales;
+  float* k_mean;
+  uint8_t* v_codes;
+  float* v_scales;
+} sage_quantized;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* sage_status_string(sage_status status);
+
+/* Bytes of scratch that sage_smooth_quant_qk and sage_quant_v need in `ws`: per-128-token
+ * column partials of K (sums) or V (absolute maxima), 4 * ceil(N/128) * H * D bytes each,
+ * plus alignment slack. */
+size_t sage_quant_scratch_bytes(int64_t n_tokens, int64_t n_heads, int64_t head_dim);
+
+/* Bytes of workspace sage_attn_fwd needs: the sage_quantized buffers above, the scratch of
+ * sage_quant_scratch_bytes and a 256-byte device status block, each 256-byte aligned. */
+size_t sage_workspace_bytes(int64_t n_tokens, int64_t n_heads, int64_t head_dim);
+
+/* Bytes of the status block that sage_attn_fwd_quantized takes. */
+size_t sage_status_block_bytes(void);
+
+/* K smoothing and INT8 quantisation of Q and K (the pages' framework_and_k_smoothing and
+ * qk_quantize stages).
+ *   k_mean[h][c] = fp32( (sum over 128-token chunks, ascending, of the fp32 chunk sum taken
+ *                  in ascending token order) / N ), the chunk sums added in fp64;
+ *   Q: per (h, 128-row block) scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)),
+ *      -127, 127) with IEEE division; an all-zero block has scale 0 and codes 0;
+ *   K: the same on fl32(k - k_mean[h][c]) per (h, 64-row block).
+ * Writes qz->q_codes, q_scales, k_codes, k_scales, k_mean.  ws: >= sage_quant_scratch_bytes,
+ * 16-byte aligned, contents ignored and overwritten. */
+sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const sage_quantized* qz,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* FP8 E4M3 quantisation of V (the pages' v_quantize stage): per (h, c) scale =
+ * fl32(max_t |v| / 448), code = E4M3 round-to-nearest-even, saturating, of fl32(v / scale);
+ * an all-zero channel has scale 0 and codes 0.  Writes qz->v_codes (transposed to
+ * [H][D][N_pad]) and qz->v_scales.  ws as for sage_smooth_quant_qk. */
+sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Fused attention on quantised operands (the pages' attention_forward stage):
+ *   s_ij = S_ij * q_scales[h][i/128] * k_scales[h][j/64] * sm_scale,  S = exact integer QK^T
+ *   running row max m over 128-key tiles; p = exp(s - m); P8 = E4M3(448 p);
+ *   l = sum of fp32 p; O and l are multiplied by exp(m_old - m_new) whenever m rises;
+ *   out[i][h][c] = bf16_rn( (sum_j P8_ij * v_codes[h][c][j]) * v_scales[h][c] / (448 l) ).
+ * out: bf16, element (t, h, c) at out[t * out_stride_token + h * out_stride_head + c];
+ * 16-byte aligned, strides multiples of 8 elements; rows >= n_tokens are never written.
+ * status_block: >= sage_status_block_bytes() bytes of device memory, zeroed by the caller
+ * once; the kernel records expired device waits there (sage_check_device_status). */
+sage_status sage_attn_fwd_quantized(int64_t n_tokens, int64_t n_heads, int64_t head_dim,
+                                    const sage_quantized* qz, float sm_scale, void* out,
+                                    int64_t out_stride_token, int64_t out_stride_head,
+                                    void* status_block, void* stream);
+
+/* The whole path: sage_smooth_quant_qk, sage_quant_v and sage_attn_fwd_quantized on
+ * buffers carved from ws (>= sage_workspace_bytes, 256-byte aligned; the status block at
+ * its start must be zeroed once by the caller before first use). */
+sage_status sage_attn_fwd(const sage_view* q, const sage_view* k, const sage_view* v, float sm_scale,
+                          void* out, int64_t out_stride_token, int64_t out_stride_head, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* Unquantised reference attention in bf16 inputs / fp32 arithmetic:
+ * out = bf16_rn(softmax(sm_scale * q k^T) v), the dense attention the pages use as the
+ * quality anchor (quality_gates.sol_fully_dense_tau_minus_100_relative_l2_vs_sage2).
+ * A correctness path, not tuned. */
+sage_status sage_attn_dense_bf16(const sage_view* q, const sage_view* k, const sage_view* v,
+                                 float sm_scale, void* out, int64_t out_stride_token,
+                                 int64_t out_stride_head, void* stream);
+
+/* Test hook: the integer S = Qc Kc^T of head `head`, query rows [i0, i0 + 128 * row_tiles)
+ * and keys [j0, j0 + 128 * col_tiles), produced by the same tensor-core QK^T code path
+ * as sage_attn_fwd_quantized and converted to int32.  i0, j0 multiples of 128 and inside
+ * N_pad.  out: int32 [128 * row_tiles][128 * col_tiles] row-major. */
+sage_status sage_debug_qk_int32(int64_t n_tokens, int64_t n_heads, int64_t head_dim,
+                                const sage_quantized* qz, int64_t head, int64_t i0, int64_t j0,
+                                int64_t row_tiles, int64_t col_tiles, int32_t* out,
+                                void* status_block, void* stream);
+
+/* Waits for `stream`, reads the status block (device pointer) and returns SAGE_OK,
+ * SAGE_ERR_DEVICE_TIMEOUT (a bounded wait expired; the block is then cleared) or
+ * SAGE_ERR_CUDA.  If where != NULL (host), *where receives the code of the wait that
+ * expired (0 if none).  This is the one call that synchronises. */
+sage_status sage_check_device_status(void* status_block, void* stream, int32_t* where);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_GB300_H */

@@ -17,3 +17,30 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+_CASES = {}
+
+
+def gpu_case(name: str):
+    """Seeded inputs of a named workload on the CPU and on cuda:0, plus the oracle's
+    quantised operands (cached for the session)."""
+    if name not in _CASES:
+        import torch
+        import oracle
+        from video_diffusion_transformer_sage_gb300 import synth
+        if name.endswith("_hndcopy"):
+            base = gpu_case(name[: -len("_hndcopy")])
+            inp = synth.to_hnd(base["inp"])
+            qz = base["qz"]
+        else:
+            inp = synth.make_inputs(name)
+            qz = oracle.Quantized(inp.q, inp.k, inp.v)
+        dev = torch.device("cuda:0")
+        storage = inp.storage.to(dev)
+        # the same views of the device copy
+        def dview(t):
+            off = t.storage_offset() - inp.storage.storage_offset()
+            return storage.as_strided(t.shape, t.stride(), storage.storage_offset() + off)
+        _CASES[name] = dict(inp=inp, qz=qz, storage=storage, q=dview(inp.q), k=dview(inp.k), v=dview(inp.v))
+    return _CASES[name]

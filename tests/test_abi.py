@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI: the library loads, exports every function that
+include/sage.h declares, sizes workspaces consistently, and rejects bad arguments before
+launching anything (these calls never reach the GPU)."""
+import ctypes
+
+import pytest
+
+import video_diffusion_transformer_sage_gb300 as sage
+from video_diffusion_transformer_sage_gb300 import _lib
+
+EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_bytes", "sage_status_block_bytes",
+            "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
+            "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status"}
+
+
+@pytest.fixture(scope="module")
+def L():
+    from video_diffusion_transformer_sage_gb300 import build
+    build.build()
+    return sage.lib()
+
+
+def test_header_declares_expected(L):
+    assert set(sage.header_functions()) == EXPECTED
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in sage.header_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = L.sage_status_string(code).decode()
+        assert s.startswith(_lib.STATUS[code])
+
+
+def test_workspace_sizes(L):
+    n, h, d = 37810, 56, 128
+    np_ = 37888
+    ws = L.sage_workspace_bytes(n, h, d)
+    need = 2 * h * np_ * d * 2 + h * d * np_ + h * (np_ // 128) * 4 + h * (np_ // 64) * 4 + 2 * h * d * 4
+    need += (np_ // 128) * h * d * 4 + 256
+    assert need <= ws <= need + 16 * 256
+    assert L.sage_quant_scratch_bytes(n, h, d) >= (np_ // 128) * h * d * 4
+    assert L.sage_workspace_bytes(n, h, 96) == 0       # unsupported head_dim
+    assert L.sage_workspace_bytes(0, h, d) == 0
+    assert L.sage_status_block_bytes() >= 8
+
+
+def _view(ptr=16, n=256, h=2, d=128, st=256, sh=128):
+    return _lib.SageView(ptr, n, h, d, st, sh)
+
+
+def _qz(ptr=4096):
+    return _lib.SageQuantizedC(*([ptr] * 7))
+
+
+def test_argument_validation_never_launches(L):
+    """Every bad argument is reported before any CUDA call: fake (non-null, aligned) device
+    pointers are never dereferenced on these paths."""
+    q, k, v = _view(), _view(), _view()
+    qz = _qz()
+    call = lambda *a: L.sage_smooth_quant_qk(*a)
+    by = ctypes.byref
+    # null view data
+    assert call(by(_view(ptr=0)), by(k), by(qz), 4096, 1 << 30, None) == 1
+    # unsupported head dim
+    assert call(by(_view(d=96)), by(_view(d=96)), by(qz), 4096, 1 << 30, None) == 3
+    # misaligned pointer / stride
+    assert call(by(_view(ptr=18)), by(k), by(qz), 4096, 1 << 30, None) == 2
+    assert call(by(_view(st=260)), by(k), by(qz), 4096, 1 << 30, None) == 2
+    # mismatched shapes
+    assert call(by(q), by(_view(n=255)), by(qz), 4096, 1 << 30, None) == 1
+    # workspace too small / missing
+    assert call(by(q), by(k), by(qz), 4096, 16, None) == 4
+    assert call(by(q), by(k), by(qz), 0, 1 << 30, None) == 4
+    # quantised buffers misaligned
+    assert call(by(q), by(k), by(_qz(ptr=4100)), 4096, 1 << 30, None) == 2
+    # fused path: bad out stride, bad scale, small workspace
+    assert L.sage_attn_fwd(by(q), by(k), by(v), 0.1, 4096, 250, 128, 4096, 1 << 34, None) == 2
+    assert L.sage_attn_fwd(by(q), by(k), by(v), -1.0, 4096, 256, 128, 4096, 1 << 34, None) == 1
+    assert L.sage_attn_fwd(by(q), by(k), by(v), 0.1, 4096, 256, 128, 4096, 1024, None) == 4
+    assert L.sage_attn_fwd(by(q), by(k), by(v), 0.1, 4096, 256, 128, 4100, 1 << 34, None) == 2
+    assert L.sage_attn_fwd_quantized(256, 2, 128, by(qz), 0.1, 4096, 256, 128, 0, None) == 1
+    assert L.sage_attn_dense_bf16(by(q), by(k), by(_view(h=3)), 0.1, 4096, 256, 128, None) == 1
+    # debug tiles outside N_pad
+    assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 0, 128, 0, 2, 1, 4096, 4096, None) == 1
+    assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 2, 0, 0, 1, 1, 4096, 4096, None) == 1
+    assert L.sage_check_device_status(0, None, None) == 1

@@ -1,0 +1,219 @@
+"""ctypes binding of `libsage_gb300.so` (include/sage.h): argument marshalling only.
+
+Every step of the attention path runs in the library's CUDA kernels; this module only turns
+torch tensors into pointers, sizes and strides, allocates outputs and workspaces with
+torch, and raises `SageError` on a non-OK status.  There is no fallback: if the library is
+missing the import of any op raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsage_gb300.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "sage.h")
+
+STATUS = {0: "SAGE_OK", 1: "SAGE_ERR_INVALID_ARG", 2: "SAGE_ERR_ALIGNMENT", 3: "SAGE_ERR_UNSUPPORTED",
+          4: "SAGE_ERR_WORKSPACE", 5: "SAGE_ERR_CUDA", 6: "SAGE_ERR_DEVICE_TIMEOUT"}
+
+
+class SageError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+class SageView(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("n_tokens", ctypes.c_int64), ("n_heads", ctypes.c_int64),
+                ("head_dim", ctypes.c_int64), ("stride_token", ctypes.c_int64),
+                ("stride_head", ctypes.c_int64)]
+
+
+class SageQuantizedC(ctypes.Structure):
+    _fields_ = [("q_codes", ctypes.c_void_p), ("q_scales", ctypes.c_void_p), ("k_codes", ctypes.c_void_p),
+                ("k_scales", ctypes.c_void_p), ("k_mean", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def header_functions() -> list:
+    """Names of the functions include/sage.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\**\s+\**(sage_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() (no CPU fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        VP = ctypes.POINTER(SageView)
+        QP = ctypes.POINTER(SageQuantizedC)
+        sig = {
+            "sage_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "sage_quant_scratch_bytes": ([I, I, I], S),
+            "sage_workspace_bytes": ([I, I, I], S),
+            "sage_status_block_bytes": ([], S),
+            "sage_smooth_quant_qk": ([VP, VP, QP, P, S, P], ctypes.c_int),
+            "sage_quant_v": ([VP, QP, P, S, P], ctypes.c_int),
+            "sage_attn_fwd_quantized": ([I, I, I, QP, F, P, I, I, P, P], ctypes.c_int),
+            "sage_attn_fwd": ([VP, VP, VP, F, P, I, I, P, S, P], ctypes.c_int),
+            "sage_attn_dense_bf16": ([VP, VP, VP, F, P, I, I, P], ctypes.c_int),
+            "sage_debug_qk_int32": ([I, I, I, QP, I, I, I, I, I, P, P, P], ctypes.c_int),
+            "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise SageError(code, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_view(t: torch.Tensor) -> SageView:
+    """A bf16 CUDA [N, H, D] tensor (any token / head strides, unit channel stride)."""
+    if t.dim() != 3 or t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(2) != 1:
+        raise ValueError("expected a bf16 CUDA [N, H, D] tensor with unit channel stride")
+    n, h, d = t.shape
+    return SageView(t.data_ptr(), n, h, d, t.stride(0), t.stride(1))
+
+
+def pad128(n: int) -> int:
+    return (n + 127) // 128 * 128
+
+
+class Quantized:
+    """Device buffers of the quantised operands (layouts of sage_quantized in include/sage.h)."""
+
+    def __init__(self, n: int, h: int, d: int, device="cuda"):
+        np_ = pad128(n)
+        self.n, self.h, self.d = n, h, d
+        self.q_codes = torch.empty((h, np_, d), dtype=torch.float16, device=device)
+        self.k_codes = torch.empty((h, np_, d), dtype=torch.float16, device=device)
+        self.v_codes = torch.empty((h, d, np_), dtype=torch.uint8, device=device)
+        self.q_scales = torch.empty((h, np_ // 128), dtype=torch.float32, device=device)
+        self.k_scales = torch.empty((h, np_ // 64), dtype=torch.float32, device=device)
+        self.k_mean = torch.empty((h, d), dtype=torch.float32, device=device)
+        self.v_scales = torch.empty((h, d), dtype=torch.float32, device=device)
+
+    def c(self) -> SageQuantizedC:
+        return SageQuantizedC(self.q_codes.data_ptr(), self.q_scales.data_ptr(), self.k_codes.data_ptr(),
+                              self.k_scales.data_ptr(), self.k_mean.data_ptr(), self.v_codes.data_ptr(),
+                              self.v_scales.data_ptr())
+
+
+def quant_scratch(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
+    return torch.empty(int(lib().sage_quant_scratch_bytes(n, h, d)), dtype=torch.uint8, device=device)
+
+
+def status_block(device="cuda") -> torch.Tensor:
+    return torch.zeros(int(lib().sage_status_block_bytes()), dtype=torch.uint8, device=device)
+
+
+def workspace(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
+    """Workspace for sage_attn_fwd; its leading status block starts zeroed."""
+    ws = torch.empty(int(lib().sage_workspace_bytes(n, h, d)) + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + int(lib().sage_workspace_bytes(n, h, d))]
+    ws[:256].zero_()
+    return ws
+
+
+def sage_smooth_quant_qk(q: torch.Tensor, k: torch.Tensor, qz: Optional[Quantized] = None,
+                         scratch: Optional[torch.Tensor] = None, stream=None) -> Quantized:
+    n, h, d = q.shape
+    qz = qz or Quantized(n, h, d, q.device)
+    scratch = scratch if scratch is not None else quant_scratch(n, h, d, q.device)
+    vq, vk, c = make_view(q), make_view(k), qz.c()
+    _check(lib().sage_smooth_quant_qk(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(c), scratch.data_ptr(),
+                                      scratch.numel(), _stream(stream)), "sage_smooth_quant_qk")
+    return qz
+
+
+def sage_quant_v(v: torch.Tensor, qz: Quantized, scratch: Optional[torch.Tensor] = None, stream=None) -> Quantized:
+    n, h, d = v.shape
+    scratch = scratch if scratch is not None else quant_scratch(n, h, d, v.device)
+    vv, c = make_view(v), qz.c()
+    _check(lib().sage_quant_v(ctypes.byref(vv), ctypes.byref(c), scratch.data_ptr(), scratch.numel(),
+                              _stream(stream)), "sage_quant_v")
+    return qz
+
+
+def _out_args(out: Optional[torch.Tensor], n: int, h: int, d: int, device):
+    if out is None:
+        out = torch.empty((n, h, d), dtype=torch.bfloat16, device=device)
+    if out.dtype != torch.bfloat16 or out.stride(2) != 1 or tuple(out.shape) != (n, h, d):
+        raise ValueError("out must be bf16 [N, H, D] with unit channel stride")
+    return out, out.stride(0), out.stride(1)
+
+
+def sage_attn_fwd_quantized(qz: Quantized, sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                            status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    sm_scale = 1.0 / math.sqrt(qz.d) if sm_scale is None else sm_scale
+    out, ost, osh = _out_args(out, qz.n, qz.h, qz.d, qz.q_codes.device)
+    status = status if status is not None else status_block(qz.q_codes.device)
+    c = qz.c()
+    _check(lib().sage_attn_fwd_quantized(qz.n, qz.h, qz.d, ctypes.byref(c), sm_scale, out.data_ptr(), ost, osh,
+                                         status.data_ptr(), _stream(stream)), "sage_attn_fwd_quantized")
+    return out
+
+
+def sage_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_scale: Optional[float] = None,
+                  out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    n, h, d = q.shape
+    sm_scale = 1.0 / math.sqrt(d) if sm_scale is None else sm_scale
+    out, ost, osh = _out_args(out, n, h, d, q.device)
+    ws = ws if ws is not None else workspace(n, h, d, q.device)
+    vq, vk, vv = make_view(q), make_view(k), make_view(v)
+    _check(lib().sage_attn_fwd(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), sm_scale, out.data_ptr(), ost,
+                               osh, ws.data_ptr(), ws.numel(), _stream(stream)), "sage_attn_fwd")
+    return out
+
+
+def sage_attn_dense_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_scale: Optional[float] = None,
+                         out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    n, h, d = q.shape
+    sm_scale = 1.0 / math.sqrt(d) if sm_scale is None else sm_scale
+    out, ost, osh = _out_args(out, n, h, d, q.device)
+    vq, vk, vv = make_view(q), make_view(k), make_view(v)
+    _check(lib().sage_attn_dense_bf16(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), sm_scale,
+                                      out.data_ptr(), ost, osh, _stream(stream)), "sage_attn_dense_bf16")
+    return out
+
+
+def sage_debug_qk_int32(qz: Quantized, head: int, i0: int, j0: int, row_tiles: int = 1, col_tiles: int = 1,
+                        status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    out = torch.empty((128 * row_tiles, 128 * col_tiles), dtype=torch.int32, device=qz.q_codes.device)
+    status = status if status is not None else status_block(qz.q_codes.device)
+    c = qz.c()
+    _check(lib().sage_debug_qk_int32(qz.n, qz.h, qz.d, ctypes.byref(c), head, i0, j0, row_tiles, col_tiles,
+                                     out.data_ptr(), status.data_ptr(), _stream(stream)), "sage_debug_qk_int32")
+    return out
+
+
+def sage_check_device_status(status: torch.Tensor, stream=None):
+    """Synchronises `stream`; returns (status code, where) and clears a recorded timeout."""
+    where = ctypes.c_int32(0)
+    code = lib().sage_check_device_status(status.data_ptr(), _stream(stream), ctypes.byref(where))
+    return int(code), int(where.value)

@@ -1,0 +1,537 @@
+// attn_fwd.cu -- fused quantised attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// Computes the attention_forward stage of the Sage2 call profiled in
+// "gb10-sampling-component-profile-1344x768-124f-seed440420.json"
+// (attention_internal_p50_milliseconds.sage2.attention_forward) on operands made by
+// quant.cu: S = exact integer QK^T (INT8 codes held in fp16, kind::f16 MMA, fp32
+// accumulator), an fp32 online softmax on S * s_q * s_k * sm_scale, P = E4M3(448 p) kept in
+// tensor memory, O += P.V with E4M3 V (kind::f8f6f4 MMA, fp32 accumulator), and a bf16
+// epilogue O * s_v / l.  The pages' kernel (an sm_89 build, cta_q 128 / cta_k 64 / 128
+// threads per CTA; "gb10-sage2-p0-interleave-softmax-latency.json", key scheduler) is prior
+// art only: this kernel is organised around Blackwell's tensor memory instead.
+//
+// CTA = 256 query rows of one head (two 128-row tiles t = 0, 1) and every 128-key tile of
+// that head.  Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K/V tiles into a kStages-deep ring
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T, O_t += P_t V
+//   warp 2      TMEM allocator
+//   warps 4-7   softmax + epilogue of tile 0 (thread = row = TMEM lane)
+//   warps 8-11  softmax + epilogue of tile 1
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [256+D, 256+2D).
+// P_t (E4M3, 4 keys per 32-bit column) overwrites columns [0,32) of S_t and is the A
+// operand of the P.V MMA straight from TMEM.
+//
+// Online softmax with P in E4M3: P is encoded against the current running max, so p <= 1
+// and 448 p never overflows; whenever a row's max rises, O and l of that row are
+// multiplied by exp2(m_old - m_new) before the next P.V is issued (an exact rescale on
+// every increase).
+//
+// Every mbarrier wait is bounded (global-timer limit); on expiry the thread records the
+// wait in the status block, raises the CTA's abort flag and every role unwinds to the
+// common exit, which frees the tensor memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "sage_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace sage {
+namespace {
+
+constexpr int kBM = 128;   // query rows per tile
+constexpr int kBN = 128;   // keys per tile
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLog2_448 = 8.807354922057604f;     // log2(448): P is encoded as E4M3(448 p)
+
+template <int D>
+struct Cfg {
+  static constexpr int kPanels = D / 64;                 // 128-byte swizzle panels per fp16 row
+  static constexpr int kPanelBytes = 128 * 128;          // 128 rows x 128 B
+  static constexpr int kQTileBytes = kBM * D * 2;
+  static constexpr int kKTileBytes = kBN * D * 2;
+  static constexpr int kVTileBytes = D * kBN;
+  static constexpr int kStageBytes = kKTileBytes + kVTileBytes;
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+  static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
+};
+
+struct AttnParams {
+  int n, npad, h;
+  const float* q_scales;   // [H][npad/128]
+  const float* k_scales;   // [H][npad/64]
+  const float* v_scales;   // [H][D]
+  float sm_scale_log2;     // sm_scale * log2(e)
+  uint16_t* out;           // bf16
+  int64_t ost, osh;
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void record_error(int32_t* status, int32_t where, volatile int* abort_flag) {
+  if (atomicCAS(status, 0, 1) == 0) status[1] = where;
+  *abort_flag = 1;
+}
+
+// Bounded wait usable by a whole warp: every lane waits, and the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit) {
+  bool ok = mbar_wait(bar, parity, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// S[tmem d_col] = Q_tile(sq) . K_tile(sk)^T over D channels: D/16 MMAs of 128x128x16.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
+  constexpr uint32_t idesc = idesc_f32acc(kBM, kBN);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * Cfg<D>::kPanelBytes + (kk & 3) * 32;
+    mma_f16_ss(d_tmem, sdesc_k_sw128(sq + off), sdesc_k_sw128(sk + off), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
+  constexpr uint32_t idesc = idesc_f32acc(kBM, D);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 32; ++kk)
+    mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_skip;
+  __shared__ volatile int s_abort;
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + 2 * C::kQTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + C::kStages;
+  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* mma_final = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hh = blockIdx.y;
+  const int q0 = blockIdx.x * 2 * kBM;
+  const int ntiles = p.npad / kBN;
+
+  if (threadIdx.x == 0) {
+    s_skip = *reinterpret_cast<volatile int32_t*>(p.status);
+    s_abort = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(p_full + t, 128);
+      mbar_init(pv_done + t, 1);
+    }
+    mbar_init(mma_final, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (s_skip) return;   // an earlier CTA already failed: do no work
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      const int qrow = hh * p.npad + q0;
+      mbar_arrive_expect_tx(q_full, 2 * C::kQTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_2d(sQ + t * C::kQTileBytes + pn * C::kPanelBytes, &qmap, q_full, pn * 64, qrow + t * kBM);
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages && !mbar_wait(kv_empty + s, ((j / C::kStages) - 1) & 1, limit)) {
+          record_error(p.status, kWhereKvEmpty, &s_abort);
+          break;
+        }
+        if (s_abort) break;
+        uint8_t* sk = sKV + s * C::kStageBytes;
+        mbar_arrive_expect_tx(kv_full + s, C::kStageBytes);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_2d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh * p.npad + j * kBN);
+        tma_load_2d(sk + C::kKTileBytes, &vmap, kv_full + s, j * kBN, hh * D);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t skv = smem_u32(sKV);
+      const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
+      const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
+      bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
+      if (!ok) record_error(p.status, kWhereQFull, &s_abort);
+      if (ok) {
+        tc_fence_after();
+        issue_qk<D>(colS[0], sq, skv);
+        tc_commit(s_full + 0);
+        issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
+        tc_commit(s_full + 1);
+      }
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!mbar_wait(p_full + t, j & 1, limit)) {
+            record_error(p.status, kWherePFull, &s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+          tc_commit(pv_done + t);
+          if (t == 1) tc_commit(kv_empty + s);
+          if (j + 1 < ntiles) {
+            if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+              record_error(p.status, kWhereKvFull, &s_abort);
+              ok = false;
+              break;
+            }
+            // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
+            if (!mbar_wait(pv_done + t, j & 1, limit)) {
+              record_error(p.status, kWherePvDone, &s_abort);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+            tc_commit(s_full + t);
+          }
+        }
+        if (s_abort) ok = false;
+      }
+      // Drain: every MMA issued above has finished before the CTA frees its tensor memory.
+      tc_commit(mma_final);
+      mbar_wait(mma_final, 0, limit);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;                     // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;                // row within the tile = TMEM lane
+    const int row = q0 + t * kBM + r;            // query row
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
+    const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
+    const int nbq = p.npad / 128, nbk = p.npad / 64;
+    const int qblk = (q0 + t * kBM) / 128;
+    const float qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
+    const float cq = qscale * p.sm_scale_log2;
+    const float* ks = p.k_scales + hh * nbk;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      if (!warp_wait(s_full + t, j & 1, limit)) {
+        if (lane == 0) record_error(p.status, kWhereSFull, &s_abort);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      SAGE_TMEM_LD32(tS + 0, (sr + 0));
+      SAGE_TMEM_LD32(tS + 32, (sr + 32));
+      SAGE_TMEM_LD32(tS + 64, (sr + 64));
+      SAGE_TMEM_LD32(tS + 96, (sr + 96));
+      tmem_wait_ld();
+      const float c0 = cq * ks[2 * j], c1 = cq * ks[2 * j + 1];
+      const int kvalid = min(kBN, p.n - j * kBN);
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (kvalid == kBN) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
+#pragma unroll
+        for (int k = 64; k < 128; ++k) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k < kvalid) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
+#pragma unroll
+        for (int k = 64; k < 128; ++k)
+          if (k < kvalid) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
+      }
+      // c >= 0 and rounding is monotone, so max_k fl(S_k c) = fl(c max_k S_k).  fmaxf drops
+      // the NaN of (-inf) * 0 for an empty half.
+      const float mt = fmaxf(mx0 * c0, mx1 * c1);
+      const float m_new = fmaxf(m, mt);
+      const bool rise = (j > 0) && (m_new > m);
+      if (__any_sync(0xffffffffu, rise)) {
+        const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
+        l *= alpha;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          SAGE_TMEM_LD32(tO + c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          SAGE_TMEM_ST32(tO + c, o);
+        }
+        tmem_wait_st();
+      }
+      m = m_new;
+      const float bias = kLog2_448 - m;
+      float lsum = 0.0f;
+#pragma unroll
+      for (int cch = 0; cch < 4; ++cch) {
+        const float cb = cch < 2 ? c0 : c1;
+        uint32_t pw[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          float pp[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int k = cch * 32 + w * 4 + u;
+            pp[u] = ex2_approx(fmaf(__uint_as_float(sr[k]), cb, bias));
+            if (kvalid < kBN && k >= kvalid) pp[u] = 0.0f;
+            lsum += pp[u];
+          }
+          pw[w] = e4m3x2(pp[0], pp[1]) | (e4m3x2(pp[2], pp[3]) << 16);
+        }
+        SAGE_TMEM_ST8(tS + cch * 8, pw);
+      }
+      l += lsum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + t);
+    }
+    if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const float* vs = p.v_scales + hh * D;
+      uint16_t* orow = p.out + static_cast<int64_t>(row) * p.ost + static_cast<int64_t>(hh) * p.osh;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        SAGE_TMEM_LD32(tO + c, o);
+        tmem_wait_ld();
+        if (row < p.n) {
+#pragma unroll
+          for (int v8 = 0; v8 < 4; ++v8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int k = v8 * 8 + u * 2;
+              const float a = __uint_as_float(o[k]) * vs[c + k] * inv_l;
+              const float b = __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
+              w[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+            }
+            *reinterpret_cast<uint4*>(orow + c + v8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    } else if (ok) {
+      if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------------- debug: S tiles
+// One CTA per (128-row, 128-key) tile: the same TMA loads and issue_qk as the fused kernel,
+// then S is read back from TMEM and written as int32.
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    debug_qk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, int npad,
+                    int head, int i0, int j0, int32_t* out, int ldo, int32_t* status, uint64_t limit) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ volatile int s_abort;
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint64_t bar_tma, bar_mma;
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::kQTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int qrow = head * npad + i0 + blockIdx.x * kBM;
+  const int krow = head * npad + j0 + blockIdx.y * kBN;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar_tma, C::kQTileBytes + C::kKTileBytes);
+    for (int pn = 0; pn < C::kPanels; ++pn) {
+      tma_load_2d(sQ + pn * C::kPanelBytes, &qmap, &bar_tma, pn * 64, qrow);
+      tma_load_2d(sK + pn * C::kPanelBytes, &kmap, &bar_tma, pn * 64, krow);
+    }
+    if (mbar_wait(&bar_tma, 0, limit)) {
+      tc_fence_after();
+      issue_qk<D>(tmem, smem_u32(sQ), smem_u32(sK));
+    } else {
+      record_error(status, kWhereDebugTma, &s_abort);
+    }
+    tc_commit(&bar_mma);
+  }
+  __syncwarp();
+  if (warp_wait(&bar_mma, 0, limit)) {
+    tc_fence_after();
+    const int r = warp * 32 + lane;
+    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    int32_t* orow = out + static_cast<int64_t>(blockIdx.x * kBM + r) * ldo + blockIdx.y * kBN;
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+      SAGE_TMEM_LD32(ta + c, v);
+      tmem_wait_ld();
+      if (!s_abort)
+        for (int k = 0; k < 32; ++k) orow[c + k] = __float2int_rn(__uint_as_float(v[k]));
+    }
+  } else if (lane == 0) {
+    record_error(status, kWhereDebugMma, &s_abort);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major [rows][inner] matrix, 128-byte swizzled boxes of box_rows x box_inner elements.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+              uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * elem_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, float sm_scale, void* out, int64_t ost,
+                              int64_t osh, int32_t* status, cudaStream_t s) {
+  using C = Cfg<D>;
+  const int npad = static_cast<int>(pad128(n));
+  CUtensorMap qmap, kmap, vmap;
+  if (!make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.q_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||
+      !make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.k_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||
+      !make_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qz.v_codes, npad, static_cast<uint64_t>(h) * D, 128, D))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  AttnParams p;
+  p.n = n;
+  p.npad = npad;
+  p.h = h;
+  p.q_scales = qz.q_scales;
+  p.k_scales = qz.k_scales;
+  p.v_scales = qz.v_scales;
+  p.sm_scale_log2 = sm_scale * kLog2e;
+  p.out = static_cast<uint16_t*>(out);
+  p.ost = ost;
+  p.osh = osh;
+  p.status = status;
+  p.wait_limit_ns = kWaitLimitNs;
+  dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
+  attn_fwd_kernel<D><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_debug_qk_t(int n, int h, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
+                              int col_tiles, int32_t* out, int32_t* status, cudaStream_t s) {
+  using C = Cfg<D>;
+  const int npad = static_cast<int>(pad128(n));
+  CUtensorMap qmap, kmap;
+  if (!make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.q_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||
+      !make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.k_codes, D, static_cast<uint64_t>(h) * npad, 64, 128))
+    return cudaErrorInvalidValue;
+  const int smem = C::kQTileBytes + C::kKTileBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(debug_qk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  debug_qk_kernel<D><<<dim3(row_tiles, col_tiles), 128, smem, s>>>(qmap, kmap, npad, head, i0, j0, out,
+                                                                    col_tiles * kBN, status, kWaitLimitNs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, float sm_scale, void* out, int64_t ost,
+                            int64_t osh, int32_t* status, cudaStream_t s) {
+  return d == 128 ? launch_attn_fwd_t<128>(n, h, qz, sm_scale, out, ost, osh, status, s)
+                  : launch_attn_fwd_t<64>(n, h, qz, sm_scale, out, ost, osh, status, s);
+}
+
+cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
+                            int col_tiles, int32_t* out, int32_t* status, cudaStream_t s) {
+  return d == 128 ? launch_debug_qk_t<128>(n, h, qz, head, i0, j0, row_tiles, col_tiles, out, status, s)
+                  : launch_debug_qk_t<64>(n, h, qz, head, i0, j0, row_tiles, col_tiles, out, status, s);
+}
+
+}  // namespace sage

@@ -1,0 +1,52 @@
+// sage_internal.h -- launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/sage.h"
+
+namespace sage {
+
+// Device-side status codes recorded in the status block (first int32: nonzero on error,
+// second int32: where the error was detected).
+enum DeviceWhere : int32_t {
+  kWhereNone = 0,
+  kWhereQFull = 1,
+  kWhereKvFull = 2,
+  kWhereKvEmpty = 3,
+  kWhereSFull = 4,
+  kWherePFull = 5,
+  kWherePvDone = 6,
+  kWhereDebugTma = 7,
+  kWhereDebugMma = 8,
+};
+
+struct StridedView {
+  const uint16_t* data;  // bf16 bits
+  int64_t st, sh;        // token and head strides in elements
+};
+
+inline int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
+
+// quant.cu
+cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, float* partials,
+                             cudaStream_t s);
+cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, bool absmax, float* out,
+                            cudaStream_t s);
+cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
+                            uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
+                            cudaStream_t s);
+cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, int h, int d, uint8_t* v_codes,
+                           cudaStream_t s);
+
+// attn_fwd.cu
+cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, float sm_scale, void* out, int64_t ost,
+                            int64_t osh, int32_t* status, cudaStream_t s);
+cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
+                            int col_tiles, int32_t* out, int32_t* status, cudaStream_t s);
+
+// attn_dense.cu
+cudaError_t launch_attn_dense(const StridedView& q, const StridedView& k, const StridedView& v, int n, int h,
+                              int d, float sm_scale, void* out, int64_t ost, int64_t osh, cudaStream_t s);
+
+}  // namespace sage
