@@ -1,0 +1,336 @@
+"""Benchmark of the quantised attention path on the pages' workload.
+
+One step = one full attention call (K mean, Q/K INT8 quantisation, V E4M3 quantisation,
+fused attention) over N=37810 packed tokens, H=56 heads, D=128, read as strided NHD views
+of a token-major [37810, 21504] bf16 QKV buffer (synthetic, seeded; the workload of the
+Sage2 call in "gb10-sage2-p0-interleave-softmax-latency.json", key q_shape).
+Metric: attention TFLOPS = 4 N^2 H D / time per call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (the only other implementation of this path) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "video"
+METRIC = "attention TFLOPS (4*N^2*H*D/time) and ms/call at N=37810,H=56,D=128 on 1 GB300"
+UNIT = "TFLOP/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+ATTN_SRC = os.path.join(ROOT, "video_diffusion_transformer_sage_gb300", "csrc", "attn_fwd.cu")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return m["bf16_tflops"], m["bf16_tflops_sustained"], m["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _traffic_per_launch():
+    """dram bytes per launch of the attention kernel from the committed ncu capture, or None
+    when the kernel source changed since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        src = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()
+        if t.get("attn_fwd_cu_sha256") != src:
+            return None
+        return t["bytes_per_launch_full_size"]
+    except Exception:
+        return None
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_gpu(args):
+    import torch
+    import video_diffusion_transformer_sage_gb300 as sage
+    from video_diffusion_transformer_sage_gb300 import build as sbuild, synth
+
+    world, rank, local = _dist()
+    sbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+
+    w = synth.WORKLOADS[args.workload]
+    n, h, d = w.n_tokens, w.n_heads, w.head_dim
+    inp = synth.make_inputs(w)
+    if w.layout != "qkv":
+        raise SystemExit("bench.py times strided views of a token-major QKV buffer")
+    host = inp.storage.pin_memory()
+    storage = host.to(dev)
+    hd = h * d
+
+    def views(buf):
+        return [buf[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3)]
+
+    q, k, v = views(storage)
+    sm_scale = 1.0 / math.sqrt(d)
+    qz = sage.Quantized(n, h, d, dev)
+    scratch = sage.quant_scratch(n, h, d, dev)
+    status = sage.status_block(dev)
+    out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 7   # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, attention
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sage.sage_smooth_quant_qk(q, k, qz, scratch, stream)
+        sage.sage_quant_v(v, qz, scratch, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        sage.sage_attn_fwd_quantized(qz, sm_scale, out, status, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    code, where = sage.sage_check_device_status(status, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at {where}")
+    total_ms = t0.elapsed_time(t1)
+    quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if pg:
+        tt = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    flops = w.flops
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers: pinned H2D of the QKV buffer,
+    # the whole path, D2H of the output, every step.
+    host_out = torch.empty((n, h, d), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 5))
+    ws = sage.workspace(n, h, d, dev)
+    storage2 = torch.empty_like(storage)
+    q2, k2, v2 = views(storage2)
+
+    def e2e_step():
+        storage2.copy_(host, non_blocking=True)
+        sage.sage_attn_fwd(q2, k2, v2, sm_scale, out, ws, stream)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_ms = float("nan")
+    if e2e_steps:
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+    if pg:
+        tt = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    bf16_burst, bf16_sus, hbm, peak_src = _peaks()
+    # The fused kernel does half its FLOPs as fp16 MMAs (QK^T on INT8 codes held in fp16)
+    # and half as E4M3 MMAs (PV); the E4M3 rate is twice the 16-bit rate.  Its roofline is
+    # the time of both halves at their own peaks (sustained: the kernel runs inside a long loop).
+    p16, p8 = bf16_sus, 2 * bf16_sus
+    composite = 1.0 / (0.5 / p16 + 0.5 / p8)
+    attn_avg = statistics.mean(attn_ms)
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    traffic = _traffic_per_launch()
+    quant_avg = statistics.mean(quant_ms)
+    quant_bytes = 13 * n * h * d
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16(int8 codes)xfp16 + e4m3xe4m3 -> fp32, bf16 io",
+        "data": "synthetic (seeded, distributions of the pages' workload)",
+        "config": {"workload": f"{w.name}: N={n}, H={h}, D={d}, batch 1, non-causal, "
+                               f"strided NHD views of a [{n}, {3 * h * d}] bf16 QKV buffer",
+                   "l2": "inputs larger than L2 (1.63 GB QKV buffer)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(composite, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / composite, 4), "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<128>",
+                     "peak_note": f"composite of {peak_src} sustained bf16 {p16} (QK^T) and 2x for E4M3 (PV)",
+                     "frac_of_e4m3_peak": round(achieved / p8, 4)},
+        "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
+                       "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
+                       "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(host.numel() * 2), "d2h_bytes_per_step": int(host_out.numel() * 2),
+                "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def cpu_baseline(inp, budget_s: float = 20.0, rows_per_step: int = 8, steps: int = 0):
+    """The oracle as it stands on the host cores: quantisation (steps 1-4) in full, then
+    same-quantisation attention for sampled query rows (all heads) until `budget_s` is spent;
+    time per call extrapolated as t_quant + N * t_row."""
+    import oracle
+    w = inp.workload
+    n, h, d = w.n_tokens, w.n_heads, w.head_dim
+    t = time.perf_counter()
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    t_quant = time.perf_counter() - t
+    from video_diffusion_transformer_sage_gb300 import synth
+    pool = synth.sample_rows(n, 4096, 17)
+    done, t_attn, i = 0, 0.0, 0
+    while (steps and i < steps) or (not steps and (t_attn < budget_s or done == 0)):
+        rows = [pool[(i * rows_per_step + r) % len(pool)] for r in range(rows_per_step)]
+        t = time.perf_counter()
+        oracle.attn_sq(qz, 1.0 / math.sqrt(d), rows, tile=128)
+        t_attn += time.perf_counter() - t
+        done += rows_per_step
+        i += 1
+    t_row = t_attn / done
+    t_call = t_quant + n * t_row
+    return {"value": round(w.flops / t_call / 1e12, 5), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"quantisation in full ({t_quant:.1f} s); attention for {done} sampled query "
+                                        f"rows x {h} heads ({t_attn:.1f} s); call time extrapolated "
+                                        f"t_quant + N*t_row = {t_call:.0f} s",
+            "host_cores": os.cpu_count()}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the same workload, K timed steps of sampled rows."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from video_diffusion_transformer_sage_gb300 import synth
+    oracle.build()
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w)
+    rows_per_step = 4
+    cb = cpu_baseline(inp, rows_per_step=rows_per_step, steps=args.warmup + args.steps)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+            "config": {"workload": f"{w.name}: N={w.n_tokens}, H={w.n_heads}, D={w.head_dim}, batch 1, non-causal, "
+                                   f"strided NHD views of a [{w.n_tokens}, {3 * w.n_heads * w.head_dim}] bf16 QKV buffer"},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": cb["value"],
+                             "unit": UNIT},
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS with qkv layout")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

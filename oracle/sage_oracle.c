@@ -96,6 +96,7 @@ uint8_t oracle_e4m3_encode(double x) {
 void oracle_k_mean(const uint16_t* k, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
                    float* mu) {
   int64_t nchunk = (n + 127) / 128;
+#pragma omp parallel for collapse(2) schedule(static)
   for (int64_t hh = 0; hh < h; ++hh) {
     for (int64_t c = 0; c < d; ++c) {
       double total = 0.0;
@@ -139,16 +140,17 @@ static float quant_block_i8(const float* x, int64_t rows, int64_t d, int8_t* cod
 void oracle_quant_q(const uint16_t* q, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
                     int8_t* codes, float* scales) {
   int64_t np = pad128(n), nb = np / 128;
-  float* buf = (float*)malloc(sizeof(float) * 128 * d);
   memset(codes, 0, (size_t)(h * np * d));
+#pragma omp parallel for collapse(2) schedule(static)
   for (int64_t hh = 0; hh < h; ++hh)
     for (int64_t b = 0; b < nb; ++b) {
+      float* buf = (float*)malloc(sizeof(float) * 128 * d);
       int64_t r0 = b * 128, r1 = r0 + 128 < n ? r0 + 128 : n;
       for (int64_t t = r0; t < r1; ++t)
         for (int64_t c = 0; c < d; ++c) buf[(t - r0) * d + c] = bf16_to_f32(q[t * st + hh * sh + c]);
       scales[hh * nb + b] = quant_block_i8(buf, r1 - r0, d, codes + (hh * np + r0) * d);
+      free(buf);
     }
-  free(buf);
 }
 
 /* 3. K smoothing then quantisation: K~ = fl32(K - mu) (one fp32 subtraction), one scale per
@@ -156,20 +158,21 @@ void oracle_quant_q(const uint16_t* q, int64_t n, int64_t h, int64_t d, int64_t 
 void oracle_quant_k(const uint16_t* k, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
                     const float* mu, int8_t* codes, float* scales) {
   int64_t np = pad128(n), nb = np / 64;
-  float* buf = (float*)malloc(sizeof(float) * 64 * d);
   memset(codes, 0, (size_t)(h * np * d));
+#pragma omp parallel for collapse(2) schedule(static)
   for (int64_t hh = 0; hh < h; ++hh)
     for (int64_t b = 0; b < nb; ++b) {
       int64_t r0 = b * 64, r1 = r0 + 64 < n ? r0 + 64 : n;
       if (r1 <= r0) { scales[hh * nb + b] = 0.0f; continue; }
+      float* buf = (float*)malloc(sizeof(float) * 64 * d);
       for (int64_t t = r0; t < r1; ++t)
         for (int64_t c = 0; c < d; ++c) {
           float m = (g_mutation == MUT_NO_SMOOTH) ? 0.0f : mu[hh * d + c];
           buf[(t - r0) * d + c] = bf16_to_f32(k[t * st + hh * sh + c]) - m;
         }
       scales[hh * nb + b] = quant_block_i8(buf, r1 - r0, d, codes + (hh * np + r0) * d);
+      free(buf);
     }
-  free(buf);
 }
 
 /* 4. V: one scale per (head, channel), scale = fl32(amax over tokens / 448), code =
@@ -178,6 +181,7 @@ void oracle_quant_v(const uint16_t* v, int64_t n, int64_t h, int64_t d, int64_t 
                     uint8_t* codes, float* scales) {
   int64_t np = pad128(n);
   memset(codes, 0, (size_t)(h * d * np));
+#pragma omp parallel for collapse(2) schedule(static)
   for (int64_t hh = 0; hh < h; ++hh)
     for (int64_t c = 0; c < d; ++c) {
       float amax = 0.0f;
