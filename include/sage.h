@@ -115,6 +115,25 @@ size_t sage_status_block_bytes(void);
 sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const sage_quantized* qz,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* Same computation and outputs as sage_smooth_quant_qk, for callers that cannot allocate
+ * device memory: plugin or custom-operator interfaces that receive only their input and
+ * output buffers from a host framework owning all device memory, and code that must not call
+ * cudaMalloc / cudaFree because those calls can synchronise the whole device.  The pages
+ * have no counterpart; it exists for such callers only.
+ *   - Scratch comes from a fixed 16 MiB array (4,194,304 floats) in the library's own device
+ *     memory, which every GPU that loads the library holds until the process exits.  Nothing
+ *     is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Limit: ceil(n_tokens / 128) * n_heads * head_dim <= 4,194,304 (the pages' call uses
+ *     2,121,728).  Larger problems return SAGE_ERR_WORKSPACE and nothing is launched.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture begins.
+ *   - Every call on a device uses the same array, so calls that can overlap on the GPU (other
+ *     streams, other host threads) race: serialise them.  No element needs to start at zero:
+ *     each call writes every scratch element it reads.
+ * Errors and argument checks as for sage_smooth_quant_qk. */
+sage_status sage_smooth_quant_qk_noalloc(const sage_view* q, const sage_view* k, const sage_quantized* qz,
+                                         void* stream);
+
 /* FP8 E4M3 quantisation of V (the pages' v_quantize stage): per (h, c) scale =
  * fl32(max_t |v| / 448), code = E4M3 round-to-nearest-even, saturating, of fl32(v / scale);
  * an all-zero channel has scale 0 and codes 0.  Writes qz->v_codes (transposed to

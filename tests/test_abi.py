@@ -10,7 +10,8 @@ from video_diffusion_transformer_sage_gb300 import _lib
 
 EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_bytes", "sage_status_block_bytes",
             "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
-            "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status"}
+            "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
+            "sage_smooth_quant_qk_noalloc"}
 
 
 @pytest.fixture(scope="module")

@@ -66,6 +66,7 @@ def lib():
             "sage_status_block_bytes": ([], S),
             "sage_smooth_quant_qk": ([VP, VP, QP, P, S, P], ctypes.c_int),
             "sage_quant_v": ([VP, QP, P, S, P], ctypes.c_int),
+            "sage_smooth_quant_qk_noalloc": ([VP, VP, QP, P], ctypes.c_int),
             "sage_attn_fwd_quantized": ([I, I, I, QP, F, P, I, I, P, P], ctypes.c_int),
             "sage_attn_fwd": ([VP, VP, VP, F, P, I, I, P, S, P], ctypes.c_int),
             "sage_attn_dense_bf16": ([VP, VP, VP, F, P, I, I, P], ctypes.c_int),
@@ -148,6 +149,18 @@ def sage_smooth_quant_qk(q: torch.Tensor, k: torch.Tensor, qz: Optional[Quantize
     vq, vk, c = make_view(q), make_view(k), qz.c()
     _check(lib().sage_smooth_quant_qk(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(c), scratch.data_ptr(),
                                       scratch.numel(), _stream(stream)), "sage_smooth_quant_qk")
+    return qz
+
+
+def sage_smooth_quant_qk_noalloc(q: torch.Tensor, k: torch.Tensor, qz: Optional[Quantized] = None,
+                                 stream=None) -> Quantized:
+    """sage_smooth_quant_qk for callers that cannot allocate: the library's fixed device
+    scratch array replaces the caller workspace (see include/sage.h for the size limit)."""
+    n, h, d = q.shape
+    qz = qz or Quantized(n, h, d, q.device)
+    vq, vk, c = make_view(q), make_view(k), qz.c()
+    _check(lib().sage_smooth_quant_qk_noalloc(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(c), _stream(stream)),
+           "sage_smooth_quant_qk_noalloc")
     return qz
 
 
