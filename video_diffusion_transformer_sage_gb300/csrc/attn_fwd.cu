@@ -87,6 +87,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// Max of 64 consecutive fp32 values (as bits), four independent 3-input chains.
+__device__ __forceinline__ float block_max64(const uint32_t* s) {
+  float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]), c = __uint_as_float(s[2]),
+        d = __uint_as_float(s[3]);
+#pragma unroll
+  for (int k = 4; k < 64; k += 8) {
+    a = fmax3(a, __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
+    b = fmax3(b, __uint_as_float(s[k + 2]), __uint_as_float(s[k + 3]));
+    c = fmax3(c, __uint_as_float(s[k + 4]), __uint_as_float(s[k + 5]));
+    d = fmax3(d, __uint_as_float(s[k + 6]), __uint_as_float(s[k + 7]));
+  }
+  return fmaxf(fmax3(a, b, c), d);
+}
+
 // S[tmem d_col] = Q_tile(sq) . K_tile(sk)^T over D channels: D/16 MMAs of 128x128x16.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
@@ -253,8 +267,14 @@ __global__ void __launch_bounds__(384, 1)
     const float cq = qscale * p.sm_scale_log2;
     const float* ks = p.k_scales + hh * nbk;
     float m = -INFINITY, l = 0.0f;
+    float ksn0 = ks[0], ksn1 = ks[1];   // k scales of the next tile, loaded one tile ahead
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
+      const float ks0 = ksn0, ks1 = ksn1;
+      if (j + 1 < ntiles) {
+        ksn0 = ks[2 * j + 2];
+        ksn1 = ks[2 * j + 3];
+      }
       if (!warp_wait(s_full + t, j & 1, limit)) {
         if (lane == 0) record_error(p.status, kWhereSFull, &s_abort);
         ok = false;
@@ -267,15 +287,15 @@ __global__ void __launch_bounds__(384, 1)
       SAGE_TMEM_LD32(tS + 64, (sr + 64));
       SAGE_TMEM_LD32(tS + 96, (sr + 96));
       tmem_wait_ld();
-      const float c0 = cq * ks[2 * j], c1 = cq * ks[2 * j + 1];
+      const float c0 = cq * ks0, c1 = cq * ks1;
       const int kvalid = min(kBN, p.n - j * kBN);
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      if (kvalid == kBN) {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
-#pragma unroll
-        for (int k = 64; k < 128; ++k) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
+      const bool tail = kvalid < kBN;
+      float mx0, mx1;
+      if (!tail) {
+        mx0 = block_max64(sr);
+        mx1 = block_max64(sr + 64);
       } else {
+        mx0 = mx1 = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 64; ++k)
           if (k < kvalid) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
@@ -291,39 +311,53 @@ __global__ void __launch_bounds__(384, 1)
       if (__any_sync(0xffffffffu, rise)) {
         const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
         l *= alpha;
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
           SAGE_TMEM_LD32(tO + c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          for (int k = 0; k < 32; k += 2) {
+            float lo, hi;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), lo, hi);
+            o[k] = __float_as_uint(lo);
+            o[k + 1] = __float_as_uint(hi);
+          }
           SAGE_TMEM_ST32(tO + c, o);
         }
         tmem_wait_st();
       }
       m = m_new;
-      const float bias = kLog2_448 - m;
-      float lsum = 0.0f;
+      // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
+      const uint64_t bias2 = f2_pack(kLog2_448 - m, kLog2_448 - m);
+      uint64_t l2 = f2_pack(0.0f, 0.0f);
 #pragma unroll
       for (int cch = 0; cch < 4; ++cch) {
         const float cb = cch < 2 ? c0 : c1;
+        const uint64_t cb2 = f2_pack(cb, cb);
         uint32_t pw[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
+          const int k = cch * 32 + w * 4;
           float pp[4];
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), cb2, bias2), pp[0], pp[1]);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), cb2, bias2), pp[2],
+                    pp[3]);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int k = cch * 32 + w * 4 + u;
-            pp[u] = ex2_approx(fmaf(__uint_as_float(sr[k]), cb, bias));
-            if (kvalid < kBN && k >= kvalid) pp[u] = 0.0f;
-            lsum += pp[u];
+            pp[u] = ex2_approx(pp[u]);
+            if (tail && k + u >= kvalid) pp[u] = 0.0f;
           }
-          pw[w] = e4m3x2(pp[0], pp[1]) | (e4m3x2(pp[2], pp[3]) << 16);
+          l2 = f2_add(l2, f2_pack(pp[0], pp[1]));
+          l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
+          pw[w] = pack_lo_hi16(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
         }
         SAGE_TMEM_ST8(tS + cch * 8, pw);
       }
-      l += lsum;
+      float llo, lhi;
+      f2_unpack(l2, llo, lhi);
+      l += llo + lhi;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + t);

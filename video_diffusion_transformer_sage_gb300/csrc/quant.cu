@@ -131,7 +131,8 @@ __device__ __forceinline__ uint16_t i8code_as_f16(float x, float scale) {
 
 // One CTA per (128-row block b, head h): Q block -> one scale; the same rows of K - mean ->
 // two 64-row blocks, one scale each.  Pad rows (>= n) are excluded from the maxima and
-// written as code 0.
+// written as code 0.  All Q and K loads of the block are issued before any arithmetic so
+// that 32 KB per CTA are in flight; the three maxima share one block reduction.
 template <int D>
 __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
                                                        const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
@@ -142,30 +143,67 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
   constexpr int VPR = D / 8;            // vectors per row
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
-  __shared__ float red[8];
+  __shared__ float red[3][8];
   const int b = blockIdx.x, hh = blockIdx.y;
   const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
   const int row0 = b * 128;
 
-  // ---- Q
-  uint4 v[NP];
-  float amax = 0.0f;
+  uint4 vq[NP], vk[NP];
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
-    v[p] = row < n ? ld_stream(q + static_cast<int64_t>(row) * qst + hh * qsh + c8 * 8) : make_uint4(0, 0, 0, 0);
-    float f[8];
-    unpack8(v[p], f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    vq[p] = row < n ? ld_stream(q + static_cast<int64_t>(row) * qst + hh * qsh + c8 * 8) : make_uint4(0, 0, 0, 0);
+    vk[p] = row < n ? ld_stream(k + static_cast<int64_t>(row) * kst + hh * ksh + c8 * 8) : make_uint4(0, 0, 0, 0);
   }
-  amax = block_max<256>(amax, red);
-  const float qs = amax / 127.0f;
+  float mu[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mu[j] = k_mean[hh * D + c8 * 8 + j];
+
+  // |q| max on the bf16 bit patterns: for finite values, magnitude order = unsigned order
+  // of the bits without the sign.
+  uint32_t qbits = 0;
+  float am[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    qbits = __vmaxu2(qbits, vq[p].x & 0x7FFF7FFFu);
+    qbits = __vmaxu2(qbits, vq[p].y & 0x7FFF7FFFu);
+    qbits = __vmaxu2(qbits, vq[p].z & 0x7FFF7FFFu);
+    qbits = __vmaxu2(qbits, vq[p].w & 0x7FFF7FFFu);
+    const int row = row0 + p * RPP + rin;
+    if (row < n) {
+      float f[8];
+      unpack8(vk[p], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) am[p >= NP / 2] = fmaxf(am[p >= NP / 2], fabsf(f[j] - mu[j]));
+    }
+  }
+  float aq = fmaxf(__uint_as_float((qbits & 0xFFFFu) << 16), __uint_as_float(qbits & 0xFFFF0000u));
+  float a0 = am[0], a1 = am[1];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    aq = fmaxf(aq, __shfl_xor_sync(0xffffffffu, aq, o));
+    a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, o));
+    a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, o));
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    red[0][warp] = aq;
+    red[1][warp] = a0;
+    red[2][warp] = a1;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    aq = fmaxf(aq, red[0][w]);
+    a0 = fmaxf(a0, red[1][w]);
+    a1 = fmaxf(a1, red[2][w]);
+  }
+  const float qs = aq / 127.0f, ks0 = a0 / 127.0f, ks1 = a1 / 127.0f;
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
     float f[8];
-    unpack8(v[p], f);
+    unpack8(vq[p], f);
     uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -173,45 +211,20 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
              (static_cast<uint32_t>(i8code_as_f16(f[2 * j + 1], qs)) << 16);
     *reinterpret_cast<uint4*>(q_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
         make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  if (threadIdx.x == 0) q_scales[hh * (npad / 128) + b] = qs;
-
-  // ---- K - mean
-  float mu[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) mu[j] = k_mean[hh * D + c8 * 8 + j];
-  float am[2] = {0.0f, 0.0f};
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const int row = row0 + p * RPP + rin;
-    v[p] = row < n ? ld_stream(k + static_cast<int64_t>(row) * kst + hh * ksh + c8 * 8) : make_uint4(0, 0, 0, 0);
-    if (row < n) {
-      float f[8];
-      unpack8(v[p], f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) am[p >= NP / 2] = fmaxf(am[p >= NP / 2], fabsf(f[j] - mu[j]));
-    }
-  }
-  const float a0 = block_max<256>(am[0], red);
-  const float a1 = block_max<256>(am[1], red);
-  const float ks0 = a0 / 127.0f, ks1 = a1 / 127.0f;
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const int row = row0 + p * RPP + rin;
     const float ks = p < NP / 2 ? ks0 : ks1;
-    uint32_t w[4] = {0, 0, 0, 0};
+    uint32_t u[4] = {0, 0, 0, 0};
     if (row < n) {
-      float f[8];
-      unpack8(v[p], f);
+      unpack8(vk[p], f);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        w[j] = static_cast<uint32_t>(i8code_as_f16(f[2 * j] - mu[2 * j], ks)) |
+        u[j] = static_cast<uint32_t>(i8code_as_f16(f[2 * j] - mu[2 * j], ks)) |
                (static_cast<uint32_t>(i8code_as_f16(f[2 * j + 1] - mu[2 * j + 1], ks)) << 16);
     }
     *reinterpret_cast<uint4*>(k_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
-        make_uint4(w[0], w[1], w[2], w[3]);
+        make_uint4(u[0], u[1], u[2], u[3]);
   }
   if (threadIdx.x == 0) {
+    q_scales[hh * (npad / 128) + b] = qs;
     k_scales[hh * (npad / 64) + 2 * b] = ks0;
     k_scales[hh * (npad / 64) + 2 * b + 1] = ks1;
   }
@@ -230,7 +243,21 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
   __shared__ uint32_t tile[D][33];
   const int b = blockIdx.x, hh = blockIdx.y;
   const int t_base = b * 128;
-  for (int it = threadIdx.x; it < VPR * 32; it += 256) {
+  constexpr int kItems = VPR * 32 / 256;   // work items per thread: 2 at D = 128, 1 at D = 64
+  uint4 raw[kItems][4];
+#pragma unroll
+  for (int i = 0; i < kItems; ++i) {
+    const int it = threadIdx.x + i * 256;
+    const int c8 = it % VPR, tg = it / VPR;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t_base + tg * 4 + u;
+      raw[i][u] = t < n ? ld_stream(v + static_cast<int64_t>(t) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kItems; ++i) {
+    const int it = threadIdx.x + i * 256;
     const int c8 = it % VPR, tg = it / VPR;
     float sc[8];
 #pragma unroll
@@ -240,12 +267,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
     for (int u = 0; u < 4; ++u) {
       const int t = t_base + tg * 4 + u;
       float f[8];
-      if (t < n) {
-        unpack8(ld_stream(v + static_cast<int64_t>(t) * st + hh * sh + c8 * 8), f);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = 0.0f;
-      }
+      unpack8(raw[i][u], f);
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
         const float y0 = (t < n && sc[j] != 0.0f) ? f[j] / sc[j] : 0.0f;
