@@ -87,17 +87,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
-// Max of 64 consecutive fp32 values (as bits), four independent 3-input chains.
+// Max of 64 consecutive fp32 values (as bits): four independent chains of 3-input maxima
+// covering s[0..11], then s[12..59] eight at a time, then s[60..63].
 __device__ __forceinline__ float block_max64(const uint32_t* s) {
-  float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]), c = __uint_as_float(s[2]),
-        d = __uint_as_float(s[3]);
+  auto f = [s](int i) { return __uint_as_float(s[i]); };
+  float a = fmax3(f(0), f(1), f(2)), b = fmax3(f(3), f(4), f(5));
+  float c = fmax3(f(6), f(7), f(8)), d = fmax3(f(9), f(10), f(11));
 #pragma unroll
-  for (int k = 4; k < 64; k += 8) {
-    a = fmax3(a, __uint_as_float(s[k]), __uint_as_float(s[k + 1]));
-    b = fmax3(b, __uint_as_float(s[k + 2]), __uint_as_float(s[k + 3]));
-    c = fmax3(c, __uint_as_float(s[k + 4]), __uint_as_float(s[k + 5]));
-    d = fmax3(d, __uint_as_float(s[k + 6]), __uint_as_float(s[k + 7]));
+  for (int k = 12; k < 60; k += 8) {
+    a = fmax3(a, f(k), f(k + 1));
+    b = fmax3(b, f(k + 2), f(k + 3));
+    c = fmax3(c, f(k + 4), f(k + 5));
+    d = fmax3(d, f(k + 6), f(k + 7));
   }
+  a = fmax3(a, f(60), f(61));
+  b = fmax3(b, f(62), f(63));
   return fmaxf(fmax3(a, b, c), d);
 }
 
