@@ -14,6 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsage_gb300.so")
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["sage_api.cu", "quant.cu", "attn_fwd.cu", "attn_dense.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -29,7 +30,7 @@ def _nvcc() -> str:
 
 def _deps_mtime() -> float:
     paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    paths.append(os.path.join(os.path.dirname(HERE), "include", "sage.h"))
+    paths.append(os.path.join(INCLUDE, "sage.h"))
     return max(os.path.getmtime(p) for p in paths)
 
 
@@ -42,7 +43,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

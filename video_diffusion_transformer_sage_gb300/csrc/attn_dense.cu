@@ -17,7 +17,7 @@ namespace {
 
 constexpr int kKeys = 64;
 // Rows per warp: 4 at D = 128 keeps the accumulators in registers.
-template <int D> constexpr int rows_per_warp() { return D == 128 ? 4 : 8; }
+template <int D> __host__ __device__ constexpr int rows_per_warp() { return D == 128 ? 4 : 8; }
 
 template <int D>
 __global__ void __launch_bounds__(256) attn_dense_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,

@@ -125,6 +125,89 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
     mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
 }
 
+// One 128-key tile of the online softmax for the calling thread's row (= TMEM lane):
+//   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
+//   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
+//   p = exp2(S c - m_new) into the first 32 columns of S; l = alpha l + sum p; and, if any row
+//   of the warp saw its max rise, multiplies that row's O by alpha = exp2(m_old - m_new).
+// kTail: keys >= kvalid are excluded from the max and get p = 0.
+template <int D, bool kTail>
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0, float c1, int kvalid, bool first,
+                                             float& m, float& l) {
+  uint32_t sr[128];
+  SAGE_TMEM_LD32(tS + 0, (sr + 0));
+  SAGE_TMEM_LD32(tS + 32, (sr + 32));
+  SAGE_TMEM_LD32(tS + 64, (sr + 64));
+  SAGE_TMEM_LD32(tS + 96, (sr + 96));
+  tmem_wait_ld();
+  float mx0, mx1;
+  if (!kTail) {
+    mx0 = block_max64(sr);
+    mx1 = block_max64(sr + 64);
+  } else {
+    mx0 = mx1 = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 64; ++k)
+      if (k < kvalid) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
+#pragma unroll
+    for (int k = 64; k < 128; ++k)
+      if (k < kvalid) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
+  }
+  // fmaxf drops the NaN of (-inf) * 0 for an empty half.
+  const float m_new = fmaxf(m, fmaxf(mx0 * c0, mx1 * c1));
+  const bool rise = !first && (m_new > m);
+  const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
+  m = m_new;
+  // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
+  const uint64_t bias2 = f2_pack(kLog2_448 - m_new, kLog2_448 - m_new);
+  uint64_t l2 = f2_pack(0.0f, 0.0f);
+#pragma unroll
+  for (int cch = 0; cch < 4; ++cch) {
+    const float cb = cch < 2 ? c0 : c1;
+    const uint64_t cb2 = f2_pack(cb, cb);
+    uint32_t pw[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int k = cch * 32 + w * 4;
+      float pp[4];
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), cb2, bias2), pp[0], pp[1]);
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), cb2, bias2), pp[2], pp[3]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        pp[u] = ex2_approx(pp[u]);
+        if (kTail && k + u >= kvalid) pp[u] = 0.0f;
+      }
+      l2 = f2_add(l2, f2_pack(pp[0], pp[1]));
+      l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
+      pw[w] = pack_lo_hi16(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
+    }
+    SAGE_TMEM_ST8(tS + cch * 8, pw);
+  }
+  float llo, lhi;
+  f2_unpack(l2, llo, lhi);
+  l = l * alpha + (llo + lhi);
+  // O is rescaled after P is formed, when S no longer occupies registers.  P.V of this tile
+  // is issued only after p_full, so O still holds the previous tiles' sum here.
+  if (__any_sync(0xffffffffu, rise)) {
+    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      SAGE_TMEM_LD32(tO + c, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        float lo, hi;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), lo, hi);
+        o[k] = __float_as_uint(lo);
+        o[k + 1] = __float_as_uint(hi);
+      }
+      SAGE_TMEM_ST32(tO + c, o);
+    }
+  }
+  tmem_wait_st();
+}
+
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -285,84 +368,12 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-      SAGE_TMEM_LD32(tS + 0, (sr + 0));
-      SAGE_TMEM_LD32(tS + 32, (sr + 32));
-      SAGE_TMEM_LD32(tS + 64, (sr + 64));
-      SAGE_TMEM_LD32(tS + 96, (sr + 96));
-      tmem_wait_ld();
       const float c0 = cq * ks0, c1 = cq * ks1;
       const int kvalid = min(kBN, p.n - j * kBN);
-      const bool tail = kvalid < kBN;
-      float mx0, mx1;
-      if (!tail) {
-        mx0 = block_max64(sr);
-        mx1 = block_max64(sr + 64);
-      } else {
-        mx0 = mx1 = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (k < kvalid) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
-#pragma unroll
-        for (int k = 64; k < 128; ++k)
-          if (k < kvalid) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
-      }
-      // c >= 0 and rounding is monotone, so max_k fl(S_k c) = fl(c max_k S_k).  fmaxf drops
-      // the NaN of (-inf) * 0 for an empty half.
-      const float mt = fmaxf(mx0 * c0, mx1 * c1);
-      const float m_new = fmaxf(m, mt);
-      const bool rise = (j > 0) && (m_new > m);
-      if (__any_sync(0xffffffffu, rise)) {
-        const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
-        l *= alpha;
-        const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          SAGE_TMEM_LD32(tO + c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            float lo, hi;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), lo, hi);
-            o[k] = __float_as_uint(lo);
-            o[k + 1] = __float_as_uint(hi);
-          }
-          SAGE_TMEM_ST32(tO + c, o);
-        }
-        tmem_wait_st();
-      }
-      m = m_new;
-      // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
-      const uint64_t bias2 = f2_pack(kLog2_448 - m, kLog2_448 - m);
-      uint64_t l2 = f2_pack(0.0f, 0.0f);
-#pragma unroll
-      for (int cch = 0; cch < 4; ++cch) {
-        const float cb = cch < 2 ? c0 : c1;
-        const uint64_t cb2 = f2_pack(cb, cb);
-        uint32_t pw[8];
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const int k = cch * 32 + w * 4;
-          float pp[4];
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), cb2, bias2), pp[0], pp[1]);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), cb2, bias2), pp[2],
-                    pp[3]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            pp[u] = ex2_approx(pp[u]);
-            if (tail && k + u >= kvalid) pp[u] = 0.0f;
-          }
-          l2 = f2_add(l2, f2_pack(pp[0], pp[1]));
-          l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
-          pw[w] = pack_lo_hi16(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
-        }
-        SAGE_TMEM_ST8(tS + cch * 8, pw);
-      }
-      float llo, lhi;
-      f2_unpack(l2, llo, lhi);
-      l += llo + lhi;
-      tmem_wait_st();
+      if (kvalid == kBN)
+        softmax_step<D, false>(tS, tO, c0, c1, kBN, j == 0, m, l);
+      else
+        softmax_step<D, true>(tS, tO, c0, c1, kvalid, j == 0, m, l);
       tc_fence_before();
       mbar_arrive(p_full + t);
     }

@@ -3,7 +3,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "../../include/sage.h"
+#include "sage.h"
 
 namespace sage {
 

@@ -30,26 +30,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+// One poll of the phase with the given parity.  The thread may sleep inside the poll, up to
+// `hint_ns`, until the phase completes; it wakes as soon as it does.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete.  Gives up after `limit_ns`
-// nanoseconds of global time and returns false (the caller records a timeout).
+// Waits for the phase with the given parity to complete, sleeping in the barrier rather than
+// spinning.  Gives up after `limit_ns` nanoseconds of global time and returns false (the
+// caller records a timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  constexpr uint32_t kHintNs = 1000000;   // 1 ms per poll at most
   const uint32_t a = smem_u32(bar);
-  if (mbar_test(a, parity)) return true;
+  if (mbar_test(a, parity, kHintNs)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test(a, parity)) return true;
+    if (mbar_test(a, parity, kHintNs)) return true;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
