@@ -11,12 +11,12 @@
 // art only: this kernel is organised around Blackwell's tensor memory instead.
 //
 // CTA = 256 query rows of one head (two 128-row tiles t = 0, 1) and every 128-key tile of
-// that head.  Warp roles (640 threads):
-//   warp 0        TMA producer: Q tiles once, then K/V tiles into a kStages-deep ring
-//   warp 1        MMA issuer (one thread): S_t = Q_t K^T, O_t += P_t V
-//   warp 2        TMEM allocator
-//   warps 4-11    softmax + epilogue of tile 0, warps 12-19 of tile 1: two threads per row
-//                 (row = TMEM lane; warp w reaches lanes 32 (w % 4) ..), one per 64-key half
+// that head.  Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K/V tiles into a kStages-deep ring
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T, O_t += P_t V
+//   warp 2      TMEM allocator
+//   warps 4-7   softmax + epilogue of tile 0 (thread = row = TMEM lane)
+//   warps 8-11  softmax + epilogue of tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [256+D, 256+2D).
 // P_t (E4M3, 4 keys per 32-bit column) overwrites columns [0,32) of S_t and is the A
 // operand of the P.V MMA straight from TMEM.
@@ -42,7 +42,6 @@
 namespace sage {
 namespace {
 
-constexpr int kThreads = 640;   // 4 role warps + 2 tiles x 8 softmax warps (two threads per row)
 constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
@@ -61,7 +60,7 @@ struct Cfg {
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1 + 8;
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -126,61 +125,53 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
     mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
 }
 
-// One 128-key tile of the online softmax, computed by two threads per row (= TMEM lane):
-// the thread of half h owns keys [64h, 64h + 64), whose K scale is c.
-//   1. reads its 64 S columns from TMEM and forms max_k fl(S_k c) as c * max_k S_k (c >= 0
-//      and rounding is monotone, so the two are equal);
-//   2. swaps that half-max with the partner thread through shared memory (an mbarrier of
-//      the 64 threads sharing these rows, waited with the usual time limit), so both hold
-//      the row's tile max and the same m_new;
-//   3. writes P = E4M3(448 p), p = exp2(S c - m_new), for its keys into P columns
-//      [16h, 16h + 16) -- P overlays the first 32 columns of S, which both threads have
-//      finished reading at the exchange;
-//   4. keeps its own partial l = alpha l + sum p (the halves are added at the end);
-//   5. if any row of the warp saw its max rise, multiplies its half of O by
-//      alpha = exp2(m_old - m_new).
-// kTail: only keys < kvalid (counted within this half) exist.  Returns false if the exchange
-// wait expired.
+// One 128-key tile of the online softmax for the calling thread's row (= TMEM lane):
+//   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
+//   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
+//   p = exp2(S c - m_new) into the first 32 columns of S; l = alpha l + sum p; and, if any row
+//   of the warp saw its max rise, multiplies that row's O by alpha = exp2(m_old - m_new).
+// kTail: keys >= kvalid are excluded from the max and get p = 0.
 template <int D, bool kTail>
-__device__ __forceinline__ bool softmax_half_step(uint32_t tSh, uint32_t tPh, uint32_t tOh, float c, int kvalid,
-                                                  bool first, float& m, float& l, float* x_mine,
-                                                  const float* x_other, uint64_t* xbar, uint32_t parity,
-                                                  uint64_t limit) {
-  uint32_t sr[64];
-  SAGE_TMEM_LD32(tSh + 0, (sr + 0));
-  SAGE_TMEM_LD32(tSh + 32, (sr + 32));
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0, float c1, int kvalid, bool first,
+                                             float& m, float& l) {
+  uint32_t sr[128];
+  SAGE_TMEM_LD32(tS + 0, (sr + 0));
+  SAGE_TMEM_LD32(tS + 32, (sr + 32));
+  SAGE_TMEM_LD32(tS + 64, (sr + 64));
+  SAGE_TMEM_LD32(tS + 96, (sr + 96));
   tmem_wait_ld();
-  float mx;
+  float mx0, mx1;
   if (!kTail) {
-    mx = block_max64(sr);
+    mx0 = block_max64(sr);
+    mx1 = block_max64(sr + 64);
   } else {
-    mx = -INFINITY;
+    mx0 = mx1 = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 64; ++k)
-      if (k < kvalid) mx = fmaxf(mx, __uint_as_float(sr[k]));
+      if (k < kvalid) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
+#pragma unroll
+    for (int k = 64; k < 128; ++k)
+      if (k < kvalid) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
   }
-  *x_mine = mx * c;   // (-inf) * 0 = NaN for an empty half; fmaxf below drops it
-  tc_fence_before();
-  mbar_arrive(xbar);
-  if (!warp_wait(xbar, parity, limit)) return false;
-  tc_fence_after();
-  const float m_new = fmaxf(m, fmaxf(*x_mine, *x_other));
+  // fmaxf drops the NaN of (-inf) * 0 for an empty half.
+  const float m_new = fmaxf(m, fmaxf(mx0 * c0, mx1 * c1));
   const bool rise = !first && (m_new > m);
   const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
   m = m_new;
   // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
   const uint64_t bias2 = f2_pack(kLog2_448 - m_new, kLog2_448 - m_new);
-  const uint64_t c2 = f2_pack(c, c);
   uint64_t l2 = f2_pack(0.0f, 0.0f);
 #pragma unroll
-  for (int cch = 0; cch < 2; ++cch) {
+  for (int cch = 0; cch < 4; ++cch) {
+    const float cb = cch < 2 ? c0 : c1;
+    const uint64_t cb2 = f2_pack(cb, cb);
     uint32_t pw[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const int k = cch * 32 + w * 4;
       float pp[4];
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, bias2), pp[0], pp[1]);
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), c2, bias2), pp[2], pp[3]);
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), cb2, bias2), pp[0], pp[1]);
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), cb2, bias2), pp[2], pp[3]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         pp[u] = ex2_approx(pp[u]);
@@ -190,7 +181,7 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tSh, uint32_t tPh, ui
       l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
       pw[w] = pack_lo_hi16(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
     }
-    SAGE_TMEM_ST8(tPh + cch * 8, pw);
+    SAGE_TMEM_ST8(tS + cch * 8, pw);
   }
   float llo, lhi;
   f2_unpack(l2, llo, lhi);
@@ -200,9 +191,9 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tSh, uint32_t tPh, ui
   if (__any_sync(0xffffffffu, rise)) {
     const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-    for (int cc = 0; cc < D / 2; cc += 32) {
+    for (int c = 0; c < D; c += 32) {
       uint32_t o[32];
-      SAGE_TMEM_LD32(tOh + cc, o);
+      SAGE_TMEM_LD32(tO + c, o);
       tmem_wait_ld();
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
@@ -211,23 +202,20 @@ __device__ __forceinline__ bool softmax_half_step(uint32_t tSh, uint32_t tPh, ui
         o[k] = __float_as_uint(lo);
         o[k + 1] = __float_as_uint(hi);
       }
-      SAGE_TMEM_ST32(tOh + cc, o);
+      SAGE_TMEM_ST32(tO + c, o);
     }
   }
   tmem_wait_st();
-  return true;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_skip;
   __shared__ volatile int s_abort;
-  // Half-row maxima swapped between the two threads of a row: [tile][tile parity][half][row].
-  __shared__ float s_xmax[2][2][2][kBM];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + 2 * C::kQTileBytes;
@@ -239,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* mma_final = pv_done + 2;
-  uint64_t* xbar = mma_final + 1;   // [tile * 4 + lane quarter]: the two warps sharing those rows
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,11 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
-      mbar_init(p_full + t, 256);
+      mbar_init(p_full + t, 128);
       mbar_init(pv_done + t, 1);
     }
     mbar_init(mma_final, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(xbar + i, 64);
     fence_mbar_init();
   }
   __syncthreads();
@@ -355,71 +341,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int t = (warp - 4) >> 3;               // Q tile
-    const int half = ((warp - 4) >> 2) & 1;      // keys [64 half, 64 half + 64) of each tile
+    const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                     // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;                // row within the tile = TMEM lane
     const int row = q0 + t * kBM + r;            // query row
-    uint64_t* pair_bar = xbar + t * 4 + wq;      // mbarrier of the two warps sharing these rows
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
-    const uint32_t tSh = tS + half * 64;         // this thread's S columns
-    const uint32_t tPh = tS + half * 16;         // this thread's P columns (4 keys per column)
-    const uint32_t tOh = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1) + half * (D / 2);
+    const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
     const int nbq = p.npad / 128, nbk = p.npad / 64;
     const int qblk = (q0 + t * kBM) / 128;
     const float qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
     const float cq = qscale * p.sm_scale_log2;
-    const float* ks = p.k_scales + hh * nbk + half;   // scale of 64-key block 2j + half
+    const float* ks = p.k_scales + hh * nbk;
     float m = -INFINITY, l = 0.0f;
-    float ksn = ks[0];   // k scale of the next tile, loaded one tile ahead
+    float ksn0 = ks[0], ksn1 = ks[1];   // k scales of the next tile, loaded one tile ahead
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const float ksj = ksn;
-      if (j + 1 < ntiles) ksn = ks[2 * j + 2];
+      const float ks0 = ksn0, ks1 = ksn1;
+      if (j + 1 < ntiles) {
+        ksn0 = ks[2 * j + 2];
+        ksn1 = ks[2 * j + 3];
+      }
       if (!warp_wait(s_full + t, j & 1, limit)) {
         if (lane == 0) record_error(p.status, kWhereSFull, &s_abort);
         ok = false;
         break;
       }
       tc_fence_after();
-      const float c = cq * ksj;
-      const int kvalid = min(kBN, p.n - j * kBN) - half * 64;   // valid keys in this half (may be <= 0)
-      float* xm = &s_xmax[t][j & 1][half][r];
-      const float* xo = &s_xmax[t][j & 1][half ^ 1][r];
-      const bool done =
-          kvalid >= 64
-              ? softmax_half_step<D, false>(tSh, tPh, tOh, c, 64, j == 0, m, l, xm, xo, pair_bar, j & 1, limit)
-              : softmax_half_step<D, true>(tSh, tPh, tOh, c, kvalid, j == 0, m, l, xm, xo, pair_bar, j & 1, limit);
-      if (!done) {
-        if (lane == 0) record_error(p.status, kWhereXchg, &s_abort);
-        ok = false;
-        break;
-      }
+      const float c0 = cq * ks0, c1 = cq * ks1;
+      const int kvalid = min(kBN, p.n - j * kBN);
+      if (kvalid == kBN)
+        softmax_step<D, false>(tS, tO, c0, c1, kBN, j == 0, m, l);
+      else
+        softmax_step<D, true>(tS, tO, c0, c1, kvalid, j == 0, m, l);
       tc_fence_before();
       mbar_arrive(p_full + t);
-    }
-    // Whole-row l = sum of the two halves' partial sums (same m, same rescales).  The slot of
-    // parity ntiles is free: the partner finished reading it before the last exchange.
-    if (ok) {
-      s_xmax[t][ntiles & 1][half][r] = l;
-      mbar_arrive(pair_bar);
-      if (warp_wait(pair_bar, ntiles & 1, limit)) {
-        l += s_xmax[t][ntiles & 1][half ^ 1][r];
-      } else {
-        if (lane == 0) record_error(p.status, kWhereXchg, &s_abort);
-        ok = false;
-      }
     }
     if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const float* vs = p.v_scales + hh * D + half * (D / 2);
-      uint16_t* orow = p.out + static_cast<int64_t>(row) * p.ost + static_cast<int64_t>(hh) * p.osh + half * (D / 2);
+      const float* vs = p.v_scales + hh * D;
+      uint16_t* orow = p.out + static_cast<int64_t>(row) * p.ost + static_cast<int64_t>(hh) * p.osh;
 #pragma unroll 1
-      for (int c = 0; c < D / 2; c += 32) {
+      for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
-        SAGE_TMEM_LD32(tOh + c, o);
+        SAGE_TMEM_LD32(tO + c, o);
         tmem_wait_ld();
         if (row < p.n) {
 #pragma unroll
@@ -582,7 +548,7 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, float sm_s
   p.status = status;
   p.wait_limit_ns = kWaitLimitNs;
   dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
+  attn_fwd_kernel<D><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 

@@ -19,7 +19,6 @@ enum DeviceWhere : int32_t {
   kWherePvDone = 6,
   kWhereDebugTma = 7,
   kWhereDebugMma = 8,
-  kWhereXchg = 9,
 };
 
 struct StridedView {
