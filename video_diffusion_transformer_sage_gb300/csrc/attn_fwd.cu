@@ -43,6 +43,12 @@ namespace sage {
 namespace {
 
 constexpr int kBM = 128;   // query rows per tile
+// Register split of the 384-thread CTA, launched at 168 registers per thread (384 x 168 =
+// 64512): the role warpgroup (warps 0-3) drops to 56, the two softmax warpgroups rise to
+// 224.  128 x 56 + 256 x 224 = 64512, exactly the launch's total, so the rise can always be
+// granted.
+constexpr int kRegsLaunch = 168, kRegsRoles = 56, kRegsSoftmax = 224;
+static_assert(128 * kRegsRoles + 256 * kRegsSoftmax <= 384 * kRegsLaunch, "register split exceeds launch");
 constexpr int kBN = 128;   // keys per tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -179,7 +185,7 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
       }
       l2 = f2_add(l2, f2_pack(pp[0], pp[1]));
       l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
-      pw[w] = pack_lo_hi16(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
+      pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
     }
     SAGE_TMEM_ST8(tS + cch * 8, pw);
   }
@@ -261,85 +267,88 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      const int qrow = hh * p.npad + q0;
-      mbar_arrive_expect_tx(q_full, 2 * C::kQTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_2d(sQ + t * C::kQTileBytes + pn * C::kPanelBytes, &qmap, q_full, pn * 64, qrow + t * kBM);
-      for (int j = 0; j < ntiles; ++j) {
-        const int s = j % C::kStages;
-        if (j >= C::kStages && !mbar_wait(kv_empty + s, ((j / C::kStages) - 1) & 1, limit)) {
-          record_error(p.status, kWhereKvEmpty, &s_abort);
-          break;
-        }
-        if (s_abort) break;
-        uint8_t* sk = sKV + s * C::kStageBytes;
-        mbar_arrive_expect_tx(kv_full + s, C::kStageBytes);
-        for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_2d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh * p.npad + j * kBN);
-        tma_load_2d(sk + C::kKTileBytes, &vmap, kv_full + s, j * kBN, hh * D);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t sq = smem_u32(sQ);
-      const uint32_t skv = smem_u32(sKV);
-      const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
-      const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
-      bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
-      if (!ok) record_error(p.status, kWhereQFull, &s_abort);
-      if (ok) {
-        tc_fence_after();
-        issue_qk<D>(colS[0], sq, skv);
-        tc_commit(s_full + 0);
-        issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
-        tc_commit(s_full + 1);
-      }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!mbar_wait(p_full + t, j & 1, limit)) {
-            record_error(p.status, kWherePFull, &s_abort);
-            ok = false;
+  if (warp < 4) {
+    regs_dec<kRegsRoles>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        const int qrow = hh * p.npad + q0;
+        mbar_arrive_expect_tx(q_full, 2 * C::kQTileBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_2d(sQ + t * C::kQTileBytes + pn * C::kPanelBytes, &qmap, q_full, pn * 64, qrow + t * kBM);
+        for (int j = 0; j < ntiles; ++j) {
+          const int s = j % C::kStages;
+          if (j >= C::kStages && !mbar_wait(kv_empty + s, ((j / C::kStages) - 1) & 1, limit)) {
+            record_error(p.status, kWhereKvEmpty, &s_abort);
             break;
           }
+          if (s_abort) break;
+          uint8_t* sk = sKV + s * C::kStageBytes;
+          mbar_arrive_expect_tx(kv_full + s, C::kStageBytes);
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_2d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh * p.npad + j * kBN);
+          tma_load_2d(sk + C::kKTileBytes, &vmap, kv_full + s, j * kBN, hh * D);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        const uint32_t sq = smem_u32(sQ);
+        const uint32_t skv = smem_u32(sKV);
+        const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
+        const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
+        bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
+        if (!ok) record_error(p.status, kWhereQFull, &s_abort);
+        if (ok) {
           tc_fence_after();
-          issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
-          tc_commit(pv_done + t);
-          if (t == 1) tc_commit(kv_empty + s);
-          if (j + 1 < ntiles) {
-            if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
-              record_error(p.status, kWhereKvFull, &s_abort);
-              ok = false;
-              break;
-            }
-            // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
-            if (!mbar_wait(pv_done + t, j & 1, limit)) {
-              record_error(p.status, kWherePvDone, &s_abort);
+          issue_qk<D>(colS[0], sq, skv);
+          tc_commit(s_full + 0);
+          issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
+          tc_commit(s_full + 1);
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int s = j % C::kStages;
+          const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(p_full + t, j & 1, limit)) {
+              record_error(p.status, kWherePFull, &s_abort);
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
-            tc_commit(s_full + t);
+            issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            tc_commit(pv_done + t);
+            if (t == 1) tc_commit(kv_empty + s);
+            if (j + 1 < ntiles) {
+              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+                record_error(p.status, kWhereKvFull, &s_abort);
+                ok = false;
+                break;
+              }
+              // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
+              if (!mbar_wait(pv_done + t, j & 1, limit)) {
+                record_error(p.status, kWherePvDone, &s_abort);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              tc_commit(s_full + t);
+            }
           }
+          if (s_abort) ok = false;
         }
-        if (s_abort) ok = false;
+        // Drain: every MMA issued above has finished before the CTA frees its tensor memory.
+        tc_commit(mma_final);
+        mbar_wait(mma_final, 0, limit);
       }
-      // Drain: every MMA issued above has finished before the CTA frees its tensor memory.
-      tc_commit(mma_final);
-      mbar_wait(mma_final, 0, limit);
     }
-  } else if (warp >= 4) {
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                     // TMEM lane quarter this warp may access

@@ -43,16 +43,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity, uint32_
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete, sleeping in the barrier rather than
-// spinning.  Gives up after `limit_ns` nanoseconds of global time and returns false (the
-// caller records a timeout).
+// spinning.  The global timer is read once per 256 polls; the wait gives up (returns false,
+// the caller records a timeout) once `limit_ns` nanoseconds have passed since the first read.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   constexpr uint32_t kHintNs = 1000000;   // 1 ms per poll at most
   const uint32_t a = smem_u32(bar);
-  if (mbar_test(a, parity, kHintNs)) return true;
-  const uint64_t t0 = global_timer_ns();
+  uint64_t t0 = 0;
   while (true) {
-    if (mbar_test(a, parity, kHintNs)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_test(a, parity, kHintNs)) return true;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) t0 = now;
+    else if (now - t0 > limit_ns) return false;
   }
 }
 
@@ -162,6 +165,17 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ register split
+// Per-warpgroup register budgets (every thread of the warpgroup executes the same one).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ packed fp32 math
 // Blackwell executes two fp32 lanes per instruction for these (.f32x2 on a 64-bit pair).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
@@ -207,9 +221,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 // Two fp32 values to two E4M3 bytes (round to nearest even, saturate to +-448):
 // `lo` lands in bits 0-7, `hi` in bits 8-15.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two 16-bit halves into one word (lo in bits 0-15) without widening either half first.
+__device__ __forceinline__ uint32_t pack_h2(uint16_t lo, uint16_t hi) {
+  uint32_t r;
+  asm("mov.b32 %0, {%1, %2};" : "=r"(r) : "h"(lo), "h"(hi));
   return r;
 }
 
