@@ -43,15 +43,17 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed loop runs."""
+    """nvidia-smi clocks and throttle reasons every 200 ms; `summary()` keeps the samples taken
+    between `mark_start()` and `mark_end()` (the timed region)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -61,6 +63,12 @@ class ClockSampler:
         except OSError:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         self.out = ""
@@ -73,24 +81,29 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        import datetime
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in (self.out or "").splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if self.t0 is not None and not (self.t0 - 0.1 <= ts <= self.t1 + 0.1):
+                    continue
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[4:8]):
+            for nm, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power)}
 
 
 def _traffic_per_launch():
@@ -161,20 +174,23 @@ def run_gpu(args):
         if ev is not None:
             ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        time.sleep(1.0)                      # let the sampler start before the timed region
+        for _ in range(args.warmup):
+            step()
         torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        clk.mark_start()
         t0.record(stream)
         for i in range(args.steps):
             step(evs[i])
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     if pg:
         pg.barrier()
     code, where = sage.sage_check_device_status(status, stream)
@@ -191,34 +207,60 @@ def run_gpu(args):
     flops = w.flops
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
-    # ---- end to end through the C ABI with host buffers: pinned H2D of the QKV buffer,
-    # the whole path, D2H of the output, every step.
-    host_out = torch.empty((n, h, d), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 5))
-    ws = sage.workspace(n, h, d, dev)
-    storage2 = torch.empty_like(storage)
-    q2, k2, v2 = views(storage2)
-
-    def e2e_step():
-        storage2.copy_(host, non_blocking=True)
-        sage.sage_attn_fwd(q2, k2, v2, sm_scale, out, ws, stream)
-        host_out.copy_(out, non_blocking=True)
-
-    e2e_ms = float("nan")
+    # ---- end to end through the C ABI with host buffers.  Every step copies its QKV input
+    # from pinned host memory (H2D), runs the whole path (sage_attn_fwd) and copies the
+    # output back to pinned host memory (D2H).  Copies run on their own streams, double
+    # buffered, so step i's compute overlaps step i+1's H2D and step i-1's D2H -- a serving
+    # loop.  The serial variant (copy, compute, copy, in order) is reported beside it.
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 10))
+    e2e_ms = e2e_serial_ms = float("nan")
+    host_out = [torch.empty((n, h, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     if e2e_steps:
-        e2e_step()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / e2e_steps
-    if pg:
-        tt = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+        ws = sage.workspace(n, h, d, dev)
+        bufs = [torch.empty_like(storage) for _ in range(2)]
+        outs = [torch.empty((n, h, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        comp = torch.cuda.current_stream(dev)
+
+        def run(steps, pipelined):
+            ev_in = [torch.cuda.Event() for _ in range(steps)]
+            ev_done = [torch.cuda.Event() for _ in range(steps)]
+            ev_out = [torch.cuda.Event() for _ in range(steps)]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(comp)
+            s_in.wait_event(a)
+            for i in range(steps):
+                k_ = i % 2
+                sin = s_in if pipelined else comp
+                sout = s_out if pipelined else comp
+                if i >= 2:
+                    sin.wait_event(ev_done[i - 2])      # compute of step i-2 released buffer k_
+                with torch.cuda.stream(sin):
+                    bufs[k_].copy_(host, non_blocking=True)
+                ev_in[i].record(sin)
+                comp.wait_event(ev_in[i])
+                if i >= 2:
+                    comp.wait_event(ev_out[i - 2])      # D2H of step i-2 released output k_
+                qv, kv, vv = views(bufs[k_])
+                sage.sage_attn_fwd(qv, kv, vv, sm_scale, outs[k_], ws, comp)
+                ev_done[i].record(comp)
+                sout.wait_event(ev_done[i])
+                with torch.cuda.stream(sout):
+                    host_out[k_].copy_(outs[k_], non_blocking=True)
+                ev_out[i].record(sout)
+            comp.wait_event(ev_out[steps - 1])
+            b.record(comp)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / steps
+
+        run(2, True)
+        e2e_ms = run(e2e_steps, True)
+        e2e_serial_ms = run(e2e_steps, False)
+        if pg:
+            tt = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
 
     bf16_burst, bf16_sus, hbm, peak_src = _peaks()
     # The fused kernel does half its FLOPs as fp16 MMAs (QK^T on INT8 codes held in fp16)
@@ -248,8 +290,11 @@ def run_gpu(args):
                        "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
                        "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
-                "h2d_bytes_per_step": int(host.numel() * 2), "d2h_bytes_per_step": int(host_out.numel() * 2),
-                "ms_per_step": round(e2e_ms, 3)},
+                "h2d_bytes_per_step": int(host.numel() * 2), "d2h_bytes_per_step": int(host_out[0].numel() * 2),
+                "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
+                "how": "pinned host QKV -> H2D, sage_attn_fwd, D2H -> pinned host each step; copies on their own "
+                       "streams, double-buffered (step i overlaps H2D of i+1 and D2H of i-1)",
+                "serial_ms_per_step": round(e2e_serial_ms, 3)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
@@ -316,7 +361,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
   __shared__ float red[3][8];
-  const int b = blockIdx.x, hh = blockIdx.y;
+  const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
   const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
   const int row0 = b * 128;
 
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
                                                       uint8_t* __restrict__ v_codes) {
   constexpr int VPR = D / 8;
   __shared__ uint32_t tile[D][33];
-  const int b = blockIdx.x, hh = blockIdx.y;
+  const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
   const int t_base = b * 128;
   constexpr int kItems = VPR * 32 / 256;   // work items per thread: 2 at D = 128, 1 at D = 64
   uint4 raw[kItems][4];
@@ -317,7 +317,7 @@ cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const fl
                             uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                             cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
-  dim3 grid(npad / 128, h);
+  dim3 grid(h, npad / 128);
   if (d == 128)
     quant_qk_kernel<128><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, q_codes,
                                               q_scales, k_codes, k_scales);
@@ -330,7 +330,7 @@ cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const fl
 cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, int h, int d, uint8_t* v_codes,
                            cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
-  dim3 grid(npad / 128, h);
+  dim3 grid(h, npad / 128);
   if (d == 128)
     quant_v_kernel<128><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
   else
