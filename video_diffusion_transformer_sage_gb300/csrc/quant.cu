@@ -13,7 +13,8 @@
 //  * INT8: scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)), -127, 127), IEEE
 //    division; all-zero block -> scale 0, codes 0.  K uses fl32(k - mean).
 //  * E4M3: scale = fl32(amax / 448), code = cvt.rn.satfinite.e4m3(fl32(v / scale)).
-// No FMA contraction can change these results: they contain no multiply-add.
+// The per-element quotient fl32(x / scale) is formed from one IEEE reciprocal per scale and
+// Markstein's FMA correction (div_rn2), which yields the same correctly rounded value.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -122,11 +123,28 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
-__device__ __forceinline__ uint16_t i8code_as_f16(float x, float scale) {
-  if (scale == 0.0f) return 0;
-  float r = rintf(x / scale);
-  r = fminf(fmaxf(r, -127.0f), 127.0f);
-  return __half_as_ushort(__float2half_rn(r));  // integers |r| <= 127 are exact in fp16
+// Correctly rounded x / s from r = RN(1 / s): y = RN(x r) is within 2 ulp of x / s, the FMA
+// gives the exact remainder x - y s, and one FMA correction y + r (x - y s) rounds to
+// RN(x / s) (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  Two quotients per call, on the
+// packed fp32x2 pipe; `neg_s2` holds -s twice and `r2` holds r twice.
+__device__ __forceinline__ uint64_t div_rn2(uint64_t x2, uint64_t neg_s2, uint64_t r2) {
+  const uint64_t y2 = f2_mul(x2, r2);
+  const uint64_t e2 = f2_fma(y2, neg_s2, x2);
+  return f2_fma(e2, r2, y2);
+}
+
+// Two INT8 codes (held as fp16) of x0, x1 for block scale s (r = RN(1/s)):
+// clamp(rint(RN(x / s)), -127, 127), or 0 when s == 0.
+__device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, uint64_t neg_s2, uint64_t r2) {
+  if (s == 0.0f) return 0u;
+  float q0, q1;
+  f2_unpack(div_rn2(f2_pack(x0, x1), neg_s2, r2), q0, q1);
+  q0 = fminf(fmaxf(rintf(q0), -127.0f), 127.0f);
+  q1 = fminf(fmaxf(rintf(q1), -127.0f), 127.0f);
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(q1), "f"(q0));   // integers |q| <= 127: exact
+  return h;
 }
 
 // One CTA per (128-row block b, head h): Q block -> one scale; the same rows of K - mean ->
@@ -199,6 +217,10 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
     a1 = fmaxf(a1, red[2][w]);
   }
   const float qs = aq / 127.0f, ks0 = a0 / 127.0f, ks1 = a1 / 127.0f;
+  const float rq = 1.0f / qs, rk0 = 1.0f / ks0, rk1 = 1.0f / ks1;   // IEEE; unused when a scale is 0
+  const uint64_t nq2 = f2_pack(-qs, -qs), rq2 = f2_pack(rq, rq);
+  const uint64_t nk02 = f2_pack(-ks0, -ks0), rk02 = f2_pack(rk0, rk0);
+  const uint64_t nk12 = f2_pack(-ks1, -ks1), rk12 = f2_pack(rk1, rk1);
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
@@ -206,19 +228,18 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
     unpack8(vq[p], f);
     uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      w[j] = static_cast<uint32_t>(i8code_as_f16(f[2 * j], qs)) |
-             (static_cast<uint32_t>(i8code_as_f16(f[2 * j + 1], qs)) << 16);
+    for (int j = 0; j < 4; ++j) w[j] = i8codes_f16x2(f[2 * j], f[2 * j + 1], qs, nq2, rq2);
     *reinterpret_cast<uint4*>(q_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
         make_uint4(w[0], w[1], w[2], w[3]);
-    const float ks = p < NP / 2 ? ks0 : ks1;
+    const bool lo = p < NP / 2;
+    const float ks = lo ? ks0 : ks1;
+    const uint64_t nk2 = lo ? nk02 : nk12, rk2 = lo ? rk02 : rk12;
     uint32_t u[4] = {0, 0, 0, 0};
     if (row < n) {
       unpack8(vk[p], f);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        u[j] = static_cast<uint32_t>(i8code_as_f16(f[2 * j] - mu[2 * j], ks)) |
-               (static_cast<uint32_t>(i8code_as_f16(f[2 * j + 1] - mu[2 * j + 1], ks)) << 16);
+        u[j] = i8codes_f16x2(f[2 * j] - mu[2 * j], f[2 * j + 1] - mu[2 * j + 1], ks, nk2, rk2);
     }
     *reinterpret_cast<uint4*>(k_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
         make_uint4(u[0], u[1], u[2], u[3]);
@@ -259,9 +280,16 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
   for (int i = 0; i < kItems; ++i) {
     const int it = threadIdx.x + i * 256;
     const int c8 = it % VPR, tg = it / VPR;
-    float sc[8];
+    uint64_t ns2[4], r2[4];
+    bool zero[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sc[j] = v_scales[hh * D + c8 * 8 + j];
+    for (int j = 0; j < 8; j += 2) {
+      const float s0 = v_scales[hh * D + c8 * 8 + j], s1 = v_scales[hh * D + c8 * 8 + j + 1];
+      zero[j] = s0 == 0.0f;
+      zero[j + 1] = s1 == 0.0f;
+      ns2[j / 2] = f2_pack(-s0, -s1);
+      r2[j / 2] = f2_pack(1.0f / s0, 1.0f / s1);   // IEEE; unused when the scale is 0
+    }
     uint32_t bytes[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -270,8 +298,10 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
       unpack8(raw[i][u], f);
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
-        const float y0 = (t < n && sc[j] != 0.0f) ? f[j] / sc[j] : 0.0f;
-        const float y1 = (t < n && sc[j + 1] != 0.0f) ? f[j + 1] / sc[j + 1] : 0.0f;
+        float y0, y1;
+        f2_unpack(div_rn2(f2_pack(f[j], f[j + 1]), ns2[j / 2], r2[j / 2]), y0, y1);
+        if (t >= n || zero[j]) y0 = 0.0f;
+        if (t >= n || zero[j + 1]) y1 = 0.0f;
         const uint32_t pr = e4m3x2(y0, y1);
         bytes[u][j] = pr & 0xFFu;
         bytes[u][j + 1] = pr >> 8;
