@@ -127,6 +127,22 @@ def _dist():
     return world, rank, local
 
 
+def reduce_max(x: float, pg, device=None) -> float:
+    """Max of a per-rank float over the process group (the slowest rank's time)."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs `steps` calls of `flops_per_step`; the job takes the
+    slowest rank's time."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
 def run_gpu(args):
     import torch
     import video_diffusion_transformer_sage_gb300 as sage
@@ -196,16 +212,12 @@ def run_gpu(args):
     code, where = sage.sage_check_device_status(status, stream)
     if code != 0:
         raise RuntimeError(f"device status {code} at {where}")
-    total_ms = t0.elapsed_time(t1)
+    total_ms = reduce_max(t0.elapsed_time(t1), pg, dev)
     quant_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if pg:
-        tt = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
     ms_per_step = total_ms / args.steps
     flops = w.flops
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, args.steps, world, total_ms)
 
     # ---- end to end through the C ABI with host buffers.  Every step copies its QKV input
     # from pinned host memory (H2D), runs the whole path (sage_attn_fwd) and copies the
@@ -255,12 +267,8 @@ def run_gpu(args):
             return a.elapsed_time(b) / steps
 
         run(2, True)
-        e2e_ms = run(e2e_steps, True)
+        e2e_ms = reduce_max(run(e2e_steps, True), pg, dev)
         e2e_serial_ms = run(e2e_steps, False)
-        if pg:
-            tt = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
 
     bf16_burst, bf16_sus, hbm, peak_src = _peaks()
     # The fused kernel does half its FLOPs as fp16 MMAs (QK^T on INT8 codes held in fp16)
@@ -289,7 +297,7 @@ def run_gpu(args):
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
                        "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
                        "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(flops, 1, world, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(host.numel() * 2), "d2h_bytes_per_step": int(host_out[0].numel() * 2),
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
                 "how": "pinned host QKV -> H2D, sage_attn_fwd, D2H -> pinned host each step; copies on their own "

@@ -179,6 +179,12 @@ sage_status sage_debug_qk_int32(int64_t n_tokens, int64_t n_heads, int64_t head_
                                 int64_t row_tiles, int64_t col_tiles, int32_t* out,
                                 void* status_block, void* stream);
 
+/* Test hook for the failure path: one thread waits, with the kernels' bounded mbarrier wait,
+ * on a barrier nothing arrives on.  After limit_ns (1 .. 1e10) nanoseconds the wait gives up
+ * and records SAGE_ERR_DEVICE_TIMEOUT (where = 10) in the status block; nothing faults or
+ * hangs.  Read the result with sage_check_device_status. */
+sage_status sage_debug_wait_timeout(void* status_block, int64_t limit_ns, void* stream);
+
 /* Waits for `stream`, reads the status block (device pointer) and returns SAGE_OK,
  * SAGE_ERR_DEVICE_TIMEOUT (a bounded wait expired; the block is then cleared) or
  * SAGE_ERR_CUDA.  If where != NULL (host), *where receives the code of the wait that

@@ -11,7 +11,7 @@ from video_diffusion_transformer_sage_gb300 import _lib
 EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_bytes", "sage_status_block_bytes",
             "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
             "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
-            "sage_smooth_quant_qk_noalloc"}
+            "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout"}
 
 
 @pytest.fixture(scope="module")
@@ -89,3 +89,5 @@ def test_argument_validation_never_launches(L):
     assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 0, 128, 0, 2, 1, 4096, 4096, None) == 1
     assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 2, 0, 0, 1, 1, 4096, 4096, None) == 1
     assert L.sage_check_device_status(0, None, None) == 1
+    assert L.sage_debug_wait_timeout(0, 1000, None) == 1
+    assert L.sage_debug_wait_timeout(4096, 0, None) == 1

@@ -130,3 +130,48 @@ def test_dense_bf16_matches_exact(name):
     got = out[rows].float().cpu().numpy().astype(np.float64)
     # bf16 output rounding (2^-9 relative) dominates
     assert rel_l2(got, ex) <= 4e-3
+
+
+def test_bounded_wait_expires_into_status():
+    """A device wait that can never be satisfied gives up after its limit and reports
+    SAGE_ERR_DEVICE_TIMEOUT through the status block; the context stays usable."""
+    status = sage.status_block()
+    sage.sage_debug_wait_timeout(status, 50_000_000)          # 50 ms
+    assert sage.sage_check_device_status(status) == (6, 10)
+    assert sage.sage_check_device_status(status) == (0, 0)    # cleared by the read
+    case = gpu_case("tiny")
+    out = sage.sage_attn_fwd(case["q"], case["k"], case["v"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name,rows", [("sweep8192", 16), ("sweep18905", 16), ("sweep75620", 12)])
+def test_sweep_sizes_match_oracle(name, rows):
+    """The sweep of the video workload's sizes (N = 8192 .. 75620, H = 56, D = 128, strided)."""
+    case = gpu_case(name)
+    n, h, d = case["q"].shape
+    sm = 1.0 / math.sqrt(d)
+    qz = _gpu_qz(case)
+    torch.cuda.synchronize()
+    oq = case["qz"]
+    assert np.array_equal(qz.k_mean.cpu().numpy().view(np.uint32), oq.k_mean.view(np.uint32))
+    assert np.array_equal(qz.q_codes.cpu().float().numpy(), oq.q_codes.astype(np.float32))
+    assert np.array_equal(qz.k_codes.cpu().float().numpy(), oq.k_codes.astype(np.float32))
+    assert np.array_equal(qz.v_codes.cpu().numpy(), oq.v_codes)
+    out = sage.sage_attn_fwd_quantized(qz, sm)
+    torch.cuda.synchronize()
+    sel = synth.sample_rows(n, rows, 21)
+    got = out[sel].float().cpu().numpy().astype(np.float64)
+    ref = oracle.attn_sq(oq, sm, sel, tile=128)
+    assert rel_l2(got, ref) <= SQ_REL and np.abs(got - ref).max() <= SQ_ABS
+
+
+def test_hnd_and_strided_layouts_bit_identical_full_size():
+    """At N = 37810, HND-contiguous inputs and strided NHD views of the same values give the
+    same output bytes (the strided-NHD page: isolated_attention_layout.max_abs_difference 0)."""
+    a = gpu_case("sweep37810")
+    b = gpu_case("sweep37810_hndcopy")
+    oa = sage.sage_attn_fwd(a["q"], a["k"], a["v"])
+    ob = sage.sage_attn_fwd(b["q"], b["k"], b["v"])
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))

@@ -72,6 +72,7 @@ def lib():
             "sage_attn_dense_bf16": ([VP, VP, VP, F, P, I, I, P], ctypes.c_int),
             "sage_debug_qk_int32": ([I, I, I, QP, I, I, I, I, I, P, P, P], ctypes.c_int),
             "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            "sage_debug_wait_timeout": ([P, I, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -223,6 +224,10 @@ def sage_debug_qk_int32(qz: Quantized, head: int, i0: int, j0: int, row_tiles: i
     _check(lib().sage_debug_qk_int32(qz.n, qz.h, qz.d, ctypes.byref(c), head, i0, j0, row_tiles, col_tiles,
                                      out.data_ptr(), status.data_ptr(), _stream(stream)), "sage_debug_qk_int32")
     return out
+
+
+def sage_debug_wait_timeout(status: torch.Tensor, limit_ns: int, stream=None) -> None:
+    _check(lib().sage_debug_wait_timeout(status.data_ptr(), int(limit_ns), _stream(stream)), "sage_debug_wait_timeout")
 
 
 def sage_check_device_status(status: torch.Tensor, stream=None):

@@ -496,6 +496,21 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// --------------------------------------------------------------------------- debug: timeout
+// One thread waits, with the same bounded wait as the kernels above, on an mbarrier that
+// nothing ever arrives on.  The wait must give up after `limit` ns and record the timeout
+// in the status block: the test of the failure path, with no fault and no hang.
+__global__ void debug_wait_timeout_kernel(int32_t* status, uint64_t limit) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int s_abort;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, limit)) record_error(status, kWhereDebugTimeout, &s_abort);
+  }
+}
+
 // --------------------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -584,6 +599,11 @@ cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, float
                             int64_t osh, int32_t* status, cudaStream_t s) {
   return d == 128 ? launch_attn_fwd_t<128>(n, h, qz, sm_scale, out, ost, osh, status, s)
                   : launch_attn_fwd_t<64>(n, h, qz, sm_scale, out, ost, osh, status, s);
+}
+
+cudaError_t launch_debug_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t s) {
+  debug_wait_timeout_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,

@@ -225,6 +225,13 @@ sage_status sage_debug_qk_int32(int64_t n, int64_t h, int64_t d, const sage_quan
                                            static_cast<cudaStream_t>(stream)));
 }
 
+sage_status sage_debug_wait_timeout(void* status_block, int64_t limit_ns, void* stream) {
+  if (!status_block || limit_ns <= 0 || limit_ns > 10000000000LL) return SAGE_ERR_INVALID_ARG;
+  return cuda_status(sage::launch_debug_wait_timeout(static_cast<int32_t*>(status_block),
+                                                     static_cast<uint64_t>(limit_ns),
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
 sage_status sage_check_device_status(void* status_block, void* stream, int32_t* where) {
   if (!status_block) return SAGE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -19,6 +19,7 @@ enum DeviceWhere : int32_t {
   kWherePvDone = 6,
   kWhereDebugTma = 7,
   kWhereDebugMma = 8,
+  kWhereDebugTimeout = 10,
 };
 
 struct StridedView {
@@ -44,6 +45,8 @@ cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, float
                             int64_t osh, int32_t* status, cudaStream_t s);
 cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
                             int col_tiles, int32_t* out, int32_t* status, cudaStream_t s);
+
+cudaError_t launch_debug_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 
 // attn_dense.cu
 cudaError_t launch_attn_dense(const StridedView& q, const StridedView& k, const StridedView& v, int n, int h,
