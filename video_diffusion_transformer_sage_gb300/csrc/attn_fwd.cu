@@ -69,9 +69,9 @@ struct Cfg {
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
   static constexpr int kPOffset = 2 * kQTileBytes;
-  static constexpr int kKVOffset = kPOffset + 2 * kPTileBytes;
+  static constexpr int kKVOffset = kPOffset + 4 * kPTileBytes;   // P double-buffered per Q tile
   static constexpr int kBarOffset = kKVOffset + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1;
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 4 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -143,17 +143,21 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t sp, uint32_t 
 //      overwrite it while this tile is still being processed;
 //   2. forms the tile max on raw S per 64-key half (c >= 0 and rounding is monotone, so
 //      max_k fl(S_k c) = fl(c max_k S_k));
-//   3. waits until P.V of the previous tile has finished (it reads the P tile in shared
-//      memory and accumulates into O), then writes P = E4M3(448 p), p = exp2(S c - m_new),
-//      as row r of the 128-byte swizzled K-major P tile;
-//   4. l = alpha l + sum p and, if any row of the warp saw its max rise, multiplies that
-//      row's O by alpha = exp2(m_old - m_new).
+//   3. P is double-buffered: waits until P.V of tile j-2 has finished reading buffer j % 2,
+//      then writes P = E4M3(448 p), p = exp2(S c - m_new), as row r of that 128-byte
+//      swizzled K-major P tile;
+//   4. l = alpha l + sum p and, if any row of the warp saw its max rise, waits for P.V of
+//      tile j-1 (it accumulates into O) and multiplies that row's O by
+//      alpha = exp2(m_old - m_new).
+// pvb[b] completes once per P.V that read buffer b, so each wait names a phase that is at
+// most one ahead of the barrier (no parity aliasing).
 // kTail: keys >= kvalid are excluded from the max and get p = 0.  Returns false if a wait
 // expired.
 template <int D, bool kTail>
 __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* p_row, int r, float c0, float c1,
-                                             int kvalid, bool first, float& m, float& l, uint64_t* s_free,
-                                             uint64_t* pv_prev, uint32_t pv_prev_parity, uint64_t limit) {
+                                             int kvalid, int j, float& m, float& l, uint64_t* s_free,
+                                             uint64_t* pvb, uint64_t limit) {
+  const bool first = j == 0;
   uint32_t sr[128];
   SAGE_TMEM_LD32(tS + 0, (sr + 0));
   SAGE_TMEM_LD32(tS + 32, (sr + 32));
@@ -180,9 +184,8 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* 
   const bool rise = !first && (m_new > m);
   const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
   m = m_new;
-  if (!first) {
-    if (!warp_wait(pv_prev, pv_prev_parity, limit)) return false;
-    tc_fence_after();
+  if (j >= 2) {
+    if (!warp_wait(pvb + (j & 1), ((j >> 1) - 1) & 1, limit)) return false;
   }
   // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA; 16 keys per 16-byte chunk
   // of the P row, chunk c stored at position c ^ (r % 8) (the 128-byte swizzle).
@@ -214,6 +217,8 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* 
   f2_unpack(l2, llo, lhi);
   l = l * alpha + (llo + lhi);
   if (__any_sync(0xffffffffu, rise)) {
+    if (!warp_wait(pvb + ((j - 1) & 1), ((j - 1) >> 1) & 1, limit)) return false;
+    tc_fence_after();
     const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
@@ -254,8 +259,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = kv_empty + C::kStages;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* mma_final = pv_done + 2;
+  uint64_t* pv_done = p_full + 2;       // [t * 2 + b]: P.V of tile t that read P buffer b
+  uint64_t* mma_final = pv_done + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,7 +280,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(s_full + t, 1);
       mbar_init(s_free + t, 128);
       mbar_init(p_full + t, 128);
-      mbar_init(pv_done + t, 1);
+      mbar_init(pv_done + 2 * t, 1);
+      mbar_init(pv_done + 2 * t + 1, 1);
     }
     mbar_init(mma_final, 1);
     fence_mbar_init();
@@ -362,8 +368,9 @@ __global__ void __launch_bounds__(384, 1)
               break;
             }
             tc_fence_after();
-            issue_pv<D>(colO[t], sp + t * C::kPTileBytes, skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
-            tc_commit(pv_done + t);
+            issue_pv<D>(colO[t], sp + (2 * t + (j & 1)) * C::kPTileBytes, skv + s * C::kStageBytes + C::kKTileBytes,
+                        j == 0);
+            tc_commit(pv_done + 2 * t + (j & 1));
             if (t == 1) tc_commit(kv_empty + s);
           }
           if (s_abort) ok = false;
@@ -383,7 +390,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
-    uint8_t* p_row = sP + t * C::kPTileBytes + r * 128;
+    uint8_t* p_rows = sP + 2 * t * C::kPTileBytes + r * 128;   // + (j % 2) * kPTileBytes
     const int nbq = p.npad / 128, nbk = p.npad / 64;
     const int qblk = (q0 + t * kBM) / 128;
     const float qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
@@ -406,12 +413,11 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float c0 = cq * ks0, c1 = cq * ks1;
       const int kvalid = min(kBN, p.n - j * kBN);
+      uint8_t* p_row = p_rows + (j & 1) * C::kPTileBytes;
       const bool done =
           kvalid == kBN
-              ? softmax_step<D, false>(tS, tO, p_row, r, c0, c1, kBN, j == 0, m, l, s_free + t, pv_done + t,
-                                       (j - 1) & 1, limit)
-              : softmax_step<D, true>(tS, tO, p_row, r, c0, c1, kvalid, j == 0, m, l, s_free + t, pv_done + t,
-                                      (j - 1) & 1, limit);
+              ? softmax_step<D, false>(tS, tO, p_row, r, c0, c1, kBN, j, m, l, s_free + t, pv_done + 2 * t, limit)
+              : softmax_step<D, true>(tS, tO, p_row, r, c0, c1, kvalid, j, m, l, s_free + t, pv_done + 2 * t, limit);
       if (!done) {
         if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
         ok = false;
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(p_full + t);
     }
-    if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
+    if (ok && warp_wait(pv_done + 2 * t + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, limit)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const float* vs = p.v_scales + hh * D;
