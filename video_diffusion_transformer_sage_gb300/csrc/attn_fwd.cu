@@ -18,10 +18,8 @@
 //   warps 4-7   softmax + epilogue of tile 0 (thread = row = TMEM lane)
 //   warps 8-11  softmax + epilogue of tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [256+D, 256+2D).
-// P_t (E4M3, 128 x 128) goes to shared memory in the 128-byte swizzled K-major layout and is
-// the A operand of the P.V MMA from there.  S_t is released as soon as the softmax has read
-// it, so Q_t . K(j+1)^T runs while the softmax of tile j is still forming P: the tensor core
-// and the softmax overlap instead of waiting on each other.
+// P_t (E4M3, 4 keys per 32-bit column) overwrites columns [0,32) of S_t and is the A
+// operand of the P.V MMA straight from TMEM.
 //
 // Online softmax with P in E4M3: P is encoded against the current running max, so p <= 1
 // and 448 p never overflows; whenever a row's max rises, O and l of that row are
@@ -61,17 +59,14 @@ struct Cfg {
   static constexpr int kPanels = D / 64;                 // 128-byte swizzle panels per fp16 row
   static constexpr int kPanelBytes = 128 * 128;          // 128 rows x 128 B
   static constexpr int kQTileBytes = kBM * D * 2;
-  static constexpr int kPTileBytes = kBM * kBN;          // E4M3 P, 128 rows x 128 keys
   static constexpr int kKTileBytes = kBN * D * 2;
   static constexpr int kVTileBytes = D * kBN;
   static constexpr int kStageBytes = kKTileBytes + kVTileBytes;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
-  static constexpr int kPOffset = 2 * kQTileBytes;
-  static constexpr int kKVOffset = kPOffset + 4 * kPTileBytes;   // P double-buffered per Q tile
-  static constexpr int kBarOffset = kKVOffset + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 4 + 1;
+  static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -127,45 +122,30 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
   }
 }
 
-// O[tmem] (+)= P_tile(sp) . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3), both operands in
-// shared memory (128-byte swizzled, K-major).
+// O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t sp, uint32_t sv, bool first) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, D);
 #pragma unroll
   for (int kk = 0; kk < kBN / 32; ++kk)
-    mma_f8_ss(o_tmem, sdesc_k_sw128(sp + kk * 32), sdesc_k_sw128(sv + kk * 32), idesc,
-              (first && kk == 0) ? 0u : 1u);
+    mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
 }
 
-// One 128-key tile of the online softmax for the calling thread's row r (= TMEM lane):
-//   1. reads S from TMEM and releases it (s_free), so that Q.K^T of the next key tile can
-//      overwrite it while this tile is still being processed;
-//   2. forms the tile max on raw S per 64-key half (c >= 0 and rounding is monotone, so
-//      max_k fl(S_k c) = fl(c max_k S_k));
-//   3. P is double-buffered: waits until P.V of tile j-2 has finished reading buffer j % 2,
-//      then writes P = E4M3(448 p), p = exp2(S c - m_new), as row r of that 128-byte
-//      swizzled K-major P tile;
-//   4. l = alpha l + sum p and, if any row of the warp saw its max rise, waits for P.V of
-//      tile j-1 (it accumulates into O) and multiplies that row's O by
-//      alpha = exp2(m_old - m_new).
-// pvb[b] completes once per P.V that read buffer b, so each wait names a phase that is at
-// most one ahead of the barrier (no parity aliasing).
-// kTail: keys >= kvalid are excluded from the max and get p = 0.  Returns false if a wait
-// expired.
+// One 128-key tile of the online softmax for the calling thread's row (= TMEM lane):
+//   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
+//   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
+//   p = exp2(S c - m_new) into the first 32 columns of S; l = alpha l + sum p; and, if any row
+//   of the warp saw its max rise, multiplies that row's O by alpha = exp2(m_old - m_new).
+// kTail: keys >= kvalid are excluded from the max and get p = 0.
 template <int D, bool kTail>
-__device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* p_row, int r, float c0, float c1,
-                                             int kvalid, int j, float& m, float& l, uint64_t* s_free,
-                                             uint64_t* pvb, uint64_t limit) {
-  const bool first = j == 0;
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0, float c1, int kvalid, bool first,
+                                             float& m, float& l) {
   uint32_t sr[128];
   SAGE_TMEM_LD32(tS + 0, (sr + 0));
   SAGE_TMEM_LD32(tS + 32, (sr + 32));
   SAGE_TMEM_LD32(tS + 64, (sr + 64));
   SAGE_TMEM_LD32(tS + 96, (sr + 96));
   tmem_wait_ld();
-  tc_fence_before();
-  mbar_arrive(s_free);
   float mx0, mx1;
   if (!kTail) {
     mx0 = block_max64(sr);
@@ -184,21 +164,17 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* 
   const bool rise = !first && (m_new > m);
   const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
   m = m_new;
-  if (j >= 2) {
-    if (!warp_wait(pvb + (j & 1), ((j >> 1) - 1) & 1, limit)) return false;
-  }
-  // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA; 16 keys per 16-byte chunk
-  // of the P row, chunk c stored at position c ^ (r % 8) (the 128-byte swizzle).
+  // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
   const uint64_t bias2 = f2_pack(kLog2_448 - m_new, kLog2_448 - m_new);
   uint64_t l2 = f2_pack(0.0f, 0.0f);
 #pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    const float cb = ch < 4 ? c0 : c1;
+  for (int cch = 0; cch < 4; ++cch) {
+    const float cb = cch < 2 ? c0 : c1;
     const uint64_t cb2 = f2_pack(cb, cb);
-    uint32_t pw[4];
+    uint32_t pw[8];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const int k = ch * 16 + w * 4;
+    for (int w = 0; w < 8; ++w) {
+      const int k = cch * 32 + w * 4;
       float pp[4];
       f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), cb2, bias2), pp[0], pp[1]);
       f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), cb2, bias2), pp[2], pp[3]);
@@ -211,14 +187,14 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* 
       l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
       pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
     }
-    *reinterpret_cast<uint4*>(p_row + ((ch ^ (r & 7)) << 4)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    SAGE_TMEM_ST8(tS + cch * 8, pw);
   }
   float llo, lhi;
   f2_unpack(l2, llo, lhi);
   l = l * alpha + (llo + lhi);
+  // O is rescaled after P is formed, when S no longer occupies registers.  P.V of this tile
+  // is issued only after p_full, so O still holds the previous tiles' sum here.
   if (__any_sync(0xffffffffu, rise)) {
-    if (!warp_wait(pvb + ((j - 1) & 1), ((j - 1) >> 1) & 1, limit)) return false;
-    tc_fence_after();
     const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
@@ -234,10 +210,8 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint8_t* 
       }
       SAGE_TMEM_ST32(tO + c, o);
     }
-    tmem_wait_st();
   }
-  fence_proxy_async_smem();
-  return true;
+  tmem_wait_st();
 }
 
 template <int D>
@@ -250,17 +224,15 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ volatile int s_abort;
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem;
-  uint8_t* sP = smem + C::kPOffset;
-  uint8_t* sKV = smem + C::kKVOffset;
+  uint8_t* sKV = smem + 2 * C::kQTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + C::kStages;
   uint64_t* s_full = kv_empty + C::kStages;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 2;       // [t * 2 + b]: P.V of tile t that read P buffer b
-  uint64_t* mma_final = pv_done + 4;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* mma_final = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -278,10 +250,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
-      mbar_init(s_free + t, 128);
       mbar_init(p_full + t, 128);
-      mbar_init(pv_done + 2 * t, 1);
-      mbar_init(pv_done + 2 * t + 1, 1);
+      mbar_init(pv_done + t, 1);
     }
     mbar_init(mma_final, 1);
     fence_mbar_init();
@@ -326,11 +296,8 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      // Per key tile j and Q tile t: as soon as the softmax has read S_t(j), Q_t . K(j+1)^T
-      // overwrites S_t; as soon as it has written P_t(j), O_t += P_t(j) . V(j).
       if (lane == 0) {
         const uint32_t sq = smem_u32(sQ);
-        const uint32_t sp = smem_u32(sP);
         const uint32_t skv = smem_u32(sKV);
         const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
         const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
@@ -347,14 +314,24 @@ __global__ void __launch_bounds__(384, 1)
           const int s = j % C::kStages;
           const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
           for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(p_full + t, j & 1, limit)) {
+              record_error(p.status, kWherePFull, &s_abort);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            tc_commit(pv_done + t);
+            if (t == 1) tc_commit(kv_empty + s);
             if (j + 1 < ntiles) {
-              if (!mbar_wait(s_free + t, j & 1, limit)) {
-                record_error(p.status, kWhereSFree, &s_abort);
+              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+                record_error(p.status, kWhereKvFull, &s_abort);
                 ok = false;
                 break;
               }
-              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
-                record_error(p.status, kWhereKvFull, &s_abort);
+              // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
+              if (!mbar_wait(pv_done + t, j & 1, limit)) {
+                record_error(p.status, kWherePvDone, &s_abort);
                 ok = false;
                 break;
               }
@@ -362,16 +339,6 @@ __global__ void __launch_bounds__(384, 1)
               issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
               tc_commit(s_full + t);
             }
-            if (!mbar_wait(p_full + t, j & 1, limit)) {
-              record_error(p.status, kWherePFull, &s_abort);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv<D>(colO[t], sp + (2 * t + (j & 1)) * C::kPTileBytes, skv + s * C::kStageBytes + C::kKTileBytes,
-                        j == 0);
-            tc_commit(pv_done + 2 * t + (j & 1));
-            if (t == 1) tc_commit(kv_empty + s);
           }
           if (s_abort) ok = false;
         }
@@ -390,7 +357,6 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
-    uint8_t* p_rows = sP + 2 * t * C::kPTileBytes + r * 128;   // + (j % 2) * kPTileBytes
     const int nbq = p.npad / 128, nbk = p.npad / 64;
     const int qblk = (q0 + t * kBM) / 128;
     const float qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
@@ -413,20 +379,14 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float c0 = cq * ks0, c1 = cq * ks1;
       const int kvalid = min(kBN, p.n - j * kBN);
-      uint8_t* p_row = p_rows + (j & 1) * C::kPTileBytes;
-      const bool done =
-          kvalid == kBN
-              ? softmax_step<D, false>(tS, tO, p_row, r, c0, c1, kBN, j, m, l, s_free + t, pv_done + 2 * t, limit)
-              : softmax_step<D, true>(tS, tO, p_row, r, c0, c1, kvalid, j, m, l, s_free + t, pv_done + 2 * t, limit);
-      if (!done) {
-        if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
-        ok = false;
-        break;
-      }
+      if (kvalid == kBN)
+        softmax_step<D, false>(tS, tO, c0, c1, kBN, j == 0, m, l);
+      else
+        softmax_step<D, true>(tS, tO, c0, c1, kvalid, j == 0, m, l);
       tc_fence_before();
       mbar_arrive(p_full + t);
     }
-    if (ok && warp_wait(pv_done + 2 * t + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, limit)) {
+    if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const float* vs = p.v_scales + hh * D;

@@ -20,7 +20,6 @@ enum DeviceWhere : int32_t {
   kWhereDebugTma = 7,
   kWhereDebugMma = 8,
   kWhereDebugTimeout = 10,
-  kWhereSFree = 11,
 };
 
 struct StridedView {
