@@ -13,7 +13,7 @@
 // CTA = 256 query rows of one head (two 128-row tiles t = 0, 1) and every 128-key tile of
 // that head.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K/V tiles into a kStages-deep ring
-//   warps 1, 3  MMA issuers (one thread each, tile 0 / tile 1): S_t = Q_t K^T, O_t += P_t V
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T, O_t += P_t V
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax + epilogue of tile 0 (thread = row = TMEM lane)
 //   warps 8-11  softmax + epilogue of tile 1
@@ -66,7 +66,7 @@ struct Cfg {
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2;
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 2);   // one commit from each tile's MMA issuer
+      mbar_init(kv_empty + s, 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
@@ -254,7 +254,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(pv_done + t, 1);
     }
     mbar_init(mma_final, 1);
-    mbar_init(mma_final + 1, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -295,52 +294,57 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_2d(sk + C::kKTileBytes, &vmap, kv_full + s, j * kBN, hh * D);
         }
       }
-    } else if (warp == 1 || warp == 3) {
-      // ------------------------------------------------------------ MMA issuers
-      // One thread per Q tile (warp 1: tile 0, warp 3: tile 1), so that each sleeps only on
-      // its own tile's barriers and neither tile's P.V or Q.K^T waits behind the other's.
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        const int t = warp == 1 ? 0 : 1;
-        const uint32_t sq = smem_u32(sQ) + t * C::kQTileBytes;
+        const uint32_t sq = smem_u32(sQ);
         const uint32_t skv = smem_u32(sKV);
-        const uint32_t colS = tmem + (t == 0 ? C::kColS0 : C::kColS1);
-        const uint32_t colO = tmem + (t == 0 ? C::kColO0 : C::kColO1);
+        const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
+        const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
         bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
         if (!ok) record_error(p.status, kWhereQFull, &s_abort);
         if (ok) {
           tc_fence_after();
-          issue_qk<D>(colS, sq, skv);
-          tc_commit(s_full + t);
+          issue_qk<D>(colS[0], sq, skv);
+          tc_commit(s_full + 0);
+          issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
+          tc_commit(s_full + 1);
         }
         for (int j = 0; ok && j < ntiles; ++j) {
           const int s = j % C::kStages;
-          if (!mbar_wait(p_full + t, j & 1, limit)) {
-            record_error(p.status, kWherePFull, &s_abort);
-            break;
-          }
-          tc_fence_after();
-          issue_pv<D>(colO, colS, skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
-          tc_commit(pv_done + t);
-          tc_commit(kv_empty + s);   // the stage is free once both tiles' MMAs on it are done
-          if (j + 1 < ntiles) {
-            if (!mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
-              record_error(p.status, kWhereKvFull, &s_abort);
-              break;
-            }
-            // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
-            if (!mbar_wait(pv_done + t, j & 1, limit)) {
-              record_error(p.status, kWherePvDone, &s_abort);
+          const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(p_full + t, j & 1, limit)) {
+              record_error(p.status, kWherePFull, &s_abort);
+              ok = false;
               break;
             }
             tc_fence_after();
-            issue_qk<D>(colS, sq, skv + ((j + 1) % C::kStages) * C::kStageBytes);
-            tc_commit(s_full + t);
+            issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            tc_commit(pv_done + t);
+            if (t == 1) tc_commit(kv_empty + s);
+            if (j + 1 < ntiles) {
+              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+                record_error(p.status, kWhereKvFull, &s_abort);
+                ok = false;
+                break;
+              }
+              // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
+              if (!mbar_wait(pv_done + t, j & 1, limit)) {
+                record_error(p.status, kWherePvDone, &s_abort);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              tc_commit(s_full + t);
+            }
           }
-          if (s_abort) break;
+          if (s_abort) ok = false;
         }
-        // Drain: every MMA this thread issued has finished before the CTA frees tensor memory.
-        tc_commit(mma_final + t);
-        mbar_wait(mma_final + t, 0, limit);
+        // Drain: every MMA issued above has finished before the CTA frees its tensor memory.
+        tc_commit(mma_final);
+        mbar_wait(mma_final, 0, limit);
       }
     }
   } else {
