@@ -195,21 +195,21 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
   // O is rescaled after P is formed, when S no longer occupies registers.  P.V of this tile
   // is issued only after p_full, so O still holds the previous tiles' sum here.
   if (__any_sync(0xffffffffu, rise)) {
+    // The whole O row in one TMEM round trip: S no longer occupies registers here.
     const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
-      uint32_t o[32];
-      SAGE_TMEM_LD32(tO + c, o);
-      tmem_wait_ld();
+    uint32_t o[D];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        float lo, hi;
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), lo, hi);
-        o[k] = __float_as_uint(lo);
-        o[k + 1] = __float_as_uint(hi);
-      }
-      SAGE_TMEM_ST32(tO + c, o);
+    for (int c = 0; c < D; c += 32) SAGE_TMEM_LD32(tO + c, (o + c));
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < D; k += 2) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), lo, hi);
+      o[k] = __float_as_uint(lo);
+      o[k + 1] = __float_as_uint(hi);
     }
+#pragma unroll
+    for (int c = 0; c < D; c += 32) SAGE_TMEM_ST32(tO + c, (o + c));
   }
   tmem_wait_st();
 }
