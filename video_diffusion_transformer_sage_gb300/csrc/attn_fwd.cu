@@ -13,8 +13,7 @@
 // CTA = 256 query rows of one head (two 128-row tiles t = 0, 1) and every 128-key tile of
 // that head.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K/V tiles into a kStages-deep ring
-//   warp 1      Q.K^T issuer (one thread): S_t = Q_t K^T
-//   warps 4, 8  (lane 0) also issue their tile's O_t += P_t V once P_t is complete
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T, O_t += P_t V
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax + epilogue of tile 0 (thread = row = TMEM lane)
 //   warps 8-11  softmax + epilogue of tile 1
@@ -247,7 +246,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 2);   // one commit from each tile's P.V issuer
+      mbar_init(kv_empty + s, 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
@@ -296,13 +295,12 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     } else if (warp == 1) {
-      // ------------------------------------------------------------ Q.K^T issuer
-      // One thread issues every S_t = Q_t K(j)^T.  P_t lives in S_t's columns, so S_t(j+1)
-      // is issued only after P_t(j).V is done; that P.V is issued by the tile's softmax.
+      // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
         const uint32_t sq = smem_u32(sQ);
         const uint32_t skv = smem_u32(sKV);
         const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
+        const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
         bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
         if (!ok) record_error(p.status, kWhereQFull, &s_abort);
         if (ok) {
@@ -312,21 +310,35 @@ __global__ void __launch_bounds__(384, 1)
           issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
           tc_commit(s_full + 1);
         }
-        for (int j = 0; ok && j + 1 < ntiles; ++j) {
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int s = j % C::kStages;
           const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
-          if (!mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
-            record_error(p.status, kWhereKvFull, &s_abort);
-            break;
-          }
           for (int t = 0; t < 2 && ok; ++t) {
-            if (!mbar_wait(pv_done + t, j & 1, limit)) {
-              record_error(p.status, kWherePvDone, &s_abort);
+            if (!mbar_wait(p_full + t, j & 1, limit)) {
+              record_error(p.status, kWherePFull, &s_abort);
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
-            tc_commit(s_full + t);
+            issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            tc_commit(pv_done + t);
+            if (t == 1) tc_commit(kv_empty + s);
+            if (j + 1 < ntiles) {
+              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+                record_error(p.status, kWhereKvFull, &s_abort);
+                ok = false;
+                break;
+              }
+              // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
+              if (!mbar_wait(pv_done + t, j & 1, limit)) {
+                record_error(p.status, kWherePvDone, &s_abort);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              tc_commit(s_full + t);
+            }
           }
           if (s_abort) ok = false;
         }
@@ -373,29 +385,6 @@ __global__ void __launch_bounds__(384, 1)
         softmax_step<D, true>(tS, tO, c0, c1, kvalid, j == 0, m, l);
       tc_fence_before();
       mbar_arrive(p_full + t);
-      if (wq == 0) {
-        // The tile's first warp issues P_t(j).V(j) once all four warps have written P_t(j).
-        if (!warp_wait(p_full + t, j & 1, limit)) {
-          if (lane == 0) record_error(p.status, kWherePFull, &s_abort);
-          ok = false;
-          break;
-        }
-        const int s = j % C::kStages;
-        // V(j) landed before S_t(j) was computed; waiting on its stage again (it is complete)
-        // makes that ordering explicit for this thread.
-        if (!warp_wait(kv_full + s, (j / C::kStages) & 1, limit)) {
-          if (lane == 0) record_error(p.status, kWhereKvFull, &s_abort);
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          tc_fence_after();
-          issue_pv<D>(tO - lane_base, tS - lane_base, smem_u32(sKV) + s * C::kStageBytes + C::kKTileBytes, j == 0);
-          tc_commit(pv_done + t);
-          tc_commit(kv_empty + s);   // the stage is free once both tiles' P.V on it are done
-        }
-        __syncwarp();
-      }
     }
     if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
       tc_fence_after();
