@@ -105,8 +105,9 @@ size_t sage_status_block_bytes(void);
 
 /* K smoothing and INT8 quantisation of Q and K (the pages' framework_and_k_smoothing and
  * qk_quantize stages).
- *   k_mean[h][c] = fp32( (sum over 128-token chunks, ascending, of the fp32 chunk sum taken
- *                  in ascending token order) / N ), the chunk sums added in fp64;
+ *   k_mean[h][c] = fp32(total / N) in fp64: each 128-token chunk summed in fp32 in
+ *                  ascending token order; the chunk sums summed in fp64 in 8 groups of
+ *                  ceil(chunks / 8) consecutive chunks, the groups added in ascending order;
  *   Q: per (h, 128-row block) scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)),
  *      -127, 127) with IEEE division; an all-zero block has scale 0 and codes 0;
  *   K: the same on fl32(k - k_mean[h][c]) per (h, 64-row block).

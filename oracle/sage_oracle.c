@@ -90,21 +90,27 @@ uint8_t oracle_e4m3_encode(double x) {
  * order of summation.  Reading used here (and in the CUDA path, so that the INT8 K codes
  * can be compared bit for bit): tokens are split into consecutive chunks of 128; each
  * chunk is summed in fp32 in ascending token order starting from 0; the chunk sums are
- * added in fp64 in ascending chunk order; the fp64 total is divided by N in fp64 and
- * rounded once to fp32.
+ * split into 8 groups of G = ceil(chunks / 8) consecutive chunks; each group is summed in
+ * fp64 in ascending chunk order starting from 0; the 8 group sums are added in fp64 in
+ * ascending group order; the total is divided by N in fp64 and rounded once to fp32.
  * ---------------------------------------------------------------------------------- */
 void oracle_k_mean(const uint16_t* k, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
                    float* mu) {
   int64_t nchunk = (n + 127) / 128;
+  int64_t g = (nchunk + 7) / 8;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t hh = 0; hh < h; ++hh) {
     for (int64_t c = 0; c < d; ++c) {
       double total = 0.0;
-      for (int64_t ch = 0; ch < nchunk; ++ch) {
-        float part = 0.0f;
-        int64_t t1 = (ch + 1) * 128 < n ? (ch + 1) * 128 : n;
-        for (int64_t t = ch * 128; t < t1; ++t) part = part + bf16_to_f32(k[t * st + hh * sh + c]);
-        total += (double)part;
+      for (int64_t grp = 0; grp < 8; ++grp) {
+        double gsum = 0.0;
+        for (int64_t ch = grp * g; ch < (grp + 1) * g && ch < nchunk; ++ch) {
+          float part = 0.0f;
+          int64_t t1 = (ch + 1) * 128 < n ? (ch + 1) * 128 : n;
+          for (int64_t t = ch * 128; t < t1; ++t) part = part + bf16_to_f32(k[t * st + hh * sh + c]);
+          gsum += (double)part;
+        }
+        total += gsum;
       }
       double denom = (g_mutation == MUT_MEAN_N_PAD) ? (double)pad128(n) : (double)n;
       mu[hh * d + c] = (float)(total / denom);

@@ -8,8 +8,10 @@
 // strided-NHD dataflow of "gb10-sage-strided-nhd-summary-...json", dataflow.qkv_input).
 //
 // Arithmetic contract (shared with nothing; the CPU oracle restates it independently):
-//  * K mean: fp32 sum of each 128-token chunk in ascending token order, chunk sums added in
-//    fp64 in ascending chunk order, divided by N in fp64, rounded once to fp32.
+//  * K mean: fp32 sum of each 128-token chunk in ascending token order; the chunk sums are
+//    split into 8 groups of ceil(chunks / 8) consecutive chunks, each group summed in fp64 in
+//    ascending order, the 8 group sums added in fp64 in ascending order; divided by N in
+//    fp64, rounded once to fp32.
 //  * INT8: scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)), -127, 127), IEEE
 //    division; all-zero block -> scale 0, codes 0.  K uses fl32(k - mean).
 //  * E4M3: scale = fl32(amax / 448), code = cvt.rn.satfinite.e4m3(fl32(v / scale)).
@@ -79,33 +81,49 @@ __global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restri
 }
 
 // ---------------------------------------------------------------------------- finalise
-// 32 columns per CTA: 8 warps stage chunk partials in shared memory (coalesced), then
-// warp 0 folds them per column in ascending chunk order.
+// 32 columns per CTA.  The chunk partials are split into 8 groups of G = ceil(nchunk / 8)
+// consecutive chunks; warp w folds group w in ascending chunk order (fp64 for sums), then
+// warp 0 folds the 8 group results in ascending group order.  Mean = fp32(total / N).
 template <bool kAbsMax>
 __global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__ partials, int nchunk, int cols,
                                                        int n, float* __restrict__ out) {
-  constexpr int kBatch = 128;
-  __shared__ float stage[kBatch][33];
+  __shared__ double gsum[8][32];
+  __shared__ float gmax[8][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int col = blockIdx.x * 32 + lane;
+  const int g = (nchunk + 7) / 8;
+  const int c0 = warp * g, c1 = min(nchunk, c0 + g);
   double total = 0.0;
   float amax = 0.0f;
-  for (int c0 = 0; c0 < nchunk; c0 += kBatch) {
-    const int cb = min(kBatch, nchunk - c0);
-    for (int c = warp; c < cb; c += 8)
-      stage[c][lane] = col < cols ? partials[static_cast<int64_t>(c0 + c) * cols + col] : 0.0f;
-    __syncthreads();
-    if (warp == 0) {
-      for (int c = 0; c < cb; ++c) {
-        if (kAbsMax)
-          amax = fmaxf(amax, stage[c][lane]);
-        else
-          total += static_cast<double>(stage[c][lane]);
+  if (col < cols) {
+    for (int c = c0; c < c1; c += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = c + u < c1 ? partials[static_cast<int64_t>(c + u) * cols + col] : 0.0f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c + u < c1) {
+          if (kAbsMax)
+            amax = fmaxf(amax, v[u]);
+          else
+            total += static_cast<double>(v[u]);
+        }
       }
     }
-    __syncthreads();
   }
-  if (warp == 0 && col < cols) out[col] = kAbsMax ? amax / 448.0f : static_cast<float>(total / static_cast<double>(n));
+  gsum[warp][lane] = total;
+  gmax[warp][lane] = amax;
+  __syncthreads();
+  if (warp == 0 && col < cols) {
+    double t = 0.0;
+    float m = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      t += gsum[w][lane];
+      m = fmaxf(m, gmax[w][lane]);
+    }
+    out[col] = kAbsMax ? m / 448.0f : static_cast<float>(t / static_cast<double>(n));
+  }
 }
 
 // ---------------------------------------------------------------------------- kernel Q
@@ -147,10 +165,10 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
   return h;
 }
 
-// One CTA per (128-row block b, head h): Q block -> one scale; the same rows of K - mean ->
-// two 64-row blocks, one scale each.  Pad rows (>= n) are excluded from the maxima and
-// written as code 0.  All Q and K loads of the block are issued before any arithmetic so
-// that 32 KB per CTA are in flight; the three maxima share one block reduction.
+// One CTA per (head h, 128-row block b, operand): z = 0 quantises the Q block with one
+// scale; z = 1 quantises the same rows of K - mean as two 64-row blocks, one scale each.
+// Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
+// all its loads before any arithmetic; the maxima share one block reduction.
 template <int D>
 __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
                                                        const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
@@ -161,93 +179,95 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
   constexpr int VPR = D / 8;            // vectors per row
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
-  __shared__ float red[3][8];
+  __shared__ float red[2][8];
   const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
+  const bool is_k = blockIdx.z != 0;
   const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
   const int row0 = b * 128;
+  const uint16_t* src = is_k ? k : q;
+  const int64_t st = is_k ? kst : qst, sh = is_k ? ksh : qsh;
 
-  uint4 vq[NP], vk[NP];
+  uint4 v[NP];
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
-    vq[p] = row < n ? ld_stream(q + static_cast<int64_t>(row) * qst + hh * qsh + c8 * 8) : make_uint4(0, 0, 0, 0);
-    vk[p] = row < n ? ld_stream(k + static_cast<int64_t>(row) * kst + hh * ksh + c8 * 8) : make_uint4(0, 0, 0, 0);
+    v[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
   }
   float mu[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) mu[j] = k_mean[hh * D + c8 * 8 + j];
+  for (int j = 0; j < 8; ++j) mu[j] = is_k ? k_mean[hh * D + c8 * 8 + j] : 0.0f;
 
-  // |q| max on the bf16 bit patterns: for finite values, magnitude order = unsigned order
-  // of the bits without the sign.
-  uint32_t qbits = 0;
+  // Q: |x| max on the bf16 bit patterns (for finite values magnitude order = unsigned order
+  // of the bits without the sign).  K: max |k - mean| per 64-row half, over valid rows.
   float am[2] = {0.0f, 0.0f};
+  if (!is_k) {
+    uint32_t qbits = 0;
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    qbits = __vmaxu2(qbits, vq[p].x & 0x7FFF7FFFu);
-    qbits = __vmaxu2(qbits, vq[p].y & 0x7FFF7FFFu);
-    qbits = __vmaxu2(qbits, vq[p].z & 0x7FFF7FFFu);
-    qbits = __vmaxu2(qbits, vq[p].w & 0x7FFF7FFFu);
-    const int row = row0 + p * RPP + rin;
-    if (row < n) {
-      float f[8];
-      unpack8(vk[p], f);
+    for (int p = 0; p < NP; ++p) {
+      qbits = __vmaxu2(qbits, v[p].x & 0x7FFF7FFFu);
+      qbits = __vmaxu2(qbits, v[p].y & 0x7FFF7FFFu);
+      qbits = __vmaxu2(qbits, v[p].z & 0x7FFF7FFFu);
+      qbits = __vmaxu2(qbits, v[p].w & 0x7FFF7FFFu);
+    }
+    am[0] = am[1] = fmaxf(__uint_as_float((qbits & 0xFFFFu) << 16), __uint_as_float(qbits & 0xFFFF0000u));
+  } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) am[p >= NP / 2] = fmaxf(am[p >= NP / 2], fabsf(f[j] - mu[j]));
+    for (int p = 0; p < NP; ++p) {
+      if (row0 + p * RPP + rin < n) {
+        float f[8];
+        unpack8(v[p], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) am[p >= NP / 2] = fmaxf(am[p >= NP / 2], fabsf(f[j] - mu[j]));
+      }
     }
   }
-  float aq = fmaxf(__uint_as_float((qbits & 0xFFFFu) << 16), __uint_as_float(qbits & 0xFFFF0000u));
   float a0 = am[0], a1 = am[1];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    aq = fmaxf(aq, __shfl_xor_sync(0xffffffffu, aq, o));
     a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, o));
     a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, o));
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
-    red[0][warp] = aq;
-    red[1][warp] = a0;
-    red[2][warp] = a1;
+    red[0][warp] = a0;
+    red[1][warp] = a1;
   }
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    aq = fmaxf(aq, red[0][w]);
-    a0 = fmaxf(a0, red[1][w]);
-    a1 = fmaxf(a1, red[2][w]);
+    a0 = fmaxf(a0, red[0][w]);
+    a1 = fmaxf(a1, red[1][w]);
   }
-  const float qs = aq / 127.0f, ks0 = a0 / 127.0f, ks1 = a1 / 127.0f;
-  const float rq = 1.0f / qs, rk0 = 1.0f / ks0, rk1 = 1.0f / ks1;   // IEEE; unused when a scale is 0
-  const uint64_t nq2 = f2_pack(-qs, -qs), rq2 = f2_pack(rq, rq);
-  const uint64_t nk02 = f2_pack(-ks0, -ks0), rk02 = f2_pack(rk0, rk0);
-  const uint64_t nk12 = f2_pack(-ks1, -ks1), rk12 = f2_pack(rk1, rk1);
+  // Q: one scale (a0 == a1); K: one per 64-row half.
+  const float s0 = a0 / 127.0f, s1 = a1 / 127.0f;
+  const float r0 = 1.0f / s0, r1 = 1.0f / s1;   // IEEE; unused when a scale is 0
+  const uint64_t ns02 = f2_pack(-s0, -s0), r02 = f2_pack(r0, r0);
+  const uint64_t ns12 = f2_pack(-s1, -s1), r12 = f2_pack(r1, r1);
+  uint16_t* dst = is_k ? k_codes : q_codes;
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
-    float f[8];
-    unpack8(vq[p], f);
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = i8codes_f16x2(f[2 * j], f[2 * j + 1], qs, nq2, rq2);
-    *reinterpret_cast<uint4*>(q_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
-        make_uint4(w[0], w[1], w[2], w[3]);
     const bool lo = p < NP / 2;
-    const float ks = lo ? ks0 : ks1;
-    const uint64_t nk2 = lo ? nk02 : nk12, rk2 = lo ? rk02 : rk12;
-    uint32_t u[4] = {0, 0, 0, 0};
+    const float sc = lo ? s0 : s1;
+    const uint64_t ns2 = lo ? ns02 : ns12, rr2 = lo ? r02 : r12;
+    uint32_t w[4] = {0, 0, 0, 0};
     if (row < n) {
-      unpack8(vk[p], f);
+      float f[8];
+      unpack8(v[p], f);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        u[j] = i8codes_f16x2(f[2 * j] - mu[2 * j], f[2 * j + 1] - mu[2 * j + 1], ks, nk2, rk2);
+        w[j] = i8codes_f16x2(f[2 * j] - mu[2 * j], f[2 * j + 1] - mu[2 * j + 1], sc, ns2, rr2);
     }
-    *reinterpret_cast<uint4*>(k_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
-        make_uint4(u[0], u[1], u[2], u[3]);
+    *reinterpret_cast<uint4*>(dst + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (threadIdx.x == 0) {
-    q_scales[hh * (npad / 128) + b] = qs;
-    k_scales[hh * (npad / 64) + 2 * b] = ks0;
-    k_scales[hh * (npad / 64) + 2 * b + 1] = ks1;
+    if (is_k) {
+      k_scales[hh * (npad / 64) + 2 * b] = s0;
+      k_scales[hh * (npad / 64) + 2 * b + 1] = s1;
+    } else {
+      q_scales[hh * (npad / 128) + b] = s0;
+    }
   }
 }
 
@@ -347,7 +367,7 @@ cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const fl
                             uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                             cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
-  dim3 grid(h, npad / 128);
+  dim3 grid(h, npad / 128, 2);
   if (d == 128)
     quant_qk_kernel<128><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, q_codes,
                                               q_scales, k_codes, k_scales);
