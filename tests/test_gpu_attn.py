@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.brute
 import video_diffusion_transformer_sage_gb300 as sage
 from conftest import gpu_case
 from video_diffusion_transformer_sage_gb300 import synth
@@ -175,3 +176,32 @@ def test_hnd_and_strided_layouts_bit_identical_full_size():
     ob = sage.sage_attn_fwd(b["q"], b["k"], b["v"])
     torch.cuda.synchronize()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+
+
+EDGE = [(1, 1, 128), (1, 2, 64), (127, 1, 128), (129, 3, 64), (255, 2, 128), (257, 1, 64), (384, 2, 128)]
+
+
+@pytest.mark.parametrize("n,h,d", EDGE)
+def test_edge_shapes_match_oracle(n, h, d):
+    """Degenerate and boundary sizes: a single token (softmax over one key, O = that key's
+    dequantised V), one partial tile, one key past a tile boundary, a second Q tile that
+    lies entirely in the padding."""
+    inp = synth.make_inputs(synth.custom(n, h, d, "qkv", seed=n + 31 * h + d, n_outlier=1))
+    qz_o = oracle.Quantized(inp.q, inp.k, inp.v)
+    st = inp.storage.to("cuda")
+    hd = h * d
+    q, k, v = (st[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    sm = 1.0 / math.sqrt(d)
+    qz = _gpu_qz({"q": q, "k": k, "v": v})
+    status = sage.status_block()
+    out = sage.sage_attn_fwd_quantized(qz, sm, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    assert np.array_equal(qz.q_codes.cpu().float().numpy(), qz_o.q_codes.astype(np.float32))
+    assert np.array_equal(qz.k_codes.cpu().float().numpy(), qz_o.k_codes.astype(np.float32))
+    assert np.array_equal(qz.v_codes.cpu().numpy(), qz_o.v_codes)
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = oracle.attn_sq(qz_o, sm, list(range(n)), tile=128)
+    assert rel_l2(got, ref) <= SQ_REL and np.abs(got - ref).max() <= SQ_ABS
+    if n == 1:
+        vdeq = oracle.brute.e4m3_decode(qz_o.v_codes[:, :, 0]) * qz_o.v_scales      # [H, D]
+        assert np.abs(got[0] - vdeq).max() <= 1e-2 * np.abs(vdeq).max()
