@@ -161,13 +161,15 @@ def run_gpu(args):
     w = synth.WORKLOADS[args.workload]
     n, h, d = w.n_tokens, w.n_heads, w.head_dim
     inp = synth.make_inputs(w)
-    if w.layout != "qkv":
-        raise SystemExit("bench.py times strided views of a token-major QKV buffer")
+    if w.layout not in ("qkv", "hnd"):
+        raise SystemExit("bench.py times a token-major QKV buffer or HND-contiguous Q, K, V")
     host = inp.storage.pin_memory()
     storage = host.to(dev)
     hd = h * d
 
     def views(buf):
+        if w.layout == "hnd":          # [3, H, N, D] -> three [N, H, D] views
+            return [buf[i].transpose(0, 1) for i in range(3)]
         return [buf[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3)]
 
     q, k, v = views(storage)
@@ -292,8 +294,9 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16(int8 codes)xfp16 + e4m3xe4m3 -> fp32, bf16 io",
         "data": "synthetic (seeded, distributions of the pages' workload)",
-        "config": {"workload": f"{w.name}: N={n}, H={h}, D={d}, batch 1, non-causal, "
-                               f"strided NHD views of a [{n}, {3 * h * d}] bf16 QKV buffer",
+        "config": {"workload": f"{w.name}: N={n}, H={h}, D={d}, batch 1, non-causal, " + (
+                               "HND-contiguous bf16 Q, K, V" if w.layout == "hnd" else
+                               f"strided NHD views of a [{n}, {3 * h * d}] bf16 QKV buffer"),
                    "l2": "inputs larger than L2 (1.63 GB QKV buffer)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(composite, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / composite, 4), "traffic": traffic,
