@@ -55,7 +55,7 @@ def lib():
             L.oracle_quant_k.argtypes = [P, I, I, I, I, I, P, P, P]
             L.oracle_quant_v.argtypes = [P, I, I, I, I, I, P, P]
             L.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, I, I, I, P]
-            L.oracle_attn_sq.argtypes = [P, P, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, P]
+            L.oracle_attn_sq.argtypes = [P, P, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
             L.oracle_attn_exact.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double,
                                             P, I, P]
             L.oracle_num_threads.restype = ctypes.c_int
@@ -158,13 +158,19 @@ def qk_int32(qz: Quantized, head: int, i0: int, j0: int, rows: int, cols: int) -
     return out
 
 
-def attn_sq(qz: Quantized, sm_scale: float, rows, tile: int = 128) -> np.ndarray:
-    """Same-quantisation attention O_sq for query `rows` (all heads): [len(rows), H, D] fp64."""
+def attn_sq(qz: Quantized, sm_scale: float, rows, tile: int = 128, score_f32=None) -> np.ndarray:
+    """Same-quantisation attention O_sq for query `rows` (all heads): [len(rows), H, D] fp64.
+
+    tile=0: the fp64 one-pass definition.  tile>0: the online schedule over `tile`-key tiles;
+    by default (score_f32=None -> True for tile>0) the E4M3 rounding of P is decided on fp32
+    scores formed as the kernel forms them; score_f32=False keeps those scores in fp64."""
+    if score_f32 is None:
+        score_f32 = tile > 0
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     out = np.zeros((len(rows), qz.h, qz.d), np.float64)
     lib().oracle_attn_sq(_ptr(qz.q_codes), _ptr(qz.q_scales), _ptr(qz.k_codes), _ptr(qz.k_scales),
                          _ptr(qz.v_codes), _ptr(qz.v_scales), qz.n, qz.h, qz.d, float(sm_scale),
-                         _ptr(rows), len(rows), int(tile), _ptr(out))
+                         _ptr(rows), len(rows), int(tile), int(bool(score_f32)), _ptr(out))
     return out
 
 

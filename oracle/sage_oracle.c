@@ -225,29 +225,35 @@ void oracle_qk_int32(const int8_t* qc, const int8_t* kc, int64_t n, int64_t h, i
 
 /* ------------------------------------------------------------------------------------
  * 6-8. Same-quantisation attention for selected query rows (all heads).
- *   s_ij = S_ij * s_q[h, i/128] * s_k[h, j/64] * sm_scale            (fp64)
- *   p_ij = exp(s_ij - m_i)                                             (fp64)
- *   P8_ij = E4M3(448 * p_ij) / 448       (static scale 448: p <= 1 never overflows)
- *   l_i  = sum_j p_ij                    (unquantised p)
+ *   s_ij = S_ij * s_q[h, i/128] * s_k[h, j/64] * sm_scale
+ *   p_ij = exp(s_ij - m_i);  P8_ij = E4M3(448 p_ij)  (static scale 448: p <= 1 never overflows)
+ *   l_i  = sum_j 448 p_ij                (unquantised p)
  *   O_ic = (sum_j P8_ij * E4M3val(vc[h,c,j])) * s_v[h,c] / l_i
- * tile == 0: m_i is the row's global max (one pass).
- * tile  > 0: keys are visited in tiles of `tile`; m_i is the running max up to the current
- *   tile, P8 is formed against it, and whenever m_i rises the partial sums (O and l) are
- *   multiplied by exp(m_old - m_new) in fp64 -- an exact rescale on every increase, the
- *   schedule of an online-softmax kernel that holds P in E4M3.
+ * tile == 0 (the definition, fp64): m_i is the row's global max, all arithmetic in fp64.
+ * tile  > 0: keys are visited in tiles of `tile` keys; m_i is the running max up to the
+ *   current tile, P8 is formed against it, and whenever m_i rises the partial sums (O, l)
+ *   are multiplied by exp(m_old - m_new) -- an exact rescale on every increase, the schedule
+ *   of an online-softmax kernel that holds P in E4M3.
+ *   score_f32 == 0: scores and exponents in fp64.
+ *   score_f32 != 0: the discrete step (the E4M3 rounding of 448 p) is taken in the kernel's
+ *   precision: in base 2, x = fma_f32(S, c_b, fl32(log2(448) - m)) with
+ *   c_b = fl32(fl32(s_q * fl32(sm_scale * log2 e)) * s_k[b]), m the fp32 running max of
+ *   fl32(c_b * max S over each 64-key half), and 448 p = RN_f32(2^x); sums stay in fp64.
  * out[r][h][c] (fp64).
  * ---------------------------------------------------------------------------------- */
 void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const float* ks,
                     const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
                     double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
-                    double* out) {
+                    int64_t score_f32, double* out) {
   int64_t np = pad128(n), nbq = np / 128, nbk = np / 64;
   int64_t nkeys = (g_mutation == MUT_DROP_LAST_KEY) ? n - 1 : n;
+  const float kLog2E = 1.4426950408889634f, kLog2_448 = 8.807354922057604f;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t rh = 0; rh < nrows * h; ++rh) {
     int64_t r = rh / h, hh = rh % h, i = rows[r];
     double* o = (double*)calloc((size_t)d, sizeof(double));
     double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    int64_t* S = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
     const int8_t* a = qc + (hh * np + i) * d;
     double sq = (double)qs[hh * nbq + i / 128];
     for (int64_t j = 0; j < nkeys; ++j) {
@@ -255,14 +261,49 @@ void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const f
       const int8_t* b = kc + (hh * np + jj) * d;
       int64_t acc = 0;
       for (int64_t c = 0; c < d; ++c) acc += (int64_t)a[c] * (int64_t)b[c];
+      S[j] = acc;
       s[j] = (double)acc * sq * (double)ks[hh * nbk + j / 64] * sm_scale;
     }
     double m = -INFINITY, l = 0.0;
+    float mf = -INFINITY;
     int64_t tw = tile > 0 ? tile : nkeys;
     if (tile <= 0)
       for (int64_t j = 0; j < nkeys; ++j) if (s[j] > m) m = s[j];
+    const float cq = qs[hh * nbq + i / 128] * ((float)sm_scale * kLog2E);
     for (int64_t j0 = 0; j0 < nkeys; j0 += tw) {
       int64_t j1 = j0 + tw < nkeys ? j0 + tw : nkeys;
+      if (tile > 0 && score_f32) {
+        float mt = -INFINITY;
+        for (int64_t h0 = j0; h0 < j1; h0 += 64) {       /* 64-key halves, one K scale each */
+          int64_t h1 = h0 + 64 < j1 ? h0 + 64 : j1;
+          float mx = -INFINITY;
+          for (int64_t j = h0; j < h1; ++j) if ((float)S[j] > mx) mx = (float)S[j];
+          float cb = cq * ks[hh * nbk + h0 / 64];
+          float v = cb * mx;
+          if (v > mt) mt = v;
+        }
+        if (mt > mf) {
+          if (mf != -INFINITY) {
+            float dm = (g_mutation == MUT_RESCALE_SIGN) ? mt - mf : mf - mt;
+            double alpha = exp2((double)dm);
+            for (int64_t c = 0; c < d; ++c) o[c] *= alpha;
+            l *= alpha;
+          }
+          mf = mt;
+        }
+        const float bias = kLog2_448 - mf;
+        for (int64_t j = j0; j < j1; ++j) {
+          float cb = cq * ks[hh * nbk + j / 64];
+          float x = fmaf((float)S[j], cb, bias);
+          float pp = (float)exp2((double)x);             /* 448 p, rounded to fp32 */
+          l += (double)pp;
+          double p8 = oracle_e4m3_decode(oracle_e4m3_encode((double)pp));
+          if (p8 == 0.0) continue;
+          for (int64_t c = 0; c < d; ++c)
+            o[c] += p8 * oracle_e4m3_decode(vc[(hh * d + c) * np + j]);
+        }
+        continue;
+      }
       if (tile > 0) {
         double mt = -INFINITY;
         for (int64_t j = j0; j < j1; ++j) if (s[j] > mt) mt = s[j];
@@ -277,7 +318,7 @@ void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const f
       }
       for (int64_t j = j0; j < j1; ++j) {
         double p = exp(s[j] - m);
-        l += p;
+        l += 448.0 * p;
         double p8 = oracle_e4m3_decode(oracle_e4m3_encode(448.0 * p));
         if (p8 == 0.0) continue;
         for (int64_t c = 0; c < d; ++c)
@@ -285,9 +326,10 @@ void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const f
       }
     }
     for (int64_t c = 0; c < d; ++c)
-      out[(r * h + hh) * d + c] = o[c] * (double)vs[hh * d + c] / (448.0 * l);
+      out[(r * h + hh) * d + c] = o[c] * (double)vs[hh * d + c] / l;
     free(o);
     free(s);
+    free(S);
   }
 }
 

@@ -251,9 +251,22 @@ def test_attn_sq_single_tile_equals_global(oracle_lib):
     inp = small_inputs(n=128, h=2, d=64, layout="nhd")
     qz = oracle.Quantized(inp.q, inp.k, inp.v)
     rows = list(range(128))
-    a = oracle.attn_sq(qz, 0.125, rows, tile=128)
+    a = oracle.attn_sq(qz, 0.125, rows, tile=128, score_f32=False)
     b = oracle.attn_sq(qz, 0.125, rows, tile=0)
     assert (a == b).all()
+
+
+@pytest.mark.parametrize("name", ["tiny", "tails"])
+def test_attn_sq_fp32_scores_close_to_fp64_scores(oracle_lib, name):
+    """Forming the scores as the kernel does (fp32) moves only the rare P whose 448 p lies
+    within fp32 rounding of an E4M3 rounding boundary."""
+    inp = synth.make_inputs(name)
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    rows = synth.sample_rows(inp.q.shape[0], 64, 3)
+    sm = 1 / math.sqrt(128)
+    a = oracle.attn_sq(qz, sm, rows, tile=128, score_f32=True)
+    b = oracle.attn_sq(qz, sm, rows, tile=128, score_f32=False)
+    assert rel_l2(a, b) < 2e-3
 
 
 def _tiled_exact_case_error() -> float:
@@ -275,7 +288,7 @@ def _tiled_exact_case_error() -> float:
     qz.q_scales[:] = 1.0
     qz.k_scales[:] = 1.0
     rows = [0, 5, 200]
-    t = oracle.attn_sq(qz, math.log(2.0), rows, tile=128)
+    t = oracle.attn_sq(qz, math.log(2.0), rows, tile=128, score_f32=False)
     gl = oracle.attn_sq(qz, math.log(2.0), rows, tile=0)
     w = 2.0 ** (kexp - kexp.max())
     vdeq = brute.e4m3_decode(qz.v_codes[0, :, :n]) * qz.v_scales[0][:, None]   # [D, N]
@@ -338,6 +351,9 @@ def _pins_pass(inp) -> bool:
     if not np.abs(gl - g).max() < 1e-12:
         return False
     if not _tiled_exact_case_error() < 1e-12:
+        return False
+    t32 = oracle.attn_sq(qz, 0.125, rows, tile=128, score_f32=True)
+    if not rel_l2(t32, g) < 0.1:
         return False
     e = oracle.attn_exact(inp.q, inp.k, inp.v, 0.125, rows)
     b = brute.attn_exact(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), 0.125)
