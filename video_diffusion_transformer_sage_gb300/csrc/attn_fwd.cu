@@ -70,7 +70,7 @@ struct Cfg {
   static constexpr int kColS = 0, kColO = 256;     // S_t buffer b at t * 128 + b * 64; O_t at 256 + t * D
   static constexpr int kTmemCols = 512;
   static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 + 4 + 1;
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 4 + 4 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -234,8 +234,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + C::kStages;
   uint64_t* s_full = kv_empty + C::kStages;   // [t * 2 + b]: S_t buffer b holds Q_t K^T of a new step
-  uint64_t* p_full = s_full + 4;              // [t]: the softmax of tile t wrote P for the step
-  uint64_t* pv_done = p_full + 2;             // [t * 2 + b]: P.V of tile t that read buffer b is done
+  // [t * 2 + b]: the softmax of tile t wrote P into buffer b.  One barrier per buffer: the
+  // softmax may finish steps g and g+1 before the MMA thread looks at step g, but step g+2
+  // needs S(g+2), which needs P(g).V -- so a barrier is never two phases ahead of its waiter.
+  uint64_t* p_full = s_full + 4;
+  uint64_t* pv_done = p_full + 4;             // [t * 2 + b]: P.V of tile t that read buffer b is done
   uint64_t* mma_final = pv_done + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
@@ -255,10 +258,9 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 128);
       mbar_init(pv_done + i, 1);
     }
-    mbar_init(p_full + 0, 128);
-    mbar_init(p_full + 1, 128);
     mbar_init(mma_final, 1);
     fence_mbar_init();
   }
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int g = 0; ok && g < nsteps; ++g) {
           const int j = g >> 1, h = g & 1, s = j % C::kStages;
           for (int t = 0; t < 2; ++t) {
-            if (!mbar_wait(p_full + t, g & 1, limit)) {
+            if (!mbar_wait(p_full + 2 * t + h, (g >> 1) & 1, limit)) {
               record_error(p.status, kWherePFull, &s_abort);
               ok = false;
               break;
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(384, 1)
         break;
       }
       tc_fence_before();
-      mbar_arrive(p_full + t);
+      mbar_arrive(p_full + 2 * t + b);
     }
     if (ok && warp_wait(pvb + ((nsteps - 1) & 1), ((nsteps - 1) >> 1) & 1, limit)) {
       tc_fence_after();
