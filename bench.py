@@ -340,7 +340,7 @@ def cpu_baseline(inp, budget_s: float = 20.0, rows_per_step: int = 8, steps: int
     while (steps and i < steps) or (not steps and (t_attn < budget_s or done == 0)):
         rows = [pool[(i * rows_per_step + r) % len(pool)] for r in range(rows_per_step)]
         t = time.perf_counter()
-        oracle.attn_sq(qz, 1.0 / math.sqrt(d), rows, tile=64)
+        oracle.attn_sq(qz, 1.0 / math.sqrt(d), rows, tile=128)
         t_attn += time.perf_counter() - t
         done += rows_per_step
         i += 1

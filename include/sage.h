@@ -144,7 +144,7 @@ sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws,
 
 /* Fused attention on quantised operands (the pages' attention_forward stage):
  *   s_ij = S_ij * q_scales[h][i/128] * k_scales[h][j/64] * sm_scale,  S = exact integer QK^T
- *   running row max m over 64-key steps; p = exp(s - m); P8 = E4M3(448 p);
+ *   running row max m over 128-key tiles; p = exp(s - m); P8 = E4M3(448 p);
  *   l = sum of fp32 p; O and l are multiplied by exp(m_old - m_new) whenever m rises;
  *   out[i][h][c] = bf16_rn( (sum_j P8_ij * v_codes[h][c][j]) * v_scales[h][c] / (448 l) ).
  * out: bf16, element (t, h, c) at out[t * out_stride_token + h * out_stride_head + c];

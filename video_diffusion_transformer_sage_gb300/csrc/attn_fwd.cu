@@ -10,19 +10,16 @@
 // threads per CTA; "gb10-sage2-p0-interleave-softmax-latency.json", key scheduler) is prior
 // art only: this kernel is organised around Blackwell's tensor memory instead.
 //
-// CTA = 256 query rows of one head (two 128-row tiles t = 0, 1) and every 128-key K/V tile
-// of that head, consumed in 64-key softmax steps (step g = half g % 2 of tile g / 2).
-// Warp roles (384 threads):
+// CTA = 256 query rows of one head (two 128-row tiles t = 0, 1) and every 128-key tile of
+// that head.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K/V tiles into a kStages-deep ring
 //   warp 1      MMA issuer (one thread): S_t = Q_t K^T, O_t += P_t V
 //   warp 2      TMEM allocator
 //   warps 4-7   softmax + epilogue of tile 0 (thread = row = TMEM lane)
 //   warps 8-11  softmax + epilogue of tile 1
-// TMEM columns: S_t has two 64-column buffers, [128 t, 128 t + 64) and [128 t + 64, 128 t + 128);
-// O_0 [256, 256+D), O_1 [256+D, 256+2D).  Step g uses buffer g % 2.  P_t (E4M3, 4 keys per
-// 32-bit column) overwrites the first 16 columns of its S buffer and is the A operand of the
-// P.V MMA straight from TMEM.  Because S is double-buffered, Q.K^T for step g+2 is computed
-// while the softmax works on steps g and g+1: the tensor core and the softmax overlap.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [256+D, 256+2D).
+// P_t (E4M3, 4 keys per 32-bit column) overwrites columns [0,32) of S_t and is the A
+// operand of the P.V MMA straight from TMEM.
 //
 // Online softmax with P in E4M3: P is encoded against the current running max, so p <= 1
 // and 448 p never overflows; whenever a row's max rises, O and l of that row are
@@ -52,8 +49,7 @@ constexpr int kBM = 128;   // query rows per tile
 // granted.
 constexpr int kRegsLaunch = 168, kRegsRoles = 56, kRegsSoftmax = 224;
 static_assert(128 * kRegsRoles + 256 * kRegsSoftmax <= 384 * kRegsLaunch, "register split exceeds launch");
-constexpr int kBN = 128;   // keys per K/V tile (one TMA stage)
-constexpr int kBS = 64;    // keys per softmax step (half a K/V tile)
+constexpr int kBN = 128;   // keys per tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2_448 = 8.807354922057604f;     // log2(448): P is encoded as E4M3(448 p)
@@ -67,10 +63,10 @@ struct Cfg {
   static constexpr int kVTileBytes = D * kBN;
   static constexpr int kStageBytes = kKTileBytes + kVTileBytes;
   static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kColS = 0, kColO = 256;     // S_t buffer b at t * 128 + b * 64; O_t at 256 + t * D
+  static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 4 + 4 + 1;
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -115,72 +111,73 @@ __device__ __forceinline__ float block_max64(const uint32_t* s) {
   return fmaxf(fmax3(a, b, c), d);
 }
 
-// S[tmem d_col .. +64) = Q_tile(sq) . K_tile(sk)[keys 64 half .. +64)^T over D channels:
-// D/16 MMAs of 128 x 64 x 16.  Rows 64 half.. of a 128-row swizzled panel start 8 KB in.
+// S[tmem d_col] = Q_tile(sq) . K_tile(sk)^T over D channels: D/16 MMAs of 128x128x16.
 template <int D>
-__device__ __forceinline__ void issue_qk64(uint32_t d_tmem, uint32_t sq, uint32_t sk, int half) {
-  constexpr uint32_t idesc = idesc_f32acc(kBM, kBS);
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
+  constexpr uint32_t idesc = idesc_f32acc(kBM, kBN);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * Cfg<D>::kPanelBytes + (kk & 3) * 32;
-    mma_f16_ss(d_tmem, sdesc_k_sw128(sq + off), sdesc_k_sw128(sk + half * (kBS * 128) + off), idesc,
-               kk > 0 ? 1u : 0u);
+    mma_f16_ss(d_tmem, sdesc_k_sw128(sq + off), sdesc_k_sw128(sk + off), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O[tmem] (+)= P[tmem, 16 columns] . V_tile(sv)[keys 64 half .. +64): 2 MMAs of 128 x D x 32
-// (E4M3).  Keys 64 half.. start 64 bytes into each 128-byte swizzled row of V^T.
+// O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3).
 template <int D>
-__device__ __forceinline__ void issue_pv64(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, int half, bool first) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, D);
 #pragma unroll
-  for (int kk = 0; kk < kBS / 32; ++kk)
-    mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + half * kBS + kk * 32), idesc,
-              (first && kk == 0) ? 0u : 1u);
+  for (int kk = 0; kk < kBN / 32; ++kk)
+    mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
 }
 
-// One 64-key step of the online softmax for the calling thread's row (= TMEM lane), with one
-// K scale c for the whole step:
-//   reads S from its TMEM buffer; forms the step max as c * max_k S_k (c >= 0 and rounding is
-//   monotone, so this equals max_k fl(S_k c)); writes P = E4M3(448 p), p = exp2(S c - m_new),
-//   into the buffer's first 16 columns; l = alpha l + sum p; and, if any row of the warp saw
-//   its max rise, waits for the previous step's P.V (it accumulates into O) and multiplies
-//   that row's O by alpha = exp2(m_old - m_new) in one TMEM round trip.
-// kTail: keys >= kvalid do not exist (kvalid may be <= 0).  Returns false if a wait expired.
+// One 128-key tile of the online softmax for the calling thread's row (= TMEM lane):
+//   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
+//   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
+//   p = exp2(S c - m_new) into the first 32 columns of S; l = alpha l + sum p; and, if any row
+//   of the warp saw its max rise, multiplies that row's O by alpha = exp2(m_old - m_new).
+// kTail: keys >= kvalid are excluded from the max and get p = 0.
 template <int D, bool kTail>
-__device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, float c, int kvalid, int g, float& m,
-                                             float& l, uint64_t* pvb, uint64_t limit) {
-  uint32_t sr[kBS];
+__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0, float c1, int kvalid, bool first,
+                                             float& m, float& l) {
+  uint32_t sr[128];
   SAGE_TMEM_LD32(tS + 0, (sr + 0));
   SAGE_TMEM_LD32(tS + 32, (sr + 32));
+  SAGE_TMEM_LD32(tS + 64, (sr + 64));
+  SAGE_TMEM_LD32(tS + 96, (sr + 96));
   tmem_wait_ld();
-  float mx;
+  float mx0, mx1;
   if (!kTail) {
-    mx = block_max64(sr);
+    mx0 = block_max64(sr);
+    mx1 = block_max64(sr + 64);
   } else {
-    mx = -INFINITY;
+    mx0 = mx1 = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kBS; ++k)
-      if (k < kvalid) mx = fmaxf(mx, __uint_as_float(sr[k]));
+    for (int k = 0; k < 64; ++k)
+      if (k < kvalid) mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
+#pragma unroll
+    for (int k = 64; k < 128; ++k)
+      if (k < kvalid) mx1 = fmaxf(mx1, __uint_as_float(sr[k]));
   }
-  // fmaxf drops the NaN of (-inf) * 0 for a step with no keys.
-  const float m_new = fmaxf(m, mx * c);
-  const bool rise = (g > 0) && (m_new > m);
+  // fmaxf drops the NaN of (-inf) * 0 for an empty half.
+  const float m_new = fmaxf(m, fmaxf(mx0 * c0, mx1 * c1));
+  const bool rise = !first && (m_new > m);
   const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
   m = m_new;
   // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
   const uint64_t bias2 = f2_pack(kLog2_448 - m_new, kLog2_448 - m_new);
-  const uint64_t c2 = f2_pack(c, c);
   uint64_t l2 = f2_pack(0.0f, 0.0f);
 #pragma unroll
-  for (int cch = 0; cch < kBS / 32; ++cch) {
+  for (int cch = 0; cch < 4; ++cch) {
+    const float cb = cch < 2 ? c0 : c1;
+    const uint64_t cb2 = f2_pack(cb, cb);
     uint32_t pw[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const int k = cch * 32 + w * 4;
       float pp[4];
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, bias2), pp[0], pp[1]);
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), c2, bias2), pp[2], pp[3]);
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), cb2, bias2), pp[0], pp[1]);
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), cb2, bias2), pp[2], pp[3]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         pp[u] = ex2_approx(pp[u]);
@@ -195,14 +192,14 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, float c, 
   float llo, lhi;
   f2_unpack(l2, llo, lhi);
   l = l * alpha + (llo + lhi);
+  // O is rescaled after P is formed, when S no longer occupies registers.  P.V of this tile
+  // is issued only after p_full, so O still holds the previous tiles' sum here.
   if (__any_sync(0xffffffffu, rise)) {
-    // O holds the sum up to step g-1 once that step's P.V has completed.
-    if (!warp_wait(pvb + ((g - 1) & 1), ((g - 1) >> 1) & 1, limit)) return false;
-    tc_fence_after();
+    // The whole O row in one TMEM round trip: S no longer occupies registers here.
     const uint64_t a2 = f2_pack(alpha, alpha);
     uint32_t o[D];
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) SAGE_TMEM_LD32(tO + cc, (o + cc));
+    for (int c = 0; c < D; c += 32) SAGE_TMEM_LD32(tO + c, (o + c));
     tmem_wait_ld();
 #pragma unroll
     for (int k = 0; k < D; k += 2) {
@@ -212,10 +209,9 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, float c, 
       o[k + 1] = __float_as_uint(hi);
     }
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) SAGE_TMEM_ST32(tO + cc, (o + cc));
+    for (int c = 0; c < D; c += 32) SAGE_TMEM_ST32(tO + c, (o + c));
   }
   tmem_wait_st();
-  return true;
 }
 
 template <int D>
@@ -233,20 +229,16 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + C::kStages;
-  uint64_t* s_full = kv_empty + C::kStages;   // [t * 2 + b]: S_t buffer b holds Q_t K^T of a new step
-  // [t * 2 + b]: the softmax of tile t wrote P into buffer b.  One barrier per buffer: the
-  // softmax may finish steps g and g+1 before the MMA thread looks at step g, but step g+2
-  // needs S(g+2), which needs P(g).V -- so a barrier is never two phases ahead of its waiter.
-  uint64_t* p_full = s_full + 4;
-  uint64_t* pv_done = p_full + 4;             // [t * 2 + b]: P.V of tile t that read buffer b is done
-  uint64_t* mma_final = pv_done + 4;
+  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* mma_final = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hh = blockIdx.y;
   const int q0 = blockIdx.x * 2 * kBM;
-  const int ntiles = p.npad / kBN;      // 128-key K/V tiles
-  const int nsteps = 2 * ntiles;        // 64-key softmax steps
+  const int ntiles = p.npad / kBN;
 
   if (threadIdx.x == 0) {
     s_skip = *reinterpret_cast<volatile int32_t*>(p.status);
@@ -256,10 +248,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
-      mbar_init(pv_done + i, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(p_full + t, 128);
+      mbar_init(pv_done + t, 1);
     }
     mbar_init(mma_final, 1);
     fence_mbar_init();
@@ -304,55 +296,48 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      // Step g covers keys [64 g, 64 g + 64), half g % 2 of K/V tile g / 2; S_t(g) goes to S
-      // buffer g % 2 of tile t.  Per step: P_0(g).V, P_1(g).V, then S_0(g+2), S_1(g+2) into the
-      // buffers those P.V just released -- each S is ready two steps before its softmax.
       if (lane == 0) {
         const uint32_t sq = smem_u32(sQ);
         const uint32_t skv = smem_u32(sKV);
-        auto colS = [&](int t, int b) { return tmem + C::kColS + t * 2 * kBS + b * kBS; };
-        auto colO = [&](int t) { return tmem + C::kColO + t * D; };
+        const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
+        const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
         bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
         if (!ok) record_error(p.status, kWhereQFull, &s_abort);
         if (ok) {
           tc_fence_after();
-          for (int h = 0; h < 2; ++h)
-            for (int t = 0; t < 2; ++t) {
-              issue_qk64<D>(colS(t, h), sq + t * C::kQTileBytes, skv, h);
-              tc_commit(s_full + 2 * t + h);
-            }
+          issue_qk<D>(colS[0], sq, skv);
+          tc_commit(s_full + 0);
+          issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
+          tc_commit(s_full + 1);
         }
-        for (int g = 0; ok && g < nsteps; ++g) {
-          const int j = g >> 1, h = g & 1, s = j % C::kStages;
-          for (int t = 0; t < 2; ++t) {
-            if (!mbar_wait(p_full + 2 * t + h, (g >> 1) & 1, limit)) {
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int s = j % C::kStages;
+          const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(p_full + t, j & 1, limit)) {
               record_error(p.status, kWherePFull, &s_abort);
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_pv64<D>(colO(t), colS(t, h), skv + s * C::kStageBytes + C::kKTileBytes, h, g == 0);
-            tc_commit(pv_done + 2 * t + h);
-          }
-          if (!ok) break;
-          if (h == 1) tc_commit(kv_empty + s);   // both halves of K/V tile j consumed by both tiles
-          const int g2 = g + 2;
-          if (g2 < nsteps) {
-            const int j2 = g2 >> 1, s2 = j2 % C::kStages;
-            if (h == 0 && !mbar_wait(kv_full + s2, (j2 / C::kStages) & 1, limit)) {
-              record_error(p.status, kWhereKvFull, &s_abort);
-              break;
-            }
-            for (int t = 0; t < 2; ++t) {
-              // P_t(g) lives in buffer h: S_t(g+2) may overwrite it only after P_t(g).V is done.
-              if (!mbar_wait(pv_done + 2 * t + h, (g >> 1) & 1, limit)) {
+            issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            tc_commit(pv_done + t);
+            if (t == 1) tc_commit(kv_empty + s);
+            if (j + 1 < ntiles) {
+              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+                record_error(p.status, kWhereKvFull, &s_abort);
+                ok = false;
+                break;
+              }
+              // P_t lives in S_t's columns: the next S_t may be written only after P_t.V is done.
+              if (!mbar_wait(pv_done + t, j & 1, limit)) {
                 record_error(p.status, kWherePvDone, &s_abort);
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_qk64<D>(colS(t, h), sq + t * C::kQTileBytes, skv + s2 * C::kStageBytes, h);
-              tc_commit(s_full + 2 * t + h);
+              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              tc_commit(s_full + t);
             }
           }
           if (s_abort) ok = false;
@@ -370,40 +355,38 @@ __global__ void __launch_bounds__(384, 1)
     const int r = wq * 32 + lane;                // row within the tile = TMEM lane
     const int row = q0 + t * kBM + r;            // query row
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + C::kColS + t * 2 * kBS;   // + buffer * kBS
-    const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
+    const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
     const int nbq = p.npad / 128, nbk = p.npad / 64;
     const int qblk = (q0 + t * kBM) / 128;
     const float qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
     const float cq = qscale * p.sm_scale_log2;
-    const float* ks = p.k_scales + hh * nbk;     // one scale per 64-key step
-    uint64_t* pvb = pv_done + 2 * t;
+    const float* ks = p.k_scales + hh * nbk;
     float m = -INFINITY, l = 0.0f;
-    float ksn = ks[0];   // k scale of the next step, loaded one step ahead
+    float ksn0 = ks[0], ksn1 = ks[1];   // k scales of the next tile, loaded one tile ahead
     bool ok = true;
-    for (int g = 0; g < nsteps; ++g) {
-      const float ksg = ksn;
-      if (g + 1 < nsteps) ksn = ks[g + 1];
-      const int b = g & 1;
-      if (!warp_wait(s_full + 2 * t + b, (g >> 1) & 1, limit)) {
+    for (int j = 0; j < ntiles; ++j) {
+      const float ks0 = ksn0, ks1 = ksn1;
+      if (j + 1 < ntiles) {
+        ksn0 = ks[2 * j + 2];
+        ksn1 = ks[2 * j + 3];
+      }
+      if (!warp_wait(s_full + t, j & 1, limit)) {
         if (lane == 0) record_error(p.status, kWhereSFull, &s_abort);
         ok = false;
         break;
       }
       tc_fence_after();
-      const float c = cq * ksg;
-      const int kvalid = p.n - g * kBS;
-      const bool done = kvalid >= kBS ? softmax_step<D, false>(tS + b * kBS, tO, c, kBS, g, m, l, pvb, limit)
-                                      : softmax_step<D, true>(tS + b * kBS, tO, c, kvalid, g, m, l, pvb, limit);
-      if (!done) {
-        if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
-        ok = false;
-        break;
-      }
+      const float c0 = cq * ks0, c1 = cq * ks1;
+      const int kvalid = min(kBN, p.n - j * kBN);
+      if (kvalid == kBN)
+        softmax_step<D, false>(tS, tO, c0, c1, kBN, j == 0, m, l);
+      else
+        softmax_step<D, true>(tS, tO, c0, c1, kvalid, j == 0, m, l);
       tc_fence_before();
-      mbar_arrive(p_full + 2 * t + b);
+      mbar_arrive(p_full + t);
     }
-    if (ok && warp_wait(pvb + ((nsteps - 1) & 1), ((nsteps - 1) >> 1) & 1, limit)) {
+    if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const float* vs = p.v_scales + hh * D;
@@ -421,9 +404,9 @@ __global__ void __launch_bounds__(384, 1)
             for (int u = 0; u < 4; ++u) {
               const int k = v8 * 8 + u * 2;
               const float a = __uint_as_float(o[k]) * vs[c + k] * inv_l;
-              const float bb = __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
+              const float b = __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
               w[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(bb))) << 16);
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
             }
             *reinterpret_cast<uint4*>(orow + c + v8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
@@ -483,8 +466,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (mbar_wait(&bar_tma, 0, limit)) {
       tc_fence_after();
-      issue_qk64<D>(tmem, smem_u32(sQ), smem_u32(sK), 0);
-      issue_qk64<D>(tmem + kBS, smem_u32(sQ), smem_u32(sK), 1);
+      issue_qk<D>(tmem, smem_u32(sQ), smem_u32(sK));
     } else {
       record_error(status, kWhereDebugTma, &s_abort);
     }
