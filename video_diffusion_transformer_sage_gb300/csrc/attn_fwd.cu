@@ -166,7 +166,9 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
   m = m_new;
   // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
   const uint64_t bias2 = f2_pack(kLog2_448 - m_new, kLog2_448 - m_new);
-  uint64_t l2 = f2_pack(0.0f, 0.0f);
+  // Partial sums of p': one per (32-key chunk, key pair parity), so no add waits on more than
+  // eight earlier ones.
+  uint64_t l2[4][2];
 #pragma unroll
   for (int cch = 0; cch < 4; ++cch) {
     const float cb = cch < 2 ? c0 : c1;
@@ -183,14 +185,21 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
         pp[u] = ex2_approx(pp[u]);
         if (kTail && k + u >= kvalid) pp[u] = 0.0f;
       }
-      l2 = f2_add(l2, f2_pack(pp[0], pp[1]));
-      l2 = f2_add(l2, f2_pack(pp[2], pp[3]));
+      if (w == 0) {
+        l2[cch][0] = f2_pack(pp[0], pp[1]);
+        l2[cch][1] = f2_pack(pp[2], pp[3]);
+      } else {
+        l2[cch][0] = f2_add(l2[cch][0], f2_pack(pp[0], pp[1]));
+        l2[cch][1] = f2_add(l2[cch][1], f2_pack(pp[2], pp[3]));
+      }
       pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
     }
     SAGE_TMEM_ST8(tS + cch * 8, pw);
   }
+  const uint64_t la = f2_add(f2_add(l2[0][0], l2[0][1]), f2_add(l2[1][0], l2[1][1]));
+  const uint64_t lb = f2_add(f2_add(l2[2][0], l2[2][1]), f2_add(l2[3][0], l2[3][1]));
   float llo, lhi;
-  f2_unpack(l2, llo, lhi);
+  f2_unpack(f2_add(la, lb), llo, lhi);
   l = l * alpha + (llo + lhi);
   // O is rescaled after P is formed, when S no longer occupies registers.  P.V of this tile
   // is issued only after p_full, so O still holds the previous tiles' sum here.
@@ -340,7 +349,6 @@ __global__ void __launch_bounds__(384, 1)
               tc_commit(s_full + t);
             }
           }
-          if (s_abort) ok = false;
         }
         // Drain: every MMA issued above has finished before the CTA frees its tensor memory.
         tc_commit(mma_final);

@@ -42,12 +42,25 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity, uint32_
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete, sleeping in the barrier rather than
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete.  A phase that has already completed
+// is seen by one non-blocking test; otherwise the thread sleeps in the barrier rather than
 // spinning.  The global timer is read once per 256 polls; the wait gives up (returns false,
 // the caller records a timeout) once `limit_ns` nanoseconds have passed since the first read.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   constexpr uint32_t kHintNs = 1000000;   // 1 ms per poll at most
   const uint32_t a = smem_u32(bar);
+  if (mbar_done(a, parity)) return true;
   uint64_t t0 = 0;
   while (true) {
 #pragma unroll 1
