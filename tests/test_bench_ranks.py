@@ -39,3 +39,18 @@ def test_two_gloo_ranks_take_max_time():
 def test_single_rank_is_identity():
     assert bench.reduce_max(12.5, None) == 12.5
     assert bench.job_throughput(4e12, 10, 1, 100.0) == pytest.approx(400.0)
+
+
+def test_call_stats_percentiles():
+    """The per-call distribution: 50 calls in 5 rounds, percentiles by linear interpolation
+    (numpy's default rule), min/max/mean exact."""
+    import numpy as np
+    rounds = [[float(10 * r + i) for i in range(10)] for r in range(5)]   # 0..49
+    st = bench.call_stats(rounds)
+    xs = np.arange(50, dtype=np.float64)
+    assert st["count"] == 50 and st["min"] == 0.0 and st["max"] == 49.0
+    assert st["mean"] == pytest.approx(24.5)
+    for q in (50, 90, 95, 99):
+        assert st[f"p{q}"] == pytest.approx(float(np.percentile(xs, q)), abs=1e-4)
+    assert st["round_means"] == [4.5, 14.5, 24.5, 34.5, 44.5]
+    assert bench.call_stats([[3.0]])["p90"] == 3.0
