@@ -23,7 +23,10 @@ _lib = None
 _lock = threading.Lock()
 
 MUTATIONS = {"none": 0, "no_smooth": 1, "rescale_sign": 2, "scale_255": 3, "key_index": 4,
-             "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8}
+             "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8,
+             "q_block_index": 9}
+
+Q_BLOCKS = (1, 2, 4, 8, 16, 32, 64, 128)
 
 
 def build(force: bool = False) -> str:
@@ -52,10 +55,12 @@ def lib():
             L.oracle_set_mutation.argtypes = [ctypes.c_int]
             L.oracle_k_mean.argtypes = [P, I, I, I, I, I, P]
             L.oracle_quant_q.argtypes = [P, I, I, I, I, I, P, P]
+            L.oracle_quant_q_blk.argtypes = [P, I, I, I, I, I, I, P, P]
             L.oracle_quant_k.argtypes = [P, I, I, I, I, I, P, P, P]
             L.oracle_quant_v.argtypes = [P, I, I, I, I, I, P, P]
             L.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, I, I, I, P]
             L.oracle_attn_sq.argtypes = [P, P, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
+            L.oracle_attn_sq_blk.argtypes = [P, P, I, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
             L.oracle_attn_exact.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double,
                                             P, I, P]
             L.oracle_num_threads.restype = ctypes.c_int
@@ -109,13 +114,15 @@ def k_mean(k: torch.Tensor) -> np.ndarray:
     return mu
 
 
-def quant_q(q: torch.Tensor):
+def quant_q(q: torch.Tensor, q_block: int = 128):
+    """INT8 Q codes [H, N_pad, D] and scales [H, N_pad / q_block] (q_block a power of two <= 128)."""
+    assert q_block in Q_BLOCKS
     n, h, d = q.shape
     np_ = pad128(n)
     codes = np.zeros((h, np_, d), np.int8)
-    scales = np.zeros((h, np_ // 128), np.float32)
+    scales = np.zeros((h, np_ // q_block), np.float32)
     p, st, sh = _view_args(q)
-    lib().oracle_quant_q(p, n, h, d, st, sh, _ptr(codes), _ptr(scales))
+    lib().oracle_quant_q_blk(p, n, h, d, st, sh, q_block, _ptr(codes), _ptr(scales))
     return codes, scales
 
 
@@ -143,10 +150,11 @@ def quant_v(v: torch.Tensor):
 class Quantized:
     """Steps 1-4 of the oracle for one set of inputs."""
 
-    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_block: int = 128):
         self.n, self.h, self.d = q.shape
+        self.q_block = q_block
         self.k_mean = k_mean(k)
-        self.q_codes, self.q_scales = quant_q(q)
+        self.q_codes, self.q_scales = quant_q(q, q_block)
         self.k_codes, self.k_scales = quant_k(k, self.k_mean)
         self.v_codes, self.v_scales = quant_v(v)
 
@@ -168,9 +176,10 @@ def attn_sq(qz: Quantized, sm_scale: float, rows, tile: int = 128, score_f32=Non
         score_f32 = tile > 0
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     out = np.zeros((len(rows), qz.h, qz.d), np.float64)
-    lib().oracle_attn_sq(_ptr(qz.q_codes), _ptr(qz.q_scales), _ptr(qz.k_codes), _ptr(qz.k_scales),
-                         _ptr(qz.v_codes), _ptr(qz.v_scales), qz.n, qz.h, qz.d, float(sm_scale),
-                         _ptr(rows), len(rows), int(tile), int(bool(score_f32)), _ptr(out))
+    lib().oracle_attn_sq_blk(_ptr(qz.q_codes), _ptr(qz.q_scales), int(getattr(qz, "q_block", 128)),
+                             _ptr(qz.k_codes), _ptr(qz.k_scales), _ptr(qz.v_codes), _ptr(qz.v_scales),
+                             qz.n, qz.h, qz.d, float(sm_scale), _ptr(rows), len(rows), int(tile),
+                             int(bool(score_f32)), _ptr(out))
     return out
 
 

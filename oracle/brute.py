@@ -73,11 +73,12 @@ def quant_v(v: np.ndarray):
     return out, scale
 
 
-def attn_sq_global(qc, qs, kc, ks, vc, vs, n, sm_scale):
-    """Global-max same-quantisation attention, all rows: [N, H, D] fp64."""
+def attn_sq_global(qc, qs, kc, ks, vc, vs, n, sm_scale, q_block=128):
+    """Global-max same-quantisation attention, all rows: [N, H, D] fp64.  qs holds one scale
+    per (head, q_block consecutive rows)."""
     h, np_, d = qc.shape
     out = np.zeros((n, h, d))
-    qrow_scale = np.repeat(qs, 128, axis=1)[:, :n]
+    qrow_scale = np.repeat(qs, q_block, axis=1)[:, :n]
     krow_scale = np.repeat(ks, 64, axis=1)[:, :n]
     for hh in range(h):
         S = qc[hh, :n].astype(np.int64) @ kc[hh, :n].astype(np.int64).T

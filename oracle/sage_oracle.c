@@ -11,10 +11,12 @@
  *
  *   1. K mean       mu[h,c] = mean over tokens of K[t,h,c]                 oracle_k_mean
  *   2. Q quantise   per (head, 128-row block) symmetric INT8, fp32 scale   oracle_quant_q
+ *                   (or per (head, qb-row block), qb | 128: the per-warp variant with the
+ *                   recorded warp_q of 32 rows, down to per row)           oracle_quant_q_blk
  *   3. K quantise   K~ = K - mu, per (head, 64-row block) INT8             oracle_quant_k
  *   4. V quantise   per (head, channel) FP8 E4M3, fp32 scale               oracle_quant_v
  *   5. S = Qc Kc^T  exact integer dot products                             oracle_qk_int32
- *   6-8. softmax(S * s_q * s_k * sm_scale) with P held in E4M3, times V    oracle_attn_sq
+ *   6-8. softmax(S * s_q * s_k * sm_scale) with P held in E4M3, times V    oracle_attn_sq(_blk)
  *   9. exact fp64 softmax attention of the bf16 inputs                     oracle_attn_exact
  *
  * The shapes are those of the attention call profiled in
@@ -38,7 +40,7 @@
  * the tests can show that the pins catch it.  Always 0 outside those tests. */
 enum { MUT_NONE = 0, MUT_NO_SMOOTH = 1, MUT_RESCALE_SIGN = 2, MUT_SCALE_255 = 3,
        MUT_KEY_INDEX = 4, MUT_V_SCALE_CHANNEL = 5, MUT_DROP_LAST_KEY = 6,
-       MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8 };
+       MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8, MUT_Q_BLOCK_INDEX = 9 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
 
@@ -142,21 +144,29 @@ static float quant_block_i8(const float* x, int64_t rows, int64_t d, int8_t* cod
   return scale;
 }
 
-/* 2. Q: one scale per (head, 128-row block). codes [H][N_pad][D], scales [H][N_pad/128]. */
-void oracle_quant_q(const uint16_t* q, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
-                    int8_t* codes, float* scales) {
-  int64_t np = pad128(n), nb = np / 128;
+/* 2. Q: one scale per (head, qb-row block), qb a power of two dividing 128 (the method's
+ * default is qb = 128; qb = 32 is the per-warp granularity of the recorded kernel's warp_q).
+ * codes [H][N_pad][D], scales [H][N_pad/qb].  A block that lies wholly in the padding has
+ * scale 0. */
+void oracle_quant_q_blk(const uint16_t* q, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                        int64_t qb, int8_t* codes, float* scales) {
+  int64_t np = pad128(n), nb = np / qb;
   memset(codes, 0, (size_t)(h * np * d));
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t hh = 0; hh < h; ++hh)
     for (int64_t b = 0; b < nb; ++b) {
-      float* buf = (float*)malloc(sizeof(float) * 128 * d);
-      int64_t r0 = b * 128, r1 = r0 + 128 < n ? r0 + 128 : n;
+      float* buf = (float*)malloc(sizeof(float) * (size_t)(qb * d));
+      int64_t r0 = b * qb, r1 = r0 + qb < n ? r0 + qb : n;
       for (int64_t t = r0; t < r1; ++t)
         for (int64_t c = 0; c < d; ++c) buf[(t - r0) * d + c] = bf16_to_f32(q[t * st + hh * sh + c]);
       scales[hh * nb + b] = quant_block_i8(buf, r1 - r0, d, codes + (hh * np + r0) * d);
       free(buf);
     }
+}
+
+void oracle_quant_q(const uint16_t* q, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                    int8_t* codes, float* scales) {
+  oracle_quant_q_blk(q, n, h, d, st, sh, 128, codes, scales);
 }
 
 /* 3. K smoothing then quantisation: K~ = fl32(K - mu) (one fp32 subtraction), one scale per
@@ -225,7 +235,8 @@ void oracle_qk_int32(const int8_t* qc, const int8_t* kc, int64_t n, int64_t h, i
 
 /* ------------------------------------------------------------------------------------
  * 6-8. Same-quantisation attention for selected query rows (all heads).
- *   s_ij = S_ij * s_q[h, i/128] * s_k[h, j/64] * sm_scale
+ *   s_ij = S_ij * s_q[h, i/qb] * s_k[h, j/64] * sm_scale     (qb = 128 unless the Q scales
+ *   are per smaller block, see oracle_quant_q_blk)
  *   p_ij = exp(s_ij - m_i);  P8_ij = E4M3(448 p_ij)  (static scale 448: p <= 1 never overflows)
  *   l_i  = sum_j 448 p_ij                (unquantised p)
  *   O_ic = (sum_j P8_ij * E4M3val(vc[h,c,j])) * s_v[h,c] / l_i
@@ -241,11 +252,11 @@ void oracle_qk_int32(const int8_t* qc, const int8_t* kc, int64_t n, int64_t h, i
  *   fl32(c_b * max S over each 64-key half), and 448 p = RN_f32(2^x); sums stay in fp64.
  * out[r][h][c] (fp64).
  * ---------------------------------------------------------------------------------- */
-void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const float* ks,
-                    const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
-                    double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
-                    int64_t score_f32, double* out) {
-  int64_t np = pad128(n), nbq = np / 128, nbk = np / 64;
+void oracle_attn_sq_blk(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
+                        const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
+                        double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
+                        int64_t score_f32, double* out) {
+  int64_t np = pad128(n), nbq = np / qb, nbk = np / 64;
   int64_t nkeys = (g_mutation == MUT_DROP_LAST_KEY) ? n - 1 : n;
   const float kLog2E = 1.4426950408889634f, kLog2_448 = 8.807354922057604f;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -255,7 +266,9 @@ void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const f
     double* s = (double*)malloc(sizeof(double) * (size_t)n);
     int64_t* S = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
     const int8_t* a = qc + (hh * np + i) * d;
-    double sq = (double)qs[hh * nbq + i / 128];
+    /* the Q block of row i (the planted mistake reads the 128-row block's index instead) */
+    const int64_t qbi = (g_mutation == MUT_Q_BLOCK_INDEX) ? i / 128 : i / qb;
+    double sq = (double)qs[hh * nbq + qbi];
     for (int64_t j = 0; j < nkeys; ++j) {
       int64_t jj = (g_mutation == MUT_KEY_INDEX) ? (j ^ 1) % n : j;
       const int8_t* b = kc + (hh * np + jj) * d;
@@ -269,7 +282,7 @@ void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const f
     int64_t tw = tile > 0 ? tile : nkeys;
     if (tile <= 0)
       for (int64_t j = 0; j < nkeys; ++j) if (s[j] > m) m = s[j];
-    const float cq = qs[hh * nbq + i / 128] * ((float)sm_scale * kLog2E);
+    const float cq = qs[hh * nbq + qbi] * ((float)sm_scale * kLog2E);
     for (int64_t j0 = 0; j0 < nkeys; j0 += tw) {
       int64_t j1 = j0 + tw < nkeys ? j0 + tw : nkeys;
       if (tile > 0 && score_f32) {
@@ -331,6 +344,14 @@ void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const f
     free(s);
     free(S);
   }
+}
+
+/* The method's default: Q scales per 128-row block. */
+void oracle_attn_sq(const int8_t* qc, const float* qs, const int8_t* kc, const float* ks,
+                    const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
+                    double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
+                    int64_t score_f32, double* out) {
+  oracle_attn_sq_blk(qc, qs, 128, kc, ks, vc, vs, n, h, d, sm_scale, rows, nrows, tile, score_f32, out);
 }
 
 /* 9. Exact attention of the bf16 inputs in fp64: O = softmax(sm_scale * q k^T) v, no

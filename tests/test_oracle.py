@@ -328,6 +328,64 @@ def test_page_shapes_golden():
     assert abs(synth.WORKLOADS["video"].flops - 40.989e12) / 40.989e12 < 1e-4
 
 
+# ---------------------------------------------------------------- Q-scale granularity
+# Q scales per q_block consecutive rows (q_block | 128): the method's 128 by default, 32 the
+# per-warp granularity of the recorded kernel's warp_q, 1 per row.
+
+@pytest.mark.parametrize("q_block", [1, 2, 8, 32, 64, 128])
+def test_q_block_quant_matches_brute(oracle_lib, q_block):
+    inp = small_inputs(n=300, h=2, d=64, layout="qkv")
+    codes, scales = oracle.quant_q(inp.q, q_block)
+    qf = np.ascontiguousarray(inp.q.float().numpy().transpose(1, 0, 2))
+    bq, bqs = brute.quant_int8_blocks(qf, q_block)
+    assert scales.shape == (2, 384 // q_block)
+    assert (bq == codes).all() and (bqs == scales).all()
+    assert (scales[:, 300 // q_block + (300 % q_block > 0):] == 0).all()   # blocks wholly in the padding
+
+
+def test_q_block_128_is_the_default(oracle_lib):
+    inp = small_inputs(n=300, h=2, d=64, layout="qkv")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    c, s = oracle.quant_q(inp.q, 128)
+    assert qz.q_block == 128 and (qz.q_codes == c).all() and (qz.q_scales == s).all()
+
+
+def test_q_block_scales_nest(oracle_lib):
+    """The max over a 128-row block is the max of its sub-blocks' maxima, and x -> fl32(x/127)
+    is monotone, so the 128-row scale equals the largest scale of the finer blocks inside it."""
+    inp = synth.make_inputs("tails")
+    _, s128 = oracle.quant_q(inp.q, 128)
+    for qb in (1, 4, 32, 64):
+        _, s = oracle.quant_q(inp.q, qb)
+        assert (s.reshape(s.shape[0], -1, 128 // qb).max(axis=2) == s128).all(), qb
+
+
+def test_q_block_per_row_error_bound(oracle_lib):
+    """Per-row scales: each row's largest |code| is 127 (unless the row is zero) and every
+    element dequantises to within half its row's scale."""
+    inp = synth.make_inputs("tails")
+    codes, s = oracle.quant_q(inp.q, 1)
+    n = inp.q.shape[0]
+    x = inp.q.float().numpy().transpose(1, 0, 2).astype(np.float64)
+    sc = s[:, :n, None].astype(np.float64)
+    assert (np.abs(codes[:, :n].astype(np.float64) * sc - x) <= sc * 0.5 * (1 + 2e-5) + 1e-30).all()
+    rowmax = np.abs(codes[:, :n].astype(np.int32)).max(axis=2)
+    assert ((rowmax == 127) | (s[:, :n] == 0)).all()
+
+
+@pytest.mark.parametrize("q_block", [1, 32])
+def test_q_block_attention_matches_brute(oracle_lib, q_block):
+    inp = small_inputs(n=300, h=2, d=64, layout="qkv")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v, q_block=q_block)
+    rows = list(range(300))
+    a = oracle.attn_sq(qz, 0.125, rows, tile=0)
+    b = brute.attn_sq_global(qz.q_codes, qz.q_scales, qz.k_codes, qz.k_scales, qz.v_codes,
+                             qz.v_scales, 300, 0.125, q_block=q_block)
+    assert np.abs(a - b).max() < 1e-12
+    t = oracle.attn_sq(qz, 0.125, rows[:128], tile=512, score_f32=False)   # one tile = global
+    assert (t == a[:128]).all()
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _pins_pass(inp) -> bool:
@@ -354,6 +412,14 @@ def _pins_pass(inp) -> bool:
         return False
     t32 = oracle.attn_sq(qz, 0.125, rows, tile=128, score_f32=True)
     if not rel_l2(t32, g) < 0.1:
+        return False
+    q32 = oracle.Quantized(inp.q, inp.k, inp.v, q_block=32)
+    bq32, bqs32 = brute.quant_int8_blocks(np.ascontiguousarray(inp.q.float().numpy().transpose(1, 0, 2)), 32)
+    if not ((bq32 == q32.q_codes).all() and (bqs32 == q32.q_scales).all()):
+        return False
+    g32 = brute.attn_sq_global(q32.q_codes, q32.q_scales, q32.k_codes, q32.k_scales, q32.v_codes,
+                               q32.v_scales, n, 0.125, q_block=32)
+    if not np.abs(oracle.attn_sq(q32, 0.125, rows, tile=0) - g32).max() < 1e-12:
         return False
     e = oracle.attn_exact(inp.q, inp.k, inp.v, 0.125, rows)
     b = brute.attn_exact(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), 0.125)
