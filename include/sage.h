@@ -71,12 +71,20 @@ typedef struct sage_view {
  *            sm_103a has no 8-bit integer MMA kind; every integer |c| <= 2048 is exact
  *            in fp16, and the fp16 MMA with fp32 accumulation reproduces the integer dot
  *            products exactly (|QK^T| <= 128 * 127^2 < 2^21).
- *   q_scales [H][N_pad/128] fp32
+ *   q_scales [H][N_pad/q_block] fp32: one scale per q_block consecutive rows
  *   k_codes  [H][N_pad][D]  as q_codes, codes of K - k_mean
  *   k_scales [H][N_pad/64]  fp32
  *   k_mean   [H][D]         fp32
  *   v_codes  [H][D][N_pad]  FP8 E4M3 bytes, keys contiguous (the K-major B operand of P.V)
  *   v_scales [H][D]         fp32
+ *   q_block  rows per Q scale: 0 or 128 (the method's default, one scale per 128-row block
+ *            as in the pages' call), or 64, 32, 16, 8, 4, 2, 1.  32 is the per-warp
+ *            granularity of the pages' recorded kernel configuration ("warp_q": 32 in the
+ *            scheduler of "gb10-sage2-p0-interleave-softmax-latency.json"); 1 is one scale
+ *            per row.  Finer blocks cost nothing in the attention kernel (each softmax
+ *            thread owns one row) and lower the quantisation error of Q on inputs with
+ *            outlier rows.  Any other value: SAGE_ERR_INVALID_ARG.  sage_attn_fwd always
+ *            uses 128.
  * All of these pointers must be 16-byte aligned. */
 typedef struct sage_quantized {
   uint16_t* q_codes;
@@ -86,6 +94,7 @@ typedef struct sage_quantized {
   float* k_mean;
   uint8_t* v_codes;
   float* v_scales;
+  int64_t q_block;
 } sage_quantized;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -108,8 +117,9 @@ size_t sage_status_block_bytes(void);
  *   k_mean[h][c] = fp32(total / N) in fp64: each 128-token chunk summed in fp32 in
  *                  ascending token order; the chunk sums summed in fp64 in 8 groups of
  *                  ceil(chunks / 8) consecutive chunks, the groups added in ascending order;
- *   Q: per (h, 128-row block) scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)),
- *      -127, 127) with IEEE division; an all-zero block has scale 0 and codes 0;
+ *   Q: per (h, q_block-row block; 128 when qz->q_block is 0) scale = fl32(amax / 127),
+ *      code = clamp(rint(fl32(x / scale)), -127, 127) with IEEE division; an all-zero
+ *      block (also one wholly in the padding) has scale 0 and codes 0;
  *   K: the same on fl32(k - k_mean[h][c]) per (h, 64-row block).
  * Writes qz->q_codes, q_scales, k_codes, k_scales, k_mean.  ws: >= sage_quant_scratch_bytes,
  * 16-byte aligned, contents ignored and overwritten. */

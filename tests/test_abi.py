@@ -88,6 +88,12 @@ def test_argument_validation_never_launches(L):
     # debug tiles outside N_pad
     assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 0, 128, 0, 2, 1, 4096, 4096, None) == 1
     assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 2, 0, 0, 1, 1, 4096, 4096, None) == 1
+    # rows per Q scale: a power of two <= 128, or 0 for the default 128
+    for bad in (3, 96, 256, -1):
+        qb = _qz()
+        qb.q_block = bad
+        assert call(by(q), by(k), by(qb), 4096, 1 << 30, None) == 1, bad
+        assert L.sage_attn_fwd_quantized(256, 2, 128, by(qb), 0.1, 4096, 256, 128, 4096, None) == 1, bad
     assert L.sage_check_device_status(0, None, None) == 1
     assert L.sage_debug_wait_timeout(0, 1000, None) == 1
     assert L.sage_debug_wait_timeout(4096, 0, None) == 1

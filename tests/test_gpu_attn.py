@@ -87,6 +87,26 @@ def test_attention_matches_oracle(name):
     assert rel_l2(got, ex) <= max(EXACT_REL, method_gap + SQ_REL), (rel_l2(got, ex), method_gap)
 
 
+@pytest.mark.parametrize("name,q_block,rows", [("tails", 32, None), ("tails", 1, None), ("strided64", 32, 192)])
+def test_q_block_attention_matches_oracle(name, q_block, rows):
+    """Q scales per q_block rows: each softmax thread reads its own row's scale."""
+    case = gpu_case(name)
+    n, h, d = case["q"].shape
+    sm = 1.0 / math.sqrt(d)
+    qz = sage.sage_smooth_quant_qk(case["q"], case["k"], q_block=q_block)
+    sage.sage_quant_v(case["v"], qz)
+    status = sage.status_block()
+    out = sage.sage_attn_fwd_quantized(qz, sm, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    oz = oracle.Quantized(case["inp"].q, case["inp"].k, case["inp"].v, q_block=q_block)
+    sel = list(range(n)) if rows is None else synth.sample_rows(n, rows, 13)
+    got = out[sel].float().cpu().numpy().astype(np.float64)
+    ref = oracle.attn_sq(oz, sm, sel, tile=128)
+    r = rel_l2(got, ref)
+    mx = float(np.abs(got - ref).max())
+    assert r <= SQ_REL and mx <= SQ_ABS, (r, mx)
+
+
 def test_quantized_entry_point_and_strided_output():
     """sage_attn_fwd_quantized on the quantise calls' buffers equals sage_attn_fwd, also when
     writing into a token-major [N, H*D] view (the layout the output projection reads)."""

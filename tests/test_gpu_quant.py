@@ -60,3 +60,46 @@ def test_quant_repeatable_and_scratch_reuse():
     torch.cuda.synchronize()
     for name in ("q_codes", "k_codes", "v_codes", "q_scales", "k_scales", "k_mean", "v_scales"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+@pytest.mark.parametrize("name,q_block", [("tails", 32), ("tails", 1), ("tails", 64), ("strided64", 32),
+                                          ("strided64", 2), ("tiny", 16)])
+def test_q_block_bit_exact(name, q_block):
+    """Q scales per q_block rows (the per-warp granularity of the recorded kernel's warp_q, and
+    finer): codes and scales bit-identical to the oracle's; K and V untouched."""
+    case = gpu_case(name)
+    import oracle
+    codes, scales = oracle.quant_q(case["inp"].q, q_block)
+    qz = sage.sage_smooth_quant_qk(case["q"], case["k"], q_block=q_block)
+    torch.cuda.synchronize()
+    assert qz.q_scales.shape == scales.shape
+    assert np.array_equal(qz.q_scales.cpu().numpy().view(np.uint32), scales.view(np.uint32))
+    assert np.array_equal(qz.q_codes.cpu().float().numpy(), codes.astype(np.float32))
+    oq = case["qz"]
+    assert np.array_equal(qz.k_codes.cpu().float().numpy(), oq.k_codes.astype(np.float32))
+    assert np.array_equal(qz.k_scales.cpu().numpy().view(np.uint32), oq.k_scales.view(np.uint32))
+
+
+def test_tiny_values_take_ieee_division():
+    """A row, block or channel of values so small that its scale is subnormal (no finite
+    reciprocal) still quantises exactly like the oracle's IEEE division."""
+    import oracle
+    from video_diffusion_transformer_sage_gb300 import synth
+    inp = synth.make_inputs(synth.custom(256, 2, 128, "qkv", seed=9, n_outlier=1))
+    st = inp.storage.clone()
+    hd = 2 * 128
+    st[:130, :] = (st[:130, :].float() * 2.0 ** -124).to(torch.bfloat16)   # Q, K, V rows 0..129 tiny
+    st[:, 2 * hd + 5] = (st[:, 2 * hd + 5].float() * 2.0 ** -124).to(torch.bfloat16)  # one V channel tiny
+    q, k, v = (st[:, i * hd:(i + 1) * hd].view(256, 2, 128) for i in range(3))
+    oz = oracle.Quantized(q, k, v, q_block=1)
+    assert (oz.q_scales[:, :130] < 2.0 ** -126).sum() > 100 and (oz.q_scales[:, :130] > 0).all()
+    assert 0 < oz.v_scales[0, 5] < 2.0 ** -126
+    dst = st.cuda()
+    dq, dk, dv = (dst[:, i * hd:(i + 1) * hd].view(256, 2, 128) for i in range(3))
+    gz = sage.sage_smooth_quant_qk(dq, dk, q_block=1)
+    sage.sage_quant_v(dv, gz)
+    torch.cuda.synchronize()
+    assert np.array_equal(gz.q_scales.cpu().numpy().view(np.uint32), oz.q_scales.view(np.uint32))
+    assert np.array_equal(gz.q_codes.cpu().float().numpy(), oz.q_codes.astype(np.float32))
+    assert np.array_equal(gz.v_scales.cpu().numpy().view(np.uint32), oz.v_scales.view(np.uint32))
+    assert np.array_equal(gz.v_codes.cpu().numpy(), oz.v_codes)

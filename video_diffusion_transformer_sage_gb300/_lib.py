@@ -38,7 +38,7 @@ class SageView(ctypes.Structure):
 class SageQuantizedC(ctypes.Structure):
     _fields_ = [("q_codes", ctypes.c_void_p), ("q_scales", ctypes.c_void_p), ("k_codes", ctypes.c_void_p),
                 ("k_scales", ctypes.c_void_p), ("k_mean", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("v_scales", ctypes.c_void_p)]
+                ("v_scales", ctypes.c_void_p), ("q_block", ctypes.c_int64)]
 
 
 _lib = None
@@ -108,13 +108,16 @@ def pad128(n: int) -> int:
 class Quantized:
     """Device buffers of the quantised operands (layouts of sage_quantized in include/sage.h)."""
 
-    def __init__(self, n: int, h: int, d: int, device="cuda"):
+    def __init__(self, n: int, h: int, d: int, device="cuda", q_block: int = 128):
+        """q_block: rows per Q scale (128, the method's default, or a smaller power of two)."""
         np_ = pad128(n)
-        self.n, self.h, self.d = n, h, d
+        if q_block not in (1, 2, 4, 8, 16, 32, 64, 128):
+            raise ValueError(f"q_block must be a power of two <= 128, got {q_block}")
+        self.n, self.h, self.d, self.q_block = n, h, d, q_block
         self.q_codes = torch.empty((h, np_, d), dtype=torch.float16, device=device)
         self.k_codes = torch.empty((h, np_, d), dtype=torch.float16, device=device)
         self.v_codes = torch.empty((h, d, np_), dtype=torch.uint8, device=device)
-        self.q_scales = torch.empty((h, np_ // 128), dtype=torch.float32, device=device)
+        self.q_scales = torch.empty((h, np_ // q_block), dtype=torch.float32, device=device)
         self.k_scales = torch.empty((h, np_ // 64), dtype=torch.float32, device=device)
         self.k_mean = torch.empty((h, d), dtype=torch.float32, device=device)
         self.v_scales = torch.empty((h, d), dtype=torch.float32, device=device)
@@ -122,7 +125,7 @@ class Quantized:
     def c(self) -> SageQuantizedC:
         return SageQuantizedC(self.q_codes.data_ptr(), self.q_scales.data_ptr(), self.k_codes.data_ptr(),
                               self.k_scales.data_ptr(), self.k_mean.data_ptr(), self.v_codes.data_ptr(),
-                              self.v_scales.data_ptr())
+                              self.v_scales.data_ptr(), self.q_block)
 
 
 def quant_scratch(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
@@ -143,9 +146,9 @@ def workspace(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
 
 
 def sage_smooth_quant_qk(q: torch.Tensor, k: torch.Tensor, qz: Optional[Quantized] = None,
-                         scratch: Optional[torch.Tensor] = None, stream=None) -> Quantized:
+                         scratch: Optional[torch.Tensor] = None, stream=None, q_block: int = 128) -> Quantized:
     n, h, d = q.shape
-    qz = qz or Quantized(n, h, d, q.device)
+    qz = qz or Quantized(n, h, d, q.device, q_block)
     scratch = scratch if scratch is not None else quant_scratch(n, h, d, q.device)
     vq, vk, c = make_view(q), make_view(k), qz.c()
     _check(lib().sage_smooth_quant_qk(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(c), scratch.data_ptr(),

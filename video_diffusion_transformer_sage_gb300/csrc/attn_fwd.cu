@@ -72,7 +72,8 @@ struct Cfg {
 
 struct AttnParams {
   int n, npad, h;
-  const float* q_scales;   // [H][npad/128]
+  const float* q_scales;   // [H][npad >> q_shift]: one scale per 2^q_shift rows
+  int q_shift;
   const float* k_scales;   // [H][npad/64]
   const float* v_scales;   // [H][D]
   float sm_scale_log2;     // sm_scale * log2(e)
@@ -365,9 +366,9 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
-    const int nbq = p.npad / 128, nbk = p.npad / 64;
-    const int qblk = (q0 + t * kBM) / 128;
-    const float qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
+    const int nbk = p.npad / 64;
+    // The scale of this thread's own row (its block of 2^q_shift rows); none past the padding.
+    const float qscale = row < p.npad ? p.q_scales[hh * (p.npad >> p.q_shift) + (row >> p.q_shift)] : 0.0f;
     const float cq = qscale * p.sm_scale_log2;
     const float* ks = p.k_scales + hh * nbk;
     float m = -INFINITY, l = 0.0f;
@@ -550,8 +551,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
 }
 
 template <int D>
-cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, float sm_scale, void* out, int64_t ost,
-                              int64_t osh, int32_t* status, cudaStream_t s) {
+cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_block, float sm_scale, void* out,
+                              int64_t ost, int64_t osh, int32_t* status, cudaStream_t s) {
   using C = Cfg<D>;
   const int npad = static_cast<int>(pad128(n));
   CUtensorMap qmap, kmap, vmap;
@@ -571,6 +572,8 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, float sm_s
   p.npad = npad;
   p.h = h;
   p.q_scales = qz.q_scales;
+  p.q_shift = 0;
+  while ((1 << p.q_shift) < q_block) ++p.q_shift;
   p.k_scales = qz.k_scales;
   p.v_scales = qz.v_scales;
   p.sm_scale_log2 = sm_scale * kLog2e;
@@ -603,10 +606,10 @@ cudaError_t launch_debug_qk_t(int n, int h, const sage_quantized& qz, int head, 
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, float sm_scale, void* out, int64_t ost,
-                            int64_t osh, int32_t* status, cudaStream_t s) {
-  return d == 128 ? launch_attn_fwd_t<128>(n, h, qz, sm_scale, out, ost, osh, status, s)
-                  : launch_attn_fwd_t<64>(n, h, qz, sm_scale, out, ost, osh, status, s);
+cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, int q_block, float sm_scale, void* out,
+                            int64_t ost, int64_t osh, int32_t* status, cudaStream_t s) {
+  return d == 128 ? launch_attn_fwd_t<128>(n, h, qz, q_block, sm_scale, out, ost, osh, status, s)
+                  : launch_attn_fwd_t<64>(n, h, qz, q_block, sm_scale, out, ost, osh, status, s);
 }
 
 cudaError_t launch_debug_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t s) {

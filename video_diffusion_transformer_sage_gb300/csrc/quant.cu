@@ -153,11 +153,17 @@ __device__ __forceinline__ uint64_t div_rn2(uint64_t x2, uint64_t neg_s2, uint64
 }
 
 // Two INT8 codes (held as fp16) of x0, x1 for block scale s (r = RN(1/s)):
-// clamp(rint(RN(x / s)), -127, 127), or 0 when s == 0.
+// clamp(rint(RN(x / s)), -127, 127), or 0 when s == 0.  The reciprocal route needs a finite
+// r, i.e. a normal s; a subnormal scale (a block of values below 2^-119) divides directly.
 __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, uint64_t neg_s2, uint64_t r2) {
   if (s == 0.0f) return 0u;
   float q0, q1;
-  f2_unpack(div_rn2(f2_pack(x0, x1), neg_s2, r2), q0, q1);
+  if (s >= 1.17549435e-38f) {
+    f2_unpack(div_rn2(f2_pack(x0, x1), neg_s2, r2), q0, q1);
+  } else {
+    q0 = __fdiv_rn(x0, s);
+    q1 = __fdiv_rn(x1, s);
+  }
   q0 = fminf(fmaxf(rintf(q0), -127.0f), 127.0f);
   q1 = fminf(fmaxf(rintf(q1), -127.0f), 127.0f);
   uint32_t h;
@@ -167,12 +173,13 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
 
 // One CTA per (head h, 128-row block b, operand): z = 0 quantises the Q block with one
 // scale; z = 1 quantises the same rows of K - mean as two 64-row blocks, one scale each.
+// only_k: every CTA does K (Q is quantised per smaller block by quant_q_grouped_kernel).
 // Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
 // all its loads before any arithmetic; the maxima share one block reduction.
 template <int D>
 __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
                                                        const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
-                                                       const float* __restrict__ k_mean, int n, int npad,
+                                                       const float* __restrict__ k_mean, int n, int npad, int only_k,
                                                        uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
                                                        uint16_t* __restrict__ k_codes,
                                                        float* __restrict__ k_scales) {
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
   constexpr int NP = 128 / RPP;         // passes per 128-row block
   __shared__ float red[2][8];
   const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
-  const bool is_k = blockIdx.z != 0;
+  const bool is_k = only_k || blockIdx.z != 0;
   const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
   const int row0 = b * 128;
   const uint16_t* src = is_k ? k : q;
@@ -271,6 +278,78 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
   }
 }
 
+// One CTA per (head h, 128-row block b) of Q when one scale covers q_block < 128 rows
+// (q_block a power of two).  The |q| maximum of each row is taken over the VPR threads that
+// hold it (on bf16 bit patterns, as above), then over each group of q_block rows: shuffles
+// within a warp (thread t < 128 holds row t), shared memory across warps for 64-row groups.
+// Pad rows count as 0, so a group wholly in the padding gets scale 0 and codes 0.
+template <int D>
+__global__ void __launch_bounds__(256) quant_q_grouped_kernel(const uint16_t* __restrict__ q, int64_t qst,
+                                                              int64_t qsh, int n, int npad, int q_block,
+                                                              uint16_t* __restrict__ q_codes,
+                                                              float* __restrict__ q_scales) {
+  constexpr int VPR = D / 8;            // vectors per row
+  constexpr int RPP = 256 / VPR;        // rows per pass
+  constexpr int NP = 128 / RPP;         // passes per 128-row block
+  __shared__ float rmax[128];
+  __shared__ float wmax[4];
+  const int hh = blockIdx.x, b = blockIdx.y;
+  const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
+  const int row0 = b * 128;
+
+  uint4 v[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int row = row0 + p * RPP + rin;
+    v[p] = row < n ? ld_stream(q + static_cast<int64_t>(row) * qst + hh * qsh + c8 * 8) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    uint32_t bits = __vmaxu2(__vmaxu2(v[p].x & 0x7FFF7FFFu, v[p].y & 0x7FFF7FFFu),
+                             __vmaxu2(v[p].z & 0x7FFF7FFFu, v[p].w & 0x7FFF7FFFu));
+    float a = fmaxf(__uint_as_float((bits & 0xFFFFu) << 16), __uint_as_float(bits & 0xFFFF0000u));
+#pragma unroll
+    for (int o = VPR / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (c8 == 0) rmax[p * RPP + rin] = a;
+  }
+  __syncthreads();
+  float g = 0.0f;
+  if (threadIdx.x < 128) {                 // warps 0-3, whole warps
+    g = rmax[threadIdx.x];
+    const int span = q_block < 32 ? q_block : 32;
+    for (int o = 1; o < span; o <<= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, o));
+    if (q_block > 32 && (threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = g;
+  }
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    if (q_block > 32) {
+      const int wpg = q_block / 32, w0 = (threadIdx.x >> 5) / wpg * wpg;
+      g = wmax[w0];
+      for (int i = 1; i < wpg; ++i) g = fmaxf(g, wmax[w0 + i]);
+    }
+    rmax[threadIdx.x] = g;                 // now the maximum of row threadIdx.x's group
+    if ((threadIdx.x & (q_block - 1)) == 0)
+      q_scales[static_cast<int64_t>(hh) * (npad / q_block) + (row0 + threadIdx.x) / q_block] = g / 127.0f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int row = row0 + p * RPP + rin;
+    const float sc = rmax[p * RPP + rin] / 127.0f;
+    const float rr = 1.0f / sc;            // IEEE; unused when the scale is 0
+    const uint64_t ns2 = f2_pack(-sc, -sc), rr2 = f2_pack(rr, rr);
+    uint32_t w[4] = {0, 0, 0, 0};
+    if (row < n) {
+      float f[8];
+      unpack8(v[p], f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = i8codes_f16x2(f[2 * j], f[2 * j + 1], sc, ns2, rr2);
+    }
+    *reinterpret_cast<uint4*>(q_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // ---------------------------------------------------------------------------- kernel V
 // One CTA per (128-token block, head).  Phase 1: each work item loads 4 tokens x 8 channels,
 // encodes them and stores, per channel, one 32-bit word of 4 consecutive tokens into a
@@ -301,12 +380,17 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
     const int it = threadIdx.x + i * 256;
     const int c8 = it % VPR, tg = it / VPR;
     uint64_t ns2[4], r2[4];
-    bool zero[8];
+    float sc[8];
+    bool zero[8], sub = false;
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
       const float s0 = v_scales[hh * D + c8 * 8 + j], s1 = v_scales[hh * D + c8 * 8 + j + 1];
+      sc[j] = s0;
+      sc[j + 1] = s1;
       zero[j] = s0 == 0.0f;
       zero[j + 1] = s1 == 0.0f;
+      // A subnormal scale (a channel below 2^-117 everywhere) has no finite reciprocal.
+      sub = sub || (s0 != 0.0f && s0 < 1.17549435e-38f) || (s1 != 0.0f && s1 < 1.17549435e-38f);
       ns2[j / 2] = f2_pack(-s0, -s1);
       r2[j / 2] = f2_pack(1.0f / s0, 1.0f / s1);   // IEEE; unused when the scale is 0
     }
@@ -319,7 +403,12 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
         float y0, y1;
-        f2_unpack(div_rn2(f2_pack(f[j], f[j + 1]), ns2[j / 2], r2[j / 2]), y0, y1);
+        if (!sub) {
+          f2_unpack(div_rn2(f2_pack(f[j], f[j + 1]), ns2[j / 2], r2[j / 2]), y0, y1);
+        } else {
+          y0 = __fdiv_rn(f[j], sc[j]);
+          y1 = __fdiv_rn(f[j + 1], sc[j + 1]);
+        }
         if (t >= n || zero[j]) y0 = 0.0f;
         if (t >= n || zero[j + 1]) y1 = 0.0f;
         const uint32_t pr = e4m3x2(y0, y1);
@@ -364,16 +453,26 @@ cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, 
 }
 
 cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
-                            uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
+                            int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                             cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
-  dim3 grid(h, npad / 128, 2);
+  const int only_k = q_block != 128;
+  dim3 grid(h, npad / 128, only_k ? 1 : 2);
   if (d == 128)
-    quant_qk_kernel<128><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, q_codes,
-                                              q_scales, k_codes, k_scales);
+    quant_qk_kernel<128><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k,
+                                              q_codes, q_scales, k_codes, k_scales);
   else
-    quant_qk_kernel<64><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, q_codes,
-                                             q_scales, k_codes, k_scales);
+    quant_qk_kernel<64><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k,
+                                             q_codes, q_scales, k_codes, k_scales);
+  if (only_k) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 gq(h, npad / 128);
+    if (d == 128)
+      quant_q_grouped_kernel<128><<<gq, 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes, q_scales);
+    else
+      quant_q_grouped_kernel<64><<<gq, 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes, q_scales);
+  }
   return cudaGetLastError();
 }
 

@@ -49,9 +49,14 @@ sage_status check_out(const void* out, int64_t ost, int64_t osh) {
   return SAGE_OK;
 }
 
+// Rows per Q scale: 0 stands for the default 128; otherwise a power of two up to 128.
+int q_block_of(const sage_quantized* qz) { return qz->q_block == 0 ? 128 : static_cast<int>(qz->q_block); }
+bool q_block_ok(int64_t qb) { return qb == 0 || (qb >= 1 && qb <= 128 && (qb & (qb - 1)) == 0); }
+
 sage_status check_qz(const sage_quantized* qz, bool need_qk, bool need_v) {
   if (!qz) return SAGE_ERR_INVALID_ARG;
   if (need_qk) {
+    if (!q_block_ok(qz->q_block)) return SAGE_ERR_INVALID_ARG;
     if (!qz->q_codes || !qz->q_scales || !qz->k_codes || !qz->k_scales || !qz->k_mean) return SAGE_ERR_INVALID_ARG;
     if (!aligned16(qz->q_codes) || !aligned16(qz->k_codes) || !aligned16(qz->q_scales) ||
         !aligned16(qz->k_scales) || !aligned16(qz->k_mean))
@@ -92,6 +97,7 @@ Carve carve(void* base, int64_t n, int64_t h, int64_t d) {
   c.qz.k_codes = reinterpret_cast<uint16_t*>(take(size_t(h) * np * d * 2));
   c.qz.v_codes = reinterpret_cast<uint8_t*>(take(size_t(h) * d * np));
   c.qz.q_scales = reinterpret_cast<float*>(take(size_t(h) * (np / 128) * 4));
+  c.qz.q_block = 128;
   c.qz.k_scales = reinterpret_cast<float*>(take(size_t(h) * (np / 64) * 4));
   c.qz.k_mean = reinterpret_cast<float*>(take(size_t(h) * d * 4));
   c.qz.v_scales = reinterpret_cast<float*>(take(size_t(h) * d * 4));
@@ -144,8 +150,8 @@ sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const s
   cudaError_t e = sage::launch_colreduce(sv(k), int(n), int(h), int(d), false, part, s);
   if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), false, qz->k_mean, s);
   if (e == cudaSuccess)
-    e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), qz->q_codes, qz->q_scales,
-                              qz->k_codes, qz->k_scales, s);
+    e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), q_block_of(qz), qz->q_codes,
+                              qz->q_scales, qz->k_codes, qz->k_scales, s);
   return cuda_status(e);
 }
 
@@ -173,7 +179,7 @@ sage_status sage_attn_fwd_quantized(int64_t n, int64_t h, int64_t d, const sage_
   if ((st = check_out(out, ost, osh)) != SAGE_OK) return st;
   if (!status_block) return SAGE_ERR_INVALID_ARG;
   if (!(sm_scale > 0.0f) || sm_scale != sm_scale) return SAGE_ERR_INVALID_ARG;
-  return cuda_status(sage::launch_attn_fwd(int(n), int(h), int(d), *qz, sm_scale, out, ost, osh,
+  return cuda_status(sage::launch_attn_fwd(int(n), int(h), int(d), *qz, q_block_of(qz), sm_scale, out, ost, osh,
                                            static_cast<int32_t*>(status_block), static_cast<cudaStream_t>(stream)));
 }
 

@@ -34,15 +34,16 @@ cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool abs
                              cudaStream_t s);
 cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, bool absmax, float* out,
                             cudaStream_t s);
+// q_block: rows per Q scale, a power of two <= 128.
 cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
-                            uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
+                            int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                             cudaStream_t s);
 cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, int h, int d, uint8_t* v_codes,
                            cudaStream_t s);
 
 // attn_fwd.cu
-cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, float sm_scale, void* out, int64_t ost,
-                            int64_t osh, int32_t* status, cudaStream_t s);
+cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, int q_block, float sm_scale, void* out,
+                            int64_t ost, int64_t osh, int32_t* status, cudaStream_t s);
 cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
                             int col_tiles, int32_t* out, int32_t* status, cudaStream_t s);
 
