@@ -82,7 +82,8 @@ def test_q_block_bit_exact(name, q_block):
 
 def test_tiny_values_take_ieee_division():
     """A row, block or channel of values so small that its scale is subnormal (no finite
-    reciprocal) still quantises exactly like the oracle's IEEE division."""
+    reciprocal) still quantises exactly like the oracle's IEEE division.  The scaled rows
+    also hold exact -0.0 (negative values that underflow bf16): IEEE -0 / s = -0, E4M3 0x80."""
     import oracle
     from video_diffusion_transformer_sage_gb300 import synth
     inp = synth.make_inputs(synth.custom(256, 2, 128, "qkv", seed=9, n_outlier=1))
@@ -91,7 +92,9 @@ def test_tiny_values_take_ieee_division():
     st[:130, :] = (st[:130, :].float() * 2.0 ** -124).to(torch.bfloat16)   # Q, K, V rows 0..129 tiny
     st[:, 2 * hd + 5] = (st[:, 2 * hd + 5].float() * 2.0 ** -124).to(torch.bfloat16)  # one V channel tiny
     q, k, v = (st[:, i * hd:(i + 1) * hd].view(256, 2, 128) for i in range(3))
+    assert (v.view(torch.int16) == -32768).sum() >= 5                   # -0.0 present in V
     oz = oracle.Quantized(q, k, v, q_block=1)
+    assert (oz.v_codes == 0x80).sum() > 100
     assert (oz.q_scales[:, :130] < 2.0 ** -126).sum() > 100 and (oz.q_scales[:, :130] > 0).all()
     assert 0 < oz.v_scales[0, 5] < 2.0 ** -126
     dst = st.cuda()

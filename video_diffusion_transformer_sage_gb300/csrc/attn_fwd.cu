@@ -72,8 +72,8 @@ struct Cfg {
 
 struct AttnParams {
   int n, npad, h;
-  const float* q_scales;   // [H][npad >> q_shift]: one scale per 2^q_shift rows
-  int q_shift;
+  int q_shift;             // log2 of the rows per Q scale
+  const float* q_scales;   // [H][npad >> q_shift]
   const float* k_scales;   // [H][npad/64]
   const float* v_scales;   // [H][D]
   float sm_scale_log2;     // sm_scale * log2(e)
@@ -224,7 +224,10 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
   tmem_wait_st();
 }
 
-template <int D>
+// kRowQ: Q scales per 2^q_shift < 128 rows, so each softmax thread reads its own row's scale;
+// otherwise one scale per 128-row tile.  Two instantiations keep the default one's code as it
+// was: the per-row lookup alone measured 0.7 % slower there.
+template <int D, bool kRowQ>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
@@ -367,8 +370,14 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
     const int nbk = p.npad / 64;
-    // The scale of this thread's own row (its block of 2^q_shift rows); none past the padding.
-    const float qscale = row < p.npad ? p.q_scales[hh * (p.npad >> p.q_shift) + (row >> p.q_shift)] : 0.0f;
+    float qscale;
+    if (kRowQ) {
+      // The scale of this thread's own row (its block of 2^q_shift rows); none past the padding.
+      qscale = row < p.npad ? p.q_scales[hh * (p.npad >> p.q_shift) + (row >> p.q_shift)] : 0.0f;
+    } else {
+      const int nbq = p.npad / 128, qblk = (q0 + t * kBM) / 128;
+      qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
+    }
     const float cq = qscale * p.sm_scale_log2;
     const float* ks = p.k_scales + hh * nbk;
     float m = -INFINITY, l = 0.0f;
@@ -560,12 +569,13 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_bloc
       !make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.k_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||
       !make_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qz.v_codes, npad, static_cast<uint64_t>(h) * D, 128, D))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  static bool attr_set[2] = {false, false};
+  const bool row_q = q_block != 128;
+  if (!attr_set[row_q]) {
+    cudaError_t e = cudaFuncSetAttribute(row_q ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[row_q] = true;
   }
   AttnParams p;
   p.n = n;
@@ -583,7 +593,10 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_bloc
   p.status = status;
   p.wait_limit_ns = kWaitLimitNs;
   dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
-  attn_fwd_kernel<D><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
+  if (row_q)
+    attn_fwd_kernel<D, true><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
+  else
+    attn_fwd_kernel<D, false><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
 

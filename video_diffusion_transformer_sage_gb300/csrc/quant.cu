@@ -405,6 +405,10 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
         float y0, y1;
         if (!sub) {
           f2_unpack(div_rn2(f2_pack(f[j], f[j + 1]), ns2[j / 2], r2[j / 2]), y0, y1);
+          // The correction step turns x = -0 into +0 (-0 + +0); a positive divisor keeps the
+          // sign of x, and E4M3 has a signed zero (0x80), so take the sign from x.
+          y0 = copysignf(y0, f[j]);
+          y1 = copysignf(y1, f[j + 1]);
         } else {
           y0 = __fdiv_rn(f[j], sc[j]);
           y1 = __fdiv_rn(f[j + 1], sc[j + 1]);
