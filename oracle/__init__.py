@@ -24,7 +24,7 @@ _lock = threading.Lock()
 
 MUTATIONS = {"none": 0, "no_smooth": 1, "rescale_sign": 2, "scale_255": 3, "key_index": 4,
              "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8,
-             "q_block_index": 9}
+             "q_block_index": 9, "rope_sign": 10, "rms_sum": 11}
 
 Q_BLOCKS = (1, 2, 4, 8, 16, 32, 64, 128)
 
@@ -63,6 +63,7 @@ def lib():
             L.oracle_attn_sq_blk.argtypes = [P, P, I, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
             L.oracle_attn_exact.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double,
                                             P, I, P]
+            L.oracle_rmsnorm_rope.argtypes = [P, I, I, I, I, I, P, P, P, ctypes.c_float]
             L.oracle_num_threads.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -194,3 +195,17 @@ def attn_exact(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_scale: floa
     lib().oracle_attn_exact(pq, pk, pv, n, h, d, qst, qsh, kst, ksh, vst, vsh, float(sm_scale),
                             _ptr(rows), len(rows), _ptr(out))
     return out
+
+
+def rmsnorm_rope(x: torch.Tensor, gamma, cos, sin, eps: float) -> torch.Tensor:
+    """In place on a bf16 CPU [N, H, D] view with unit channel stride: RMSNorm over D with
+    weight gamma [D], then the rotation of channel pairs (2i, 2i+1) by the angles whose cos /
+    sin are given as [N, D/2] fp32.  Returns x."""
+    n, h, d = x.shape
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float32))
+    c = np.ascontiguousarray(np.asarray(cos, dtype=np.float32))
+    s = np.ascontiguousarray(np.asarray(sin, dtype=np.float32))
+    assert g.shape == (d,) and c.shape == (n, d // 2) and s.shape == (n, d // 2)
+    p, st, sh = _view_args(x)
+    lib().oracle_rmsnorm_rope(p, n, h, d, st, sh, _ptr(g), _ptr(c), _ptr(s), float(eps))
+    return x

@@ -100,3 +100,17 @@ def attn_exact(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: float) -> 
         p = np.exp(s - s.max(axis=1, keepdims=True))
         out[:, hh] = (p / p.sum(axis=1, keepdims=True)) @ v[:, hh]
     return out
+
+
+def rmsnorm_rope(x: np.ndarray, gamma: np.ndarray, cos: np.ndarray, sin: np.ndarray, eps: float) -> np.ndarray:
+    """fp64, [N, H, D]: RMSNorm over D with weight gamma, then each channel pair (2i, 2i+1)
+    rotated by the angle whose cos / sin are cos[t, i], sin[t, i].  No rounding to bf16."""
+    x = np.asarray(x, np.float64)
+    r = 1.0 / np.sqrt((x * x).mean(axis=2, keepdims=True) + eps)
+    y = x * r * np.asarray(gamma, np.float64)[None, None, :]
+    c = np.asarray(cos, np.float64)[:, None, :]
+    s = np.asarray(sin, np.float64)[:, None, :]
+    z = np.empty_like(y)
+    z[..., 0::2] = y[..., 0::2] * c - y[..., 1::2] * s
+    z[..., 1::2] = y[..., 0::2] * s + y[..., 1::2] * c
+    return z

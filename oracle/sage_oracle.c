@@ -18,6 +18,7 @@
  *   5. S = Qc Kc^T  exact integer dot products                             oracle_qk_int32
  *   6-8. softmax(S * s_q * s_k * sm_scale) with P held in E4M3, times V    oracle_attn_sq(_blk)
  *   9. exact fp64 softmax attention of the bf16 inputs                     oracle_attn_exact
+ *   0. (upstream of 1-4) in-place RMSNorm + rotary embedding of Q / K       oracle_rmsnorm_rope
  *
  * The shapes are those of the attention call profiled in
  * "gb10-sage2-p0-interleave-softmax-latency.json" (q_shape [1, 37810, 56, 128]).
@@ -40,7 +41,8 @@
  * the tests can show that the pins catch it.  Always 0 outside those tests. */
 enum { MUT_NONE = 0, MUT_NO_SMOOTH = 1, MUT_RESCALE_SIGN = 2, MUT_SCALE_255 = 3,
        MUT_KEY_INDEX = 4, MUT_V_SCALE_CHANNEL = 5, MUT_DROP_LAST_KEY = 6,
-       MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8, MUT_Q_BLOCK_INDEX = 9 };
+       MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8, MUT_Q_BLOCK_INDEX = 9, MUT_ROPE_SIGN = 10,
+       MUT_RMS_SUM = 11 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
 
@@ -388,6 +390,62 @@ void oracle_attn_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
 }
 
 /* Threads OpenMP will use (1 without OpenMP). */
+/* ------------------------------------------------------------------------------------
+ * 0. The qk_transform stage of the strided-NHD dataflow ("in-place ... RMSNorm and RoPE on
+ * strided views", gb10-sage-strided-nhd-summary key dataflow.qk_transform; timed as rms_rope
+ * in the block profile), in place on a bf16 [N, H, D] view, per (token t, head h):
+ *   ms = (sum_c x_c^2) / D,   r = 1 / sqrt(ms + eps),   y_c = (x_c * r) * gamma[c]
+ *   z_2i   = y_2i * cos[t][i] - y_2i+1 * sin[t][i]
+ *   z_2i+1 = y_2i * sin[t][i] + y_2i+1 * cos[t][i]           (rotation of channel pairs)
+ *   x_c <- bf16_RNE(z_c)
+ * The pages fix neither the precision nor the order of the sum, and the bf16 rounding of z
+ * turns a float into a code, so this follows the kernel's fp32 arithmetic exactly: every
+ * product and sum rounded to fp32 (no fused multiply-add), IEEE sqrt and division, and
+ * sum_c x_c^2 formed as D/8 partial sums of 8 consecutive channels (each in channel order)
+ * folded pairwise: partial g += partial g + stride for stride = D/16, ..., 2, 1.
+ * cos and sin hold [N][D/2] fp32 angles' cosines and sines (the caller's rotary table). */
+static inline uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40);   /* quiet NaN */
+  u += 0x7FFFu + ((u >> 16) & 1u);                                            /* ties to even */
+  return (uint16_t)(u >> 16);
+}
+
+void oracle_rmsnorm_rope(uint16_t* x, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                         const float* gamma, const float* cosb, const float* sinb, float eps) {
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t t = 0; t < n; ++t)
+    for (int64_t hh = 0; hh < h; ++hh) {
+      uint16_t* row = x + t * st + hh * sh;
+      float v[128], part[16];
+      for (int64_t c = 0; c < d; ++c) v[c] = bf16_to_f32(row[c]);
+      const int64_t ng = d / 8;
+      for (int64_t g = 0; g < ng; ++g) {
+        float acc = 0.0f;
+        for (int64_t j = 0; j < 8; ++j) {
+          float sq = v[8 * g + j] * v[8 * g + j];
+          acc = acc + sq;
+        }
+        part[g] = acc;
+      }
+      for (int64_t stride = ng / 2; stride >= 1; stride /= 2)
+        for (int64_t g = 0; g < stride; ++g) part[g] = part[g] + part[g + stride];
+      float ms = (g_mutation == MUT_RMS_SUM) ? part[0] : part[0] * (1.0f / (float)d);
+      float r = 1.0f / sqrtf(ms + eps);
+      for (int64_t i = 0; i < d / 2; ++i) {
+        float y0 = (v[2 * i] * r) * gamma[2 * i];
+        float y1 = (v[2 * i + 1] * r) * gamma[2 * i + 1];
+        float c = cosb[t * (d / 2) + i], s = sinb[t * (d / 2) + i];
+        float a = y0 * c, b = y1 * s, e = y0 * s, f = y1 * c;
+        float z0 = (g_mutation == MUT_ROPE_SIGN) ? a + b : a - b;
+        float z1 = e + f;
+        row[2 * i] = f32_to_bf16_rne(z0);
+        row[2 * i + 1] = f32_to_bf16_rne(z1);
+      }
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   extern int omp_get_max_threads(void);

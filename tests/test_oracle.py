@@ -386,6 +386,78 @@ def test_q_block_attention_matches_brute(oracle_lib, q_block):
     assert (t == a[:128]).all()
 
 
+# ---------------------------------------------------------------- qk_transform: RMSNorm + RoPE
+
+def _rr_inputs(n=96, h=3, d=128, seed=3):
+    inp = small_inputs(n=n, h=h, d=d, layout="qkv", seed=seed)
+    gq, _ = synth.qk_norm_weights(d)
+    cos, sin = synth.rope_table(synth.rope_positions(n, n_text=20, grid=(2, 4, 10)), d)
+    return inp, gq.numpy(), cos.numpy(), sin.numpy()
+
+
+def _rr_closed_forms_hold() -> bool:
+    """The two closed forms below, as one boolean (also used by the planted-mistake battery)."""
+    for d in (64, 128):
+        x = torch.full((5, 2, d), 2.0, dtype=torch.bfloat16)
+        oracle.rmsnorm_rope(x, np.ones(d), np.ones((5, d // 2)), np.zeros((5, d // 2)), 0.0)
+        if not (x.float() == 1.0).all():
+            return False
+    inp, g, _, _ = _rr_inputs()
+    n, h, d = inp.q.shape
+    a, b = inp.q.contiguous().clone(), inp.q.contiguous().clone()
+    oracle.rmsnorm_rope(a, g, np.ones((n, d // 2)), np.zeros((n, d // 2)), 1e-6)
+    oracle.rmsnorm_rope(b, g, np.zeros((n, d // 2)), np.ones((n, d // 2)), 1e-6)
+    ab, bb = a.view(torch.int16).numpy(), b.view(torch.int16).numpy()
+    return bool((bb[..., 1::2] == ab[..., 0::2]).all() and
+                (bb[..., 0::2] == (ab[..., 1::2] ^ np.int16(-32768))).all())
+
+
+def test_rmsnorm_rope_closed_forms(oracle_lib):
+    """(1) x = 2 everywhere, eps = 0, gamma = 1, no turn: mean square 4, r = 1/2, every output
+    exactly 1.  (2) A quarter turn (cos 0, sin 1): z_2i = -y_2i+1 and z_2i+1 = y_2i exactly,
+    i.e. the unturned result with each pair swapped and its first element negated."""
+    assert _rr_closed_forms_hold()
+
+
+def test_rmsnorm_rope_gamma_power_of_two_scales_exactly(oracle_lib):
+    inp, g, cos, sin = _rr_inputs()
+    a, b = inp.k.contiguous().clone(), inp.k.contiguous().clone()
+    oracle.rmsnorm_rope(a, g, cos, sin, 1e-6)
+    oracle.rmsnorm_rope(b, 2.0 * g, cos, sin, 1e-6)
+    assert torch.equal(b.float(), 2.0 * a.float())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_rmsnorm_rope_matches_brute(oracle_lib, d):
+    inp, g, cos, sin = _rr_inputs(d=d)
+    x = inp.q.contiguous().clone()
+    want = brute.rmsnorm_rope(x.float().numpy(), g, cos, sin, 1e-6)
+    got = oracle.rmsnorm_rope(x, g, cos, sin, 1e-6).float().numpy().astype(np.float64)
+    # bf16 rounding (half an ulp, 2^-9 relative) plus the fp32 arithmetic before it
+    assert (np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-6 * np.abs(want).max()).all()
+
+
+def test_rmsnorm_rope_unit_rms(oracle_lib):
+    """gamma = 1: the rotation keeps each pair's norm, so every (token, head) row leaves with
+    mean square ms / (ms + eps) -- 1 to within the bf16 rounding of its elements."""
+    inp, _, cos, sin = _rr_inputs()
+    x = oracle.rmsnorm_rope(inp.v.contiguous().clone(), np.ones(128), cos, sin, 1e-6).float().numpy()
+    ms = (x.astype(np.float64) ** 2).mean(axis=2)
+    assert np.abs(ms - 1.0).max() < 2.0 ** -7
+
+
+def test_rmsnorm_rope_in_place_on_strided_views(oracle_lib):
+    """On the Q slice of a token-major QKV buffer: the K and V slices stay untouched, and Q
+    becomes what the same op gives on a contiguous copy."""
+    inp, g, cos, sin = _rr_inputs()
+    before = inp.storage.clone()
+    ref = oracle.rmsnorm_rope(inp.q.contiguous().clone(), g, cos, sin, 1e-6)
+    oracle.rmsnorm_rope(inp.q, g, cos, sin, 1e-6)
+    hd = inp.q.shape[1] * inp.q.shape[2]
+    assert torch.equal(inp.storage[:, hd:].view(torch.int16), before[:, hd:].view(torch.int16))
+    assert torch.equal(inp.q.contiguous().view(torch.int16), ref.view(torch.int16))
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _pins_pass(inp) -> bool:
@@ -420,6 +492,8 @@ def _pins_pass(inp) -> bool:
     g32 = brute.attn_sq_global(q32.q_codes, q32.q_scales, q32.k_codes, q32.k_scales, q32.v_codes,
                                q32.v_scales, n, 0.125, q_block=32)
     if not np.abs(oracle.attn_sq(q32, 0.125, rows, tile=0) - g32).max() < 1e-12:
+        return False
+    if not _rr_closed_forms_hold():
         return False
     e = oracle.attn_exact(inp.q, inp.k, inp.v, 0.125, rows)
     b = brute.attn_exact(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), 0.125)

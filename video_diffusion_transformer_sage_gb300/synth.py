@@ -152,3 +152,50 @@ def sample_rows(n_tokens: int, count: int, seed: int) -> list:
         if r not in must:
             out.append(r)
     return sorted(out)
+
+
+# ---------------------------------------------------------------------------------------
+# Inputs of the qk_transform stage ("in-place ... RMSNorm and RoPE on strided views",
+# gb10-sage-strided-nhd-summary key dataflow.qk_transform).  The pages give neither the norm
+# weights nor the rotary table, so both are inputs made here; the norm and the rotation that
+# use them live in the CUDA kernel and in the oracle only.
+#   gamma: per-channel norm weights ~ N(1, 0.1^2), one vector for Q and one for K.
+#   positions: the 514 text / conditioning tokens get the 1-D position (t, t, t); the 37296
+#     video tokens a (frame, row, column) position on a 37 x 24 x 42 latent grid, in
+#     frame-major order (37 * 24 * 42 = 37296).
+#   table: D/2 channel pairs split into three bands (frame, row, column; the frame band takes
+#     the remainder), pair i of a band of size nb turning at base^(-i/nb) radians per
+#     position step; cos and sin of the angles computed in fp64, stored as fp32 [N, D/2].
+VIDEO_GRID = (37, 24, 42)
+
+
+def qk_norm_weights(head_dim: int, seed: int = 7):
+    g = torch.Generator("cpu").manual_seed(seed)
+    gq = (1.0 + 0.1 * torch.randn(head_dim, generator=g)).float()
+    gk = (1.0 + 0.1 * torch.randn(head_dim, generator=g)).float()
+    return gq, gk
+
+
+def rope_positions(n_tokens: int, n_text: int = 514, grid=VIDEO_GRID) -> torch.Tensor:
+    """[N, 3] int64 (frame, row, column) positions of the packed sequence."""
+    t = torch.arange(n_tokens, dtype=torch.int64)
+    v = (t - n_text).clamp(min=0)
+    _, gy, gx = grid
+    pos = torch.stack([v // (gy * gx), (v // gx) % gy, v % gx], dim=1)
+    text = t < n_text
+    pos[text] = t[text, None].expand(-1, 3)
+    return pos
+
+
+def rope_table(positions: torch.Tensor, head_dim: int, base: float = 10000.0):
+    """cos, sin fp32 [N, D/2] of the rotary angles of `positions` ([N, 3])."""
+    half = head_dim // 2
+    nb_y = nb_x = half // 3
+    nb_f = half - nb_y - nb_x
+    ang = torch.empty((positions.shape[0], half), dtype=torch.float64)
+    off = 0
+    for axis, nb in enumerate((nb_f, nb_y, nb_x)):
+        freq = base ** (-torch.arange(nb, dtype=torch.float64) / nb)
+        ang[:, off:off + nb] = positions[:, axis:axis + 1].double() * freq[None, :]
+        off += nb
+    return torch.cos(ang).float().contiguous(), torch.sin(ang).float().contiguous()
