@@ -293,7 +293,35 @@ def run_gpu(args):
             raise RuntimeError(f"device status {code} at {where}")
         call_timing = call_stats(rounds)
 
+    # ---- the qk_transform stage upstream of the path (in-place RMSNorm + rotary embedding of
+    # Q and K), timed on its own on a copy of the QKV buffer: 3 warm-up calls, then 20 calls,
+    # CUDA events per call.  Algorithmic bytes: Q and K read and written once (8 N H D) plus
+    # the fp32 cos / sin table (4 N D).
+    qk_transform = None
+    if not args.no_qk_transform and w.layout == "qkv":
+        gq, gk = synth.qk_norm_weights(d)
+        cos, sin = synth.rope_table(synth.rope_positions(n), d)
+        gq, gk, cos, sin = (t_.to(dev) for t_ in (gq, gk, cos, sin))
+        buf = storage.clone()
+        tq, tk, _ = views(buf)
+        for _ in range(3):
+            sage.sage_qk_rmsnorm_rope(tq, tk, gq, gk, cos, sin, 1e-6, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+        torch.cuda.synchronize()
+        for a_, b_ in ev:
+            a_.record(stream)
+            sage.sage_qk_rmsnorm_rope(tq, tk, gq, gk, cos, sin, 1e-6, stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        t_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
+        t_bytes = 8 * n * h * d + 4 * n * d
+        qk_transform = {"kernel": "rmsnorm_rope_kernel<%d>" % d, "ms": round(t_ms, 4), "bytes": t_bytes,
+                        "gbs": round(t_bytes / (t_ms * 1e-3) / 1e9, 1), "calls": 20}
+        del buf
+
     bf16_burst, bf16_sus, hbm, peak_src = _peaks()
+    if qk_transform is not None:
+        qk_transform["hbm_frac"] = round(qk_transform["gbs"] / hbm, 4)
     # The fused kernel does half its FLOPs as fp16 MMAs (QK^T on INT8 codes held in fp16)
     # and half as E4M3 MMAs (PV); the E4M3 rate is twice the 16-bit rate.  Its roofline is
     # the time of both halves at their own peaks.  The burst bf16 figure applies when the
@@ -336,6 +364,7 @@ def run_gpu(args):
                        "streams, double-buffered (step i overlaps H2D of i+1 and D2H of i-1)",
                 "serial_ms_per_step": round(e2e_serial_ms, 3)},
         "call_timing": call_timing,
+        "qk_transform": qk_transform,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -434,6 +463,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-call-timing", action="store_true",
                     help="skip the 5 x 10 per-call timing of sage_attn_fwd")
+    ap.add_argument("--no-qk-transform", action="store_true",
+                    help="skip the timing of the in-place RMSNorm + rotary stage")
     ap.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS with qkv layout")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -166,6 +166,28 @@ sage_status sage_attn_fwd_quantized(int64_t n_tokens, int64_t n_heads, int64_t h
                                     int64_t out_stride_token, int64_t out_stride_head,
                                     void* status_block, void* stream);
 
+/* The qk_transform stage upstream of the quantisation: RMSNorm and a rotary embedding of Q
+ * and K, in place on their strided views (the strided-NHD dataflow of
+ * "gb10-sage-strided-nhd-summary-1344x768-124f-seed440420.json", key dataflow.qk_transform;
+ * timed as rms_rope in the block-24 profile of the sampling-component page).  Per token t
+ * and head h of each of Q and K, in fp32, every product and sum rounded on its own:
+ *   ms = (sum_c x_c^2) / D, the sum as D/8 partial sums of 8 consecutive channels (each in
+ *        channel order) folded pairwise, partial g + partial g + s for s = D/16, ..., 1;
+ *   r  = 1 / sqrt(ms + eps) (IEEE sqrt and division);  y_c = (x_c * r) * gamma[c];
+ *   z_2i = y_2i cos[t][i] - y_2i+1 sin[t][i],  z_2i+1 = y_2i sin[t][i] + y_2i+1 cos[t][i];
+ *   x_c <- bf16 round-to-nearest-even(z_c).
+ * The pages give neither the norm weights nor the rotary table: both are caller inputs.
+ *   q, k: views as above (same shape); their data is WRITTEN in place.
+ *   gamma_q, gamma_k: device fp32 [D] norm weights of Q and K.
+ *   rope_cos, rope_sin: device fp32 [n_tokens][D/2]: cos and sin of the angle that turns
+ *     channel pair (2i, 2i+1) of token t (the caller's rotary table, e.g. 3-D positions).
+ *   eps: >= 0 and finite (a row of zeros with eps = 0 gives NaN, as the formula does).
+ * All device pointers 16-byte aligned.  Q and K may be slices of one projection buffer; they
+ * must not overlap each other. */
+sage_status sage_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const float* gamma_q,
+                                 const float* gamma_k, const float* rope_cos, const float* rope_sin,
+                                 float eps, void* stream);
+
 /* The whole path: sage_smooth_quant_qk, sage_quant_v and sage_attn_fwd_quantized on
  * buffers carved from ws (>= sage_workspace_bytes, 256-byte aligned; the status block at
  * its start must be zeroed once by the caller before first use). */

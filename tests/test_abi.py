@@ -11,7 +11,7 @@ from video_diffusion_transformer_sage_gb300 import _lib
 EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_bytes", "sage_status_block_bytes",
             "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
             "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
-            "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout"}
+            "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout", "sage_qk_rmsnorm_rope"}
 
 
 @pytest.fixture(scope="module")
@@ -94,6 +94,13 @@ def test_argument_validation_never_launches(L):
         qb.q_block = bad
         assert call(by(q), by(k), by(qb), 4096, 1 << 30, None) == 1, bad
         assert L.sage_attn_fwd_quantized(256, 2, 128, by(qb), 0.1, 4096, 256, 128, 4096, None) == 1, bad
+    # in-place RMSNorm + RoPE: null tables, misaligned weights, bad eps, mismatched views
+    rr = L.sage_qk_rmsnorm_rope
+    assert rr(by(q), by(k), 4096, 4096, 0, 4096, 1e-6, None) == 1
+    assert rr(by(q), by(k), 4100, 4096, 4096, 4096, 1e-6, None) == 2
+    assert rr(by(q), by(k), 4096, 4096, 4096, 4096, -1.0, None) == 1
+    assert rr(by(q), by(k), 4096, 4096, 4096, 4096, float("nan"), None) == 1
+    assert rr(by(q), by(_view(h=3)), 4096, 4096, 4096, 4096, 1e-6, None) == 1
     assert L.sage_check_device_status(0, None, None) == 1
     assert L.sage_debug_wait_timeout(0, 1000, None) == 1
     assert L.sage_debug_wait_timeout(4096, 0, None) == 1

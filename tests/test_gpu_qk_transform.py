@@ -1,0 +1,84 @@
+"""GPU parity of the in-place RMSNorm + rotary embedding of Q and K (the qk_transform stage)
+against the CPU oracle: every bf16 output bit-identical, V and everything outside the Q and K
+views untouched."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import video_diffusion_transformer_sage_gb300 as sage
+from video_diffusion_transformer_sage_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+
+
+def _tables(n, d, n_text=514, grid=synth.VIDEO_GRID):
+    gq, gk = synth.qk_norm_weights(d)
+    cos, sin = synth.rope_table(synth.rope_positions(n, n_text=n_text, grid=grid), d)
+    return gq, gk, cos, sin
+
+
+def _run_both(inp, n_text=514, grid=synth.VIDEO_GRID):
+    """(oracle result, GPU result) as whole input buffers (int16 bit patterns)."""
+    n, h, d = inp.q.shape
+    gq, gk, cos, sin = _tables(n, d, n_text, grid)
+    dev = torch.device("cuda:0")
+    storage = inp.storage.to(dev)
+
+    def dview(t):
+        off = t.storage_offset() - inp.storage.storage_offset()
+        return storage.as_strided(t.shape, t.stride(), storage.storage_offset() + off)
+
+    sage.sage_qk_rmsnorm_rope(dview(inp.q), dview(inp.k), gq.to(dev), gk.to(dev), cos.to(dev), sin.to(dev), EPS)
+    torch.cuda.synchronize()
+    oracle.rmsnorm_rope(inp.q, gq.numpy(), cos.numpy(), sin.numpy(), EPS)
+    oracle.rmsnorm_rope(inp.k, gk.numpy(), cos.numpy(), sin.numpy(), EPS)
+    return inp.storage.view(torch.int16).numpy(), storage.cpu().view(torch.int16).numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "strided64", "video"])
+def test_rmsnorm_rope_bit_exact(name):
+    inp = synth.make_inputs(name)
+    before = inp.storage.clone().view(torch.int16).numpy()
+    want, got = _run_both(inp)
+    assert np.array_equal(got, want)
+    if inp.storage.dim() == 2:                    # token-major QKV buffer: V slice untouched
+        hd = inp.q.shape[1] * inp.q.shape[2]
+        assert np.array_equal(got[:, 2 * hd:], before[:, 2 * hd:])
+    assert (want != before).any()                 # the transform did change Q and K
+
+
+@pytest.mark.parametrize("n,h,d", [(257, 3, 128), (129, 5, 64), (1, 1, 64)])
+def test_rmsnorm_rope_ragged_row_counts(n, h, d):
+    """Row counts that leave a partial CTA (and a single row)."""
+    inp = synth.make_inputs(synth.custom(n, h, d, "qkv", seed=n + h, n_outlier=1))
+    want, got = _run_both(inp, n_text=min(n, 20), grid=(4, 4, 8))
+    assert np.array_equal(got, want)
+
+
+def test_transform_then_attention_matches_oracle():
+    """The stage composed with the quantised attention: transform Q and K in place, then
+    sage_attn_fwd, against the oracle doing the same on the CPU."""
+    inp = synth.make_inputs(synth.custom(600, 4, 128, "qkv", seed=3, n_outlier=2))
+    n, h, d = inp.q.shape
+    gq, gk, cos, sin = _tables(n, d, n_text=100, grid=(2, 10, 25))
+    dev = torch.device("cuda:0")
+    storage = inp.storage.to(dev)
+    hd = h * d
+    q, k, v = (storage[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    sage.sage_qk_rmsnorm_rope(q, k, gq.to(dev), gk.to(dev), cos.to(dev), sin.to(dev), EPS)
+    sm = 1.0 / math.sqrt(d)
+    out = sage.sage_attn_fwd(q, k, v, sm)
+    torch.cuda.synchronize()
+    oracle.rmsnorm_rope(inp.q, gq.numpy(), cos.numpy(), sin.numpy(), EPS)
+    oracle.rmsnorm_rope(inp.k, gk.numpy(), cos.numpy(), sin.numpy(), EPS)
+    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    rows = list(range(n))
+    ref = oracle.attn_sq(qz, sm, rows, tile=128)
+    got = out.float().cpu().numpy().astype(np.float64)
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert rel <= 5e-3 and float(np.abs(got - ref).max()) <= 3e-2, rel

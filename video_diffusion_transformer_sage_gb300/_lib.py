@@ -73,6 +73,7 @@ def lib():
             "sage_debug_qk_int32": ([I, I, I, QP, I, I, I, I, I, P, P, P], ctypes.c_int),
             "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "sage_debug_wait_timeout": ([P, I, P], ctypes.c_int),
+            "sage_qk_rmsnorm_rope": ([VP, VP, P, P, P, P, F, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -238,3 +239,17 @@ def sage_check_device_status(status: torch.Tensor, stream=None):
     where = ctypes.c_int32(0)
     code = lib().sage_check_device_status(status.data_ptr(), _stream(stream), ctypes.byref(where))
     return int(code), int(where.value)
+
+
+def sage_qk_rmsnorm_rope(q: torch.Tensor, k: torch.Tensor, gamma_q: torch.Tensor, gamma_k: torch.Tensor,
+                         rope_cos: torch.Tensor, rope_sin: torch.Tensor, eps: float = 1e-6, stream=None) -> None:
+    """In place on the bf16 [N, H, D] CUDA views q and k: RMSNorm over D (weights gamma_q /
+    gamma_k, fp32 [D]) and the rotation of channel pairs by the fp32 [N, D/2] cos / sin table."""
+    n, h, d = q.shape
+    for t, shape in ((gamma_q, (d,)), (gamma_k, (d,)), (rope_cos, (n, d // 2)), (rope_sin, (n, d // 2))):
+        if t.dtype != torch.float32 or not t.is_cuda or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"expected a contiguous fp32 CUDA tensor of shape {shape}")
+    vq, vk = make_view(q), make_view(k)
+    _check(lib().sage_qk_rmsnorm_rope(ctypes.byref(vq), ctypes.byref(vk), gamma_q.data_ptr(), gamma_k.data_ptr(),
+                                      rope_cos.data_ptr(), rope_sin.data_ptr(), float(eps), _stream(stream)),
+           "sage_qk_rmsnorm_rope")

@@ -1,0 +1,141 @@
+// qk_transform.cu -- in-place RMSNorm + rotary embedding of Q and K on strided views.
+//
+// The qk_transform stage of the strided-NHD dataflow in
+// "gb10-sage-strided-nhd-summary-1344x768-124f-seed440420.json" (key dataflow.qk_transform:
+// RMSNorm and RoPE applied in place on the projection's strided views; timed as rms_rope in
+// the block-24 profile of "gb10-sampling-component-profile-1344x768-124f-seed440420.json").
+// It runs upstream of the K mean and the quantisation, on the same bf16 [N, H, D] views.
+//
+// Per (token t, head h), in fp32 with every product and sum rounded on its own (no
+// contraction into fused multiply-adds), IEEE square root and division:
+//   ms = (sum_c x_c^2) / D       the sum as D/8 partial sums of 8 consecutive channels, each
+//                                in channel order, folded pairwise by a butterfly over the
+//                                row's D/8 threads (partial g + partial g^s, s = D/16 .. 1)
+//   r  = 1 / sqrt(ms + eps),     y_c = (x_c * r) * gamma[c]
+//   z_2i = y_2i cos - y_2i+1 sin,   z_2i+1 = y_2i sin + y_2i+1 cos    (cos, sin of [t][i])
+//   x_c <- bf16_rne(z_c)
+// The pages fix no precision or order; this one is stated so that the result is reproducible
+// bit for bit.
+//
+// HBM-bound: each row is read once and written once (4 N H D bytes for Q and K together).
+// D/8 threads hold a row, 16 bytes each; every thread issues its loads for kRows rows before
+// any arithmetic.  The rotary table ([N][D/2] cos and sin, fp32) is read through L1/L2: a
+// token's 2 D bytes of table serve all H heads.
+#include <cuda_bf16.h>
+
+#include "sage_internal.h"
+
+namespace sage {
+namespace {
+
+constexpr int kRows = 4;   // rows in flight per thread
+
+__device__ __forceinline__ uint4 ld_rows(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// blockIdx.z: 0 = Q, 1 = K.  Rows (t, h) are numbered t * H + h, heads fastest, so that a
+// warp's rows lie in one token's contiguous H * D slice of the projection buffer.
+template <int D>
+__global__ void __launch_bounds__(256) rmsnorm_rope_kernel(uint16_t* q, int64_t qst, int64_t qsh, uint16_t* k,
+                                                           int64_t kst, int64_t ksh, int n, int h,
+                                                           const float* __restrict__ gamma_q,
+                                                           const float* __restrict__ gamma_k,
+                                                           const float* __restrict__ rope_cos,
+                                                           const float* __restrict__ rope_sin, float eps) {
+  constexpr int VPR = D / 8;            // threads per row
+  constexpr int RPP = 256 / VPR;        // rows per pass of the CTA
+  const bool is_k = blockIdx.z != 0;
+  uint16_t* x = is_k ? k : q;
+  const int64_t st = is_k ? kst : qst, sh = is_k ? ksh : qsh;
+  const float* gamma = is_k ? gamma_k : gamma_q;
+  const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
+  const int64_t nrows = static_cast<int64_t>(n) * h;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * (RPP * kRows);
+
+  uint4 v[kRows];
+  int64_t addr[kRows];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int64_t r = row0 + i * RPP + rin;
+    addr[i] = -1;
+    v[i] = make_uint4(0, 0, 0, 0);
+    if (r < nrows) {
+      const int64_t t = r / h, hh = r - t * h;
+      addr[i] = t * st + hh * sh + c8 * 8;
+      v[i] = ld_rows(x + addr[i]);
+    }
+  }
+  float g[8];
+  {
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8 + 4));
+    g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+    g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+  }
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int64_t r = row0 + i * RPP + rin;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, __fmul_rn(f[j], f[j]));
+#pragma unroll
+    for (int s = VPR / 2; s > 0; s >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, s));
+    if (r >= nrows) continue;           // whole rows only: the shuffles above ran in every lane
+    const float ms = __fmul_rn(acc, 1.0f / D);
+    const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    const int64_t t = r / h;
+    const float4 cs = __ldg(reinterpret_cast<const float4*>(rope_cos + t * (D / 2) + c8 * 4));
+    const float4 sn = __ldg(reinterpret_cast<const float4*>(rope_sin + t * (D / 2) + c8 * 4));
+    const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float y0 = __fmul_rn(__fmul_rn(f[2 * j], rs), g[2 * j]);
+      const float y1 = __fmul_rn(__fmul_rn(f[2 * j + 1], rs), g[2 * j + 1]);
+      const float z0 = __fsub_rn(__fmul_rn(y0, cc[j]), __fmul_rn(y1, ss[j]));
+      const float z1 = __fadd_rn(__fmul_rn(y0, ss[j]), __fmul_rn(y1, cc[j]));
+      o[j] = bf16x2_rne(z0, z1);
+    }
+    *reinterpret_cast<uint4*>(x + addr[i]) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_rope(const StridedView& q, const StridedView& k, int n, int h, int d,
+                                const float* gamma_q, const float* gamma_k, const float* rope_cos,
+                                const float* rope_sin, float eps, cudaStream_t s) {
+  const int64_t nrows = static_cast<int64_t>(n) * h;
+  const int vpr = d / 8, rows_per_cta = (256 / vpr) * kRows;
+  const int64_t blocks = (nrows + rows_per_cta - 1) / rows_per_cta;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(blocks), 1, 2);
+  uint16_t* qd = const_cast<uint16_t*>(q.data);
+  uint16_t* kd = const_cast<uint16_t*>(k.data);
+  if (d == 128)
+    rmsnorm_rope_kernel<128><<<grid, 256, 0, s>>>(qd, q.st, q.sh, kd, k.st, k.sh, n, h, gamma_q, gamma_k, rope_cos,
+                                                  rope_sin, eps);
+  else
+    rmsnorm_rope_kernel<64><<<grid, 256, 0, s>>>(qd, q.st, q.sh, kd, k.st, k.sh, n, h, gamma_q, gamma_k, rope_cos,
+                                                 rope_sin, eps);
+  return cudaGetLastError();
+}
+
+}  // namespace sage

@@ -3,6 +3,7 @@
 // attention path.  No entry point allocates device memory.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
@@ -169,6 +170,21 @@ sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws,
   if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), true, qz->v_scales, s);
   if (e == cudaSuccess) e = sage::launch_quant_v(sv(v), qz->v_scales, int(n), int(h), int(d), qz->v_codes, s);
   return cuda_status(e);
+}
+
+sage_status sage_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const float* gamma_q,
+                                 const float* gamma_k, const float* rope_cos, const float* rope_sin,
+                                 float eps, void* stream) {
+  sage_status st;
+  if ((st = check_view(q)) != SAGE_OK || (st = check_view(k)) != SAGE_OK) return st;
+  if (!same_shape(q, k)) return SAGE_ERR_INVALID_ARG;
+  if (!gamma_q || !gamma_k || !rope_cos || !rope_sin) return SAGE_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !(eps < INFINITY)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(gamma_q) || !aligned16(gamma_k) || !aligned16(rope_cos) || !aligned16(rope_sin))
+    return SAGE_ERR_ALIGNMENT;
+  return cuda_status(sage::launch_rmsnorm_rope(sv(q), sv(k), int(q->n_tokens), int(q->n_heads), int(q->head_dim),
+                                               gamma_q, gamma_k, rope_cos, rope_sin, eps,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 sage_status sage_attn_fwd_quantized(int64_t n, int64_t h, int64_t d, const sage_quantized* qz, float sm_scale,

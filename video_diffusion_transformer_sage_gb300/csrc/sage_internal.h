@@ -41,6 +41,11 @@ cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const fl
 cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, int h, int d, uint8_t* v_codes,
                            cudaStream_t s);
 
+// qk_transform.cu: in place on the Q and K views.
+cudaError_t launch_rmsnorm_rope(const StridedView& q, const StridedView& k, int n, int h, int d,
+                                const float* gamma_q, const float* gamma_k, const float* rope_cos,
+                                const float* rope_sin, float eps, cudaStream_t s);
+
 // attn_fwd.cu
 cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, int q_block, float sm_scale, void* out,
                             int64_t ost, int64_t osh, int32_t* status, cudaStream_t s);
