@@ -44,7 +44,8 @@ typedef enum sage_status {
   SAGE_OK = 0,
   SAGE_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, mismatched shapes */
   SAGE_ERR_ALIGNMENT = 2,       /* pointer not 16-byte aligned or stride not a multiple of 8 elements */
-  SAGE_ERR_UNSUPPORTED = 3,     /* head_dim not in {64, 128}; sizes beyond the int32 index range */
+  SAGE_ERR_UNSUPPORTED = 3,     /* head_dim not in {64, 128}; n_tokens > 2^22, n_heads > 4096 or
+                                   n_heads * N_pad >= 2^30 (every TMA row coordinate in int32) */
   SAGE_ERR_WORKSPACE = 4,       /* workspace pointer null or smaller than required */
   SAGE_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed */
   SAGE_ERR_DEVICE_TIMEOUT = 6   /* a bounded device-side wait expired (see sage_check_device_status) */

@@ -225,3 +225,67 @@ def test_edge_shapes_match_oracle(n, h, d):
     if n == 1:
         vdeq = oracle.brute.e4m3_decode(qz_o.v_codes[:, :, 0]) * qz_o.v_scales      # [H, D]
         assert np.abs(got[0] - vdeq).max() <= 1e-2 * np.abs(vdeq).max()
+
+
+def test_max_rises_at_every_tile():
+    """Queries along one direction u, keys orthogonal to u plus a component along u that grows
+    with the token index: every row's logits increase along the sequence, so its running max
+    rises at every 128-key tile and O is rescaled at every step (the path ordinary inputs take
+    only now and then)."""
+    n, h, d = 1500, 2, 128
+    g = torch.Generator("cpu").manual_seed(17)
+    u = torch.randn(h, d, generator=g)
+    u = u / u.norm(dim=1, keepdim=True)
+    kb = torch.randn(n, h, d, generator=g)
+    kb = kb - (kb * u[None]).sum(-1, keepdim=True) * u[None]          # orthogonal to u
+    ramp = torch.linspace(0.0, 6.0, n)[:, None, None]
+    k = kb + ramp * u[None]
+    q = 3.0 * u[None].expand(n, h, d) + 0.05 * torch.randn(n, h, d, generator=g)
+    v = torch.randn(n, h, d, generator=g)
+    qkv = torch.cat([t.reshape(n, h * d) for t in (q, k, v)], dim=1).to(torch.bfloat16)
+    hd = h * d
+    cq, ck, cv = (qkv[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    qz_o = oracle.Quantized(cq, ck, cv)
+    # the premise: tile maxima increase for the sampled rows (checked on the oracle's codes)
+    s = (qz_o.q_codes[0, :n].astype(np.int64) @ qz_o.k_codes[0, :n].astype(np.int64).T).astype(np.float64)
+    s *= np.repeat(qz_o.k_scales[0], 64)[None, :n]                    # the decision is on scaled logits
+    tile_max = np.stack([s[:, j:j + 128].max(axis=1) for j in range(0, n, 128)], axis=1)
+    assert (np.diff(tile_max, axis=1) > 0).mean() > 0.99
+    st = qkv.cuda()
+    q_, k_, v_ = (st[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    sm = 1.0 / math.sqrt(d)
+    status = sage.status_block()
+    qz = _gpu_qz({"q": q_, "k": k_, "v": v_})
+    out = sage.sage_attn_fwd_quantized(qz, sm, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    rows = list(range(n))
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = oracle.attn_sq(qz_o, sm, rows, tile=128)
+    assert rel_l2(got, ref) <= SQ_REL and np.abs(got - ref).max() <= SQ_ABS
+
+
+def test_largest_token_count():
+    """N = 2^22, the largest the library accepts (H = 1, D = 64): every index and TMA
+    coordinate at its limit.  Quantised operands bit-exact with the oracle at sampled rows,
+    output within the usual bars on sampled query rows (including the last tile)."""
+    n, h, d = 1 << 22, 1, 64
+    inp = synth.make_inputs(synth.custom(n, h, d, "qkv", seed=23, n_outlier=0))
+    st = inp.storage.cuda()
+    hd = h * d
+    q, k, v = (st[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    sm = 1.0 / math.sqrt(d)
+    qz = _gpu_qz({"q": q, "k": k, "v": v})
+    status = sage.status_block()
+    out = sage.sage_attn_fwd_quantized(qz, sm, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    oz = oracle.Quantized(inp.q, inp.k, inp.v)
+    assert np.array_equal(qz.k_mean.cpu().numpy().view(np.uint32), oz.k_mean.view(np.uint32))
+    for name in ("q_scales", "k_scales", "v_scales"):
+        assert np.array_equal(getattr(qz, name).cpu().numpy().view(np.uint32), getattr(oz, name).view(np.uint32)), name
+    sel = synth.sample_rows(n, 6, 29)
+    assert n - 1 in sel
+    assert np.array_equal(qz.q_codes[:, sel].cpu().float().numpy(), oz.q_codes[:, sel].astype(np.float32))
+    assert np.array_equal(qz.v_codes[:, :, -256:].cpu().numpy(), oz.v_codes[:, :, -256:])
+    got = out[sel].float().cpu().numpy().astype(np.float64)
+    ref = oracle.attn_sq(oz, sm, sel, tile=128)
+    assert rel_l2(got, ref) <= SQ_REL and np.abs(got - ref).max() <= SQ_ABS
