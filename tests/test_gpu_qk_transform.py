@@ -82,3 +82,12 @@ def test_transform_then_attention_matches_oracle():
     got = out.float().cpu().numpy().astype(np.float64)
     rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
     assert rel <= 5e-3 and float(np.abs(got - ref).max()) <= 3e-2, rel
+
+
+def test_rmsnorm_rope_hnd_layout():
+    """HND-contiguous Q and K (head stride N * D): heads are not contiguous within a token, so
+    the row kernel runs instead of the token-slice (bulk copy) kernel; same bits as the oracle."""
+    inp = synth.to_hnd(synth.make_inputs(synth.custom(700, 3, 128, "qkv", seed=5, n_outlier=1)))
+    assert inp.q.stride(1) == 700 * 128
+    want, got = _run_both(inp, n_text=50, grid=(5, 5, 26))
+    assert np.array_equal(got, want)

@@ -25,13 +25,15 @@
 // token's cos / sin (2 D bytes of fp32 table) once for them.  Stores stream (st.global.cs):
 // the rows are not read again by this kernel.  The loads cannot take the read-only
 // (non-coherent) path: the kernel writes the very addresses it reads.  Measured on the video
-// workload: 474 us for 2.19 GB (4.61 TB/s, 0.69 of the measured copy bandwidth); one row
+// workload: 474 us for 2.19 GB (4.61 TB/s, 0.69 of the measured copy bandwidth; the bulk kernel
+// below, 458 us); one row
 // per thread-iteration without the persistent loop reached 3.84 TB/s.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
 #include "sage_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace sage {
 namespace {
@@ -49,6 +51,55 @@ __device__ __forceinline__ uint4 ld_rows(const uint16_t* p) {
 __device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// ---- the row arithmetic, shared by both kernels ----------------------------------------
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+// sum_c x_c^2 of the row: the thread's 8 channels in channel order, then the butterfly over
+// the row's VPR consecutive lanes.  Every lane of the warp must call it.
+template <int VPR>
+__device__ __forceinline__ float row_sumsq(const float f[8]) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, __fmul_rn(f[j], f[j]));
+#pragma unroll
+  for (int s = VPR / 2; s > 0; s >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, s));
+  return acc;
+}
+
+// The thread's 8 channels after the norm (1 / sqrt(sum / D + eps), weight g) and the rotation
+// of its 4 channel pairs by (cs, sn), as 4 bf16x2 words.
+template <int D>
+__device__ __forceinline__ uint4 norm_rotate8(const float f[8], float sumsq, float eps, const float g[8],
+                                              const float4& cs, const float4& sn) {
+  const float ms = __fmul_rn(sumsq, 1.0f / D);
+  const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float y0 = __fmul_rn(__fmul_rn(f[2 * j], rs), g[2 * j]);
+    const float y1 = __fmul_rn(__fmul_rn(f[2 * j + 1], rs), g[2 * j + 1]);
+    const float z0 = __fsub_rn(__fmul_rn(y0, cc[j]), __fmul_rn(y1, ss[j]));
+    const float z1 = __fadd_rn(__fmul_rn(y0, ss[j]), __fmul_rn(y1, cc[j]));
+    o[j] = bf16x2_rne(z0, z1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ void load_gamma8(const float* gamma, int c8, float g[8]) {
+  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8));
+  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8 + 4));
+  g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+  g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
 }
 
 // blockIdx.z: 0 = Q, 1 = K.  Rows (t, h) are numbered t * H + h, heads fastest; batch b holds
@@ -72,12 +123,7 @@ __global__ void __launch_bounds__(256) rmsnorm_rope_kernel(uint16_t* q, int64_t 
   const uint32_t nrows = static_cast<uint32_t>(n) * static_cast<uint32_t>(h);
   const uint32_t nbatch = (nrows + kBatch - 1) / kBatch;
   float g[8];
-  {
-    const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8));
-    const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8 + 4));
-    g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-    g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-  }
+  load_gamma8(gamma, c8, g);
   uint4 v[kRows];
   auto load = [&](uint32_t b) {
 #pragma unroll
@@ -102,44 +148,101 @@ __global__ void __launch_bounds__(256) rmsnorm_rope_kernel(uint16_t* q, int64_t 
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       const uint32_t r = b * kBatch + rin * kRows + i;
-      const uint32_t w[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
       float f[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        f[2 * j] = __uint_as_float(w[j] << 16);
-        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-      float acc = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, __fmul_rn(f[j], f[j]));
-#pragma unroll
-      for (int s = VPR / 2; s > 0; s >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, s));
-      if (r >= nrows) continue;
-      const float ms = __fmul_rn(acc, 1.0f / D);
-      const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+      unpack_bf16x8(cur[i], f);
+      const float acc = row_sumsq<VPR>(f);
+      if (r >= nrows) continue;           // whole rows only: the shuffles above ran in every lane
       const uint32_t t = r / static_cast<uint32_t>(h);
       if (t != t_tab) {                 // the thread's rows are mostly heads of one token
         cs = __ldg(reinterpret_cast<const float4*>(rope_cos + static_cast<size_t>(t) * (D / 2) + c8 * 4));
         sn = __ldg(reinterpret_cast<const float4*>(rope_sin + static_cast<size_t>(t) * (D / 2) + c8 * 4));
         t_tab = t;
       }
-      const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float y0 = __fmul_rn(__fmul_rn(f[2 * j], rs), g[2 * j]);
-        const float y1 = __fmul_rn(__fmul_rn(f[2 * j + 1], rs), g[2 * j + 1]);
-        const float z0 = __fsub_rn(__fmul_rn(y0, cc[j]), __fmul_rn(y1, ss[j]));
-        const float z1 = __fadd_rn(__fmul_rn(y0, ss[j]), __fmul_rn(y1, cc[j]));
-        o[j] = bf16x2_rne(z0, z1);
-      }
+      const uint4 o = norm_rotate8<D>(f, acc, eps, g, cs, sn);
       {
         uint16_t* dst = x + t * st + (r - t * h) * sh + c8 * 8;
-        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(dst), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
                      : "memory");
       }
     }
   }
+}
+
+// Token slices through shared memory, for views whose heads lie contiguously in a token
+// (head stride D, as in the projection buffer): unit u < N is Q's token u, unit N + t is K's
+// token t, each H * D bf16 contiguous.  A persistent CTA takes units blockIdx.x + i gridDim.x;
+// thread 0 streams them in with bulk copies kBulkAhead units ahead into a ring of kBulkSlots
+// slots and writes each transformed slice back with a bulk store.  The bulk copies move whole
+// slices at DMA rates, which the in-place loads of the kernel above cannot (they may not take
+// the read-only path).  A slot is reloaded only after the store of its previous unit has
+// finished reading it; the compute of that unit ended at the barrier before that store.
+constexpr int kBulkSlots = 4, kBulkAhead = 2;
+constexpr int kBulkMaxBytes = 28672;   // H * D * 2 up to 28 KB (H <= 112 at D = 128)
+constexpr uint64_t kBulkWaitNs = 2000000000ull;
+
+template <int D>
+__global__ void __launch_bounds__(256) rmsnorm_rope_bulk_kernel(uint16_t* q, int64_t qst, uint16_t* k, int64_t kst,
+                                                                int n, int h, const float* __restrict__ gamma_q,
+                                                                const float* __restrict__ gamma_k,
+                                                                const float* __restrict__ rope_cos,
+                                                                const float* __restrict__ rope_sin, float eps) {
+  constexpr int VPR = D / 8, RPP = 256 / VPR;
+  extern __shared__ __align__(128) uint8_t slices[];
+  __shared__ __align__(8) uint64_t full[kBulkSlots];
+  const uint32_t bytes = static_cast<uint32_t>(h) * D * 2;
+  const uint32_t slot_bytes = (bytes + 127u) & ~127u;
+  const int units = 2 * n;
+  const int count = static_cast<int>(blockIdx.x) < units ? (units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  auto unit_ptr = [&](int i) -> uint16_t* {
+    const int u = blockIdx.x + i * gridDim.x;
+    return u < n ? q + static_cast<int64_t>(u) * qst : k + static_cast<int64_t>(u - n) * kst;
+  };
+  auto issue_load = [&](int i) {
+    const int sl = i % kBulkSlots;
+    mbar_arrive_expect_tx(full + sl, bytes);
+    bulk_load(slices + sl * slot_bytes, unit_ptr(i), bytes, full + sl);
+  };
+  if (threadIdx.x == 0) {
+    for (int sl = 0; sl < kBulkSlots; ++sl) mbar_init(full + sl, 1);
+    fence_mbar_init();
+    for (int i = 0; i < kBulkAhead && i < count; ++i) issue_load(i);
+  }
+  __syncthreads();
+  const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
+  float gq[8], gk[8];
+  load_gamma8(gamma_q, c8, gq);
+  load_gamma8(gamma_k, c8, gk);
+  for (int i = 0; i < count; ++i) {
+    if (threadIdx.x == 0 && i + kBulkAhead < count) {
+      bulk_wait_read<kBulkSlots - kBulkAhead - 1>();   // the store of unit i + kBulkAhead - kBulkSlots
+      issue_load(i + kBulkAhead);
+    }
+    const int sl = i % kBulkSlots;
+    const bool landed = mbar_wait(full + sl, (i / kBulkSlots) & 1, kBulkWaitNs);
+    if (!__syncthreads_and(landed)) break;   // a copy that never lands (a failing device): stop
+    const int u = blockIdx.x + i * gridDim.x;
+    const bool is_k = u >= n;
+    const int64_t t = is_k ? u - n : u;
+    const float4 cs = __ldg(reinterpret_cast<const float4*>(rope_cos + t * (D / 2) + c8 * 4));
+    const float4 sn = __ldg(reinterpret_cast<const float4*>(rope_sin + t * (D / 2) + c8 * 4));
+    uint16_t* base = reinterpret_cast<uint16_t*>(slices + sl * slot_bytes);
+    for (int r0 = 0; r0 < h; r0 += RPP) {
+      const int r = r0 + rin;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < h) v = *reinterpret_cast<const uint4*>(base + r * D + c8 * 8);
+      float f[8];
+      unpack_bf16x8(v, f);
+      const float acc = row_sumsq<VPR>(f);
+      if (r < h) *reinterpret_cast<uint4*>(base + r * D + c8 * 8) = norm_rotate8<D>(f, acc, eps, is_k ? gk : gq, cs, sn);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      bulk_store(unit_ptr(i), base, bytes);
+      bulk_commit();
+    }
+  }
+  if (threadIdx.x == 0) bulk_wait_all();
 }
 
 }  // namespace
@@ -147,6 +250,32 @@ __global__ void __launch_bounds__(256) rmsnorm_rope_kernel(uint16_t* q, int64_t 
 cudaError_t launch_rmsnorm_rope(const StridedView& q, const StridedView& k, int n, int h, int d,
                                 const float* gamma_q, const float* gamma_k, const float* rope_cos,
                                 const float* rope_sin, float eps, cudaStream_t s) {
+  const int64_t slice = static_cast<int64_t>(h) * d * 2;
+  if (q.sh == d && k.sh == d && slice <= kBulkMaxBytes) {
+    // Heads contiguous in each token: whole token slices by bulk copy.
+    const int slot = static_cast<int>((slice + 127) / 128 * 128);
+    const int smem = kBulkSlots * slot;
+    int sms = 0, dev = 0, occ = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = d == 128 ? cudaFuncSetAttribute(rmsnorm_rope_bulk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                   : cudaFuncSetAttribute(rmsnorm_rope_bulk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = d == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rmsnorm_rope_bulk_kernel<128>, 256, smem)
+                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rmsnorm_rope_bulk_kernel<64>, 256, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(int64_t(2) * n, int64_t(sms) * std::max(occ, 1)));
+    uint16_t* qd = const_cast<uint16_t*>(q.data);
+    uint16_t* kd = const_cast<uint16_t*>(k.data);
+    if (d == 128)
+      rmsnorm_rope_bulk_kernel<128><<<static_cast<unsigned>(grid), 256, smem, s>>>(qd, q.st, kd, k.st, n, h, gamma_q,
+                                                                                  gamma_k, rope_cos, rope_sin, eps);
+    else
+      rmsnorm_rope_bulk_kernel<64><<<static_cast<unsigned>(grid), 256, smem, s>>>(qd, q.st, kd, k.st, n, h, gamma_q,
+                                                                                 gamma_k, rope_cos, rope_sin, eps);
+    return cudaGetLastError();
+  }
   const int64_t nrows = static_cast<int64_t>(n) * h;
   const int vpr = d / 8, rows_per_cta = (256 / vpr) * kRows;
   const int64_t blocks = (nrows + rows_per_cta - 1) / rows_per_cta;
