@@ -18,16 +18,14 @@
 // bit for bit.
 //
 // HBM-bound: each row is read once and written once (8 N H D bytes for Q and K together).
-// D/8 threads hold a row, 16 bytes each.  The grid is persistent (as many CTAs as fit,
-// half for Q, half for K), striding over batches of rows; each thread loads its rows of the
-// next batch before it computes and stores those of the current one, so two batches are in
-// flight.  A thread's rows are consecutive, i.e. mostly heads of one token, so it loads that
-// token's cos / sin (2 D bytes of fp32 table) once for them.  Stores stream (st.global.cs):
-// the rows are not read again by this kernel.  The loads cannot take the read-only
-// (non-coherent) path: the kernel writes the very addresses it reads.  Measured on the video
-// workload: 474 us for 2.19 GB (4.61 TB/s, 0.69 of the measured copy bandwidth; the bulk kernel
-// below, 458 us); one row
-// per thread-iteration without the persistent loop reached 3.84 TB/s.
+// Two kernels, the same row arithmetic (the inline functions below), identical results:
+//  * rmsnorm_rope_bulk_kernel, when the heads of a token are contiguous (head stride D): whole
+//    token slices move between HBM and shared memory by bulk copy (458 us on the video
+//    workload, 4.77 TB/s);
+//  * rmsnorm_rope_kernel, for any strides: D/8 threads hold a row, 16 bytes each; a persistent
+//    grid strides over batches of rows, each thread loading its rows of the next batch before
+//    it computes and stores those of the current one (474 us, 4.61 TB/s).
+// Neither may load through the read-only (non-coherent) path: they write what they read.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -103,8 +101,10 @@ __device__ __forceinline__ void load_gamma8(const float* gamma, int c8, float g[
 }
 
 // blockIdx.z: 0 = Q, 1 = K.  Rows (t, h) are numbered t * H + h, heads fastest; batch b holds
-// rows [b * kBatch, (b + 1) * kBatch), thread (rin, c8) rows b * kBatch + rin * kRows + i.
-// Persistent: gridDim.x CTAs stride over the batches.
+// rows [b * kBatch, (b + 1) * kBatch), thread (rin, c8) rows b * kBatch + rin * kRows + i, so
+// a thread's rows are mostly heads of one token and it loads that token's cos / sin once for
+// them.  Persistent: gridDim.x CTAs stride over the batches.  Stores stream (st.global.cs):
+// the rows are not read again here.
 template <int D>
 __global__ void __launch_bounds__(256) rmsnorm_rope_kernel(uint16_t* q, int64_t qst, int64_t qsh, uint16_t* k,
                                                            int64_t kst, int64_t ksh, int n, int h,
