@@ -179,7 +179,7 @@ def run_gpu(args):
     status = sage.status_block(dev)
     out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 7   # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, attention
+    launches_per_step = 8   # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, quant_v_fixup, attention
 
     def step(ev=None):
         if ev is not None:

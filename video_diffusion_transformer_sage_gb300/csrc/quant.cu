@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "sage_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -152,13 +154,19 @@ __device__ __forceinline__ uint64_t div_rn2(uint64_t x2, uint64_t neg_s2, uint64
   return f2_fma(e2, r2, y2);
 }
 
+// A nonzero scale below the smallest normal float has no finite reciprocal, so the
+// reciprocal route of div_rn2 does not apply; it needs a block of values below ~2^-119.
+// Kernels test it once per block and take a separate, directly dividing loop for it.
+__device__ __forceinline__ bool subnormal_scale(float s) { return s != 0.0f && s < 1.17549435e-38f; }
+
 // Two INT8 codes (held as fp16) of x0, x1 for block scale s (r = RN(1/s)):
-// clamp(rint(RN(x / s)), -127, 127), or 0 when s == 0.  The reciprocal route needs a finite
-// r, i.e. a normal s; a subnormal scale (a block of values below 2^-119) divides directly.
+// clamp(rint(RN(x / s)), -127, 127), or 0 when s == 0.  kDivide: IEEE division instead of
+// the reciprocal route (for a subnormal s).
+template <bool kDivide = false>
 __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, uint64_t neg_s2, uint64_t r2) {
   if (s == 0.0f) return 0u;
   float q0, q1;
-  if (s >= 1.17549435e-38f) {
+  if (!kDivide) {
     f2_unpack(div_rn2(f2_pack(x0, x1), neg_s2, r2), q0, q1);
   } else {
     q0 = __fdiv_rn(x0, s);
@@ -177,7 +185,8 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
 // Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
 // all its loads before any arithmetic; the maxima share one block reduction.
 template <int D>
-__global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
+// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.
+__global__ void __launch_bounds__(256, 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
                                                        const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
                                                        const float* __restrict__ k_mean, int n, int npad, int only_k,
                                                        uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
@@ -251,23 +260,30 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const uint16_t* __restric
   const uint64_t ns02 = f2_pack(-s0, -s0), r02 = f2_pack(r0, r0);
   const uint64_t ns12 = f2_pack(-s1, -s1), r12 = f2_pack(r1, r1);
   uint16_t* dst = is_k ? k_codes : q_codes;
+  auto write_codes = [&](auto divide) {
+    constexpr bool kDiv = decltype(divide)::value;
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const int row = row0 + p * RPP + rin;
-    const bool lo = p < NP / 2;
-    const float sc = lo ? s0 : s1;
-    const uint64_t ns2 = lo ? ns02 : ns12, rr2 = lo ? r02 : r12;
-    uint32_t w[4] = {0, 0, 0, 0};
-    if (row < n) {
-      float f[8];
-      unpack8(v[p], f);
+    for (int p = 0; p < NP; ++p) {
+      const int row = row0 + p * RPP + rin;
+      const bool lo = p < NP / 2;
+      const float sc = lo ? s0 : s1;
+      const uint64_t ns2 = lo ? ns02 : ns12, rr2 = lo ? r02 : r12;
+      uint32_t w[4] = {0, 0, 0, 0};
+      if (row < n) {
+        float f[8];
+        unpack8(v[p], f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        w[j] = i8codes_f16x2(f[2 * j] - mu[2 * j], f[2 * j + 1] - mu[2 * j + 1], sc, ns2, rr2);
+        for (int j = 0; j < 4; ++j)
+          w[j] = i8codes_f16x2<kDiv>(f[2 * j] - mu[2 * j], f[2 * j + 1] - mu[2 * j + 1], sc, ns2, rr2);
+      }
+      *reinterpret_cast<uint4*>(dst + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4*>(dst + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
-        make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  };
+  if (!subnormal_scale(s0) && !subnormal_scale(s1))   // uniform over the CTA
+    write_codes(std::false_type{});
+  else
+    write_codes(std::true_type{});
   if (threadIdx.x == 0) {
     if (is_k) {
       k_scales[hh * (npad / 64) + 2 * b] = s0;
@@ -342,8 +358,13 @@ __global__ void __launch_bounds__(256) quant_q_grouped_kernel(const uint16_t* __
     if (row < n) {
       float f[8];
       unpack8(v[p], f);
+      if (!subnormal_scale(sc)) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = i8codes_f16x2(f[2 * j], f[2 * j + 1], sc, ns2, rr2);
+        for (int j = 0; j < 4; ++j) w[j] = i8codes_f16x2(f[2 * j], f[2 * j + 1], sc, ns2, rr2);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = i8codes_f16x2<true>(f[2 * j], f[2 * j + 1], sc, ns2, rr2);
+      }
     }
     *reinterpret_cast<uint4*>(q_codes + (static_cast<int64_t>(hh) * npad + row) * D + c8 * 8) =
         make_uint4(w[0], w[1], w[2], w[3]);
@@ -356,6 +377,8 @@ __global__ void __launch_bounds__(256) quant_q_grouped_kernel(const uint16_t* __
 // [D][33]-word shared tile.  Phase 2: 8 threads write each channel's 128 contiguous bytes
 // of v_codes[h][c][block] with 16-byte stores.
 template <int D>
+// The codes of a channel with a subnormal scale (no finite reciprocal) come out wrong here and
+// are rewritten by quant_v_fixup_kernel, so the loop below stays free of that case.
 __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict__ v, int64_t st, int64_t sh,
                                                       const float* __restrict__ v_scales, int n, int npad,
                                                       uint8_t* __restrict__ v_codes) {
@@ -380,17 +403,12 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
     const int it = threadIdx.x + i * 256;
     const int c8 = it % VPR, tg = it / VPR;
     uint64_t ns2[4], r2[4];
-    float sc[8];
-    bool zero[8], sub = false;
+    bool zero[8];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
       const float s0 = v_scales[hh * D + c8 * 8 + j], s1 = v_scales[hh * D + c8 * 8 + j + 1];
-      sc[j] = s0;
-      sc[j + 1] = s1;
       zero[j] = s0 == 0.0f;
       zero[j + 1] = s1 == 0.0f;
-      // A subnormal scale (a channel below 2^-117 everywhere) has no finite reciprocal.
-      sub = sub || (s0 != 0.0f && s0 < 1.17549435e-38f) || (s1 != 0.0f && s1 < 1.17549435e-38f);
       ns2[j / 2] = f2_pack(-s0, -s1);
       r2[j / 2] = f2_pack(1.0f / s0, 1.0f / s1);   // IEEE; unused when the scale is 0
     }
@@ -403,16 +421,11 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
         float y0, y1;
-        if (!sub) {
-          f2_unpack(div_rn2(f2_pack(f[j], f[j + 1]), ns2[j / 2], r2[j / 2]), y0, y1);
-          // The correction step turns x = -0 into +0 (-0 + +0); a positive divisor keeps the
-          // sign of x, and E4M3 has a signed zero (0x80), so take the sign from x.
-          y0 = copysignf(y0, f[j]);
-          y1 = copysignf(y1, f[j + 1]);
-        } else {
-          y0 = __fdiv_rn(f[j], sc[j]);
-          y1 = __fdiv_rn(f[j + 1], sc[j + 1]);
-        }
+        f2_unpack(div_rn2(f2_pack(f[j], f[j + 1]), ns2[j / 2], r2[j / 2]), y0, y1);
+        // The correction step turns x = -0 into +0 (-0 + +0); a positive divisor keeps the sign
+        // of x, and E4M3 has a signed zero (0x80), so take the sign from x.
+        y0 = copysignf(y0, f[j]);
+        y1 = copysignf(y1, f[j + 1]);
         if (t >= n || zero[j]) y0 = 0.0f;
         if (t >= n || zero[j + 1]) y1 = 0.0f;
         const uint32_t pr = e4m3x2(y0, y1);
@@ -429,6 +442,26 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
     const int c = o >> 3, seg = o & 7;
     const uint4 w = make_uint4(tile[c][seg * 4], tile[c][seg * 4 + 1], tile[c][seg * 4 + 2], tile[c][seg * 4 + 3]);
     *reinterpret_cast<uint4*>(v_codes + (static_cast<int64_t>(hh) * D + c) * npad + t_base + seg * 16) = w;
+  }
+}
+
+// One CTA per head: if a channel of the head has a subnormal scale (all |v| of the channel
+// below ~2^-117), its codes are recomputed with IEEE division; otherwise the CTA exits at once.
+template <int D>
+__global__ void __launch_bounds__(256) quant_v_fixup_kernel(const uint16_t* __restrict__ v, int64_t st, int64_t sh,
+                                                            const float* __restrict__ v_scales, int n, int npad,
+                                                            uint8_t* __restrict__ v_codes) {
+  const int hh = blockIdx.x;
+  bool sub = false;
+  for (int c = threadIdx.x; c < D; c += 256) sub = sub || subnormal_scale(v_scales[hh * D + c]);
+  if (!__syncthreads_or(sub)) return;
+  for (int c = 0; c < D; ++c) {
+    const float sc = v_scales[hh * D + c];
+    if (!subnormal_scale(sc)) continue;
+    for (int t = threadIdx.x; t < n; t += 256) {
+      const float x = __uint_as_float(static_cast<uint32_t>(v[static_cast<int64_t>(t) * st + hh * sh + c]) << 16);
+      v_codes[(static_cast<int64_t>(hh) * D + c) * npad + t] = static_cast<uint8_t>(e4m3x2(__fdiv_rn(x, sc), 0.0f) & 0xFFu);
+    }
   }
 }
 
@@ -488,6 +521,12 @@ cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, i
     quant_v_kernel<128><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
   else
     quant_v_kernel<64><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (d == 128)
+    quant_v_fixup_kernel<128><<<h, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
+  else
+    quant_v_fixup_kernel<64><<<h, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
   return cudaGetLastError();
 }
 
