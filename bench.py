@@ -228,6 +228,7 @@ def run_gpu(args):
     # loop.  The serial variant (copy, compute, copy, in order) is reported beside it.
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 10))
     e2e_ms = e2e_serial_ms = float("nan")
+    e2e_runs = []
     host_out = [torch.empty((n, h, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     if e2e_steps:
         ws = sage.workspace(n, h, d, dev)
@@ -237,28 +238,36 @@ def run_gpu(args):
         comp = torch.cuda.current_stream(dev)
 
         def run(steps, pipelined):
+            # The H2D of step i+1 is enqueued before the D2H of step i: a D2H waits for its
+            # step's compute, and if both copy streams share one copy engine, a prefetch
+            # queued behind it would wait for that compute too (measured: 29-30 ms per step
+            # instead of 23.8 on some runs).
             ev_in = [torch.cuda.Event() for _ in range(steps)]
             ev_done = [torch.cuda.Event() for _ in range(steps)]
             ev_out = [torch.cuda.Event() for _ in range(steps)]
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            sin = s_in if pipelined else comp
+            sout = s_out if pipelined else comp
             torch.cuda.synchronize()
             a.record(comp)
-            s_in.wait_event(a)
+            sin.wait_event(a)
+            with torch.cuda.stream(sin):
+                bufs[0].copy_(host, non_blocking=True)
+            ev_in[0].record(sin)
             for i in range(steps):
                 k_ = i % 2
-                sin = s_in if pipelined else comp
-                sout = s_out if pipelined else comp
-                if i >= 2:
-                    sin.wait_event(ev_done[i - 2])      # compute of step i-2 released buffer k_
-                with torch.cuda.stream(sin):
-                    bufs[k_].copy_(host, non_blocking=True)
-                ev_in[i].record(sin)
                 comp.wait_event(ev_in[i])
                 if i >= 2:
                     comp.wait_event(ev_out[i - 2])      # D2H of step i-2 released output k_
                 qv, kv, vv = views(bufs[k_])
                 sage.sage_attn_fwd(qv, kv, vv, sm_scale, outs[k_], ws, comp)
                 ev_done[i].record(comp)
+                if i + 1 < steps:
+                    if i >= 1:
+                        sin.wait_event(ev_done[i - 1])  # compute of step i-1 released buffer (i+1)%2
+                    with torch.cuda.stream(sin):
+                        bufs[(i + 1) % 2].copy_(host, non_blocking=True)
+                    ev_in[i + 1].record(sin)
                 sout.wait_event(ev_done[i])
                 with torch.cuda.stream(sout):
                     host_out[k_].copy_(outs[k_], non_blocking=True)
@@ -269,7 +278,10 @@ def run_gpu(args):
             return a.elapsed_time(b) / steps
 
         run(2, True)
-        e2e_ms = reduce_max(run(e2e_steps, True), pg, dev)
+        # The overlap of copies with compute varies from run to run on these boxes (23.8 or
+        # 27.6-30 ms per step for the same code): three runs, the median reported, all listed.
+        e2e_runs = [run(e2e_steps, True) for _ in range(3)]
+        e2e_ms = reduce_max(statistics.median(e2e_runs), pg, dev)
         e2e_serial_ms = run(e2e_steps, False)
 
     # ---- per-call distribution of the public call, in the pages' protocol: after the warm-up
@@ -315,7 +327,9 @@ def run_gpu(args):
         torch.cuda.synchronize()
         t_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
         t_bytes = 8 * n * h * d + 4 * n * d
-        qk_transform = {"kernel": "rmsnorm_rope_kernel<%d>" % d, "ms": round(t_ms, 4), "bytes": t_bytes,
+        kname = ("rmsnorm_rope_bulk_kernel<%d>" if tq.stride(1) == d and tk.stride(1) == d
+                 else "rmsnorm_rope_kernel<%d>") % d
+        qk_transform = {"kernel": kname, "ms": round(t_ms, 4), "bytes": t_bytes,
                         "gbs": round(t_bytes / (t_ms * 1e-3) / 1e9, 1), "calls": 20}
         del buf
 
@@ -361,8 +375,10 @@ def run_gpu(args):
                 "h2d_bytes_per_step": int(host.numel() * 2), "d2h_bytes_per_step": int(host_out[0].numel() * 2),
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
                 "how": "pinned host QKV -> H2D, sage_attn_fwd, D2H -> pinned host each step; copies on their own "
-                       "streams, double-buffered (step i overlaps H2D of i+1 and D2H of i-1)",
-                "serial_ms_per_step": round(e2e_serial_ms, 3)},
+                       "streams, double-buffered (step i overlaps H2D of i+1 and D2H of i-1; the H2D of i+1 "
+                       "is enqueued before the D2H of i)",
+                "serial_ms_per_step": round(e2e_serial_ms, 3),
+                "pipelined_runs_ms": [round(x, 3) for x in e2e_runs] if e2e_steps else []},
         "call_timing": call_timing,
         "qk_transform": qk_transform,
         "gpu_launches": launches_per_step * args.steps,
