@@ -24,9 +24,10 @@ _lock = threading.Lock()
 
 MUTATIONS = {"none": 0, "no_smooth": 1, "rescale_sign": 2, "scale_255": 3, "key_index": 4,
              "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8,
-             "q_block_index": 9, "rope_sign": 10, "rms_sum": 11}
+             "q_block_index": 9, "rope_sign": 10, "rms_sum": 11, "v_mean_sign": 12, "p_i8_255": 13}
 
 Q_BLOCKS = (1, 2, 4, 8, 16, 32, 64, 128)
+V_FORMATS = {"e4m3": 0, "int8": 1}
 
 
 def build(force: bool = False) -> str:
@@ -58,6 +59,8 @@ def lib():
             L.oracle_quant_q_blk.argtypes = [P, I, I, I, I, I, I, P, P]
             L.oracle_quant_k.argtypes = [P, I, I, I, I, I, P, P, P]
             L.oracle_quant_v.argtypes = [P, I, I, I, I, I, P, P]
+            L.oracle_quant_v_fmt.argtypes = [P, I, I, I, I, I, P, I, P, P]
+            L.oracle_attn_sq_v.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, ctypes.c_double, P, I, I, I, P]
             L.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, I, I, I, P]
             L.oracle_attn_sq.argtypes = [P, P, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
             L.oracle_attn_sq_blk.argtypes = [P, P, I, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
@@ -138,26 +141,43 @@ def quant_k(k: torch.Tensor, mu: np.ndarray):
     return codes, scales
 
 
-def quant_v(v: torch.Tensor):
+def channel_mean(x: torch.Tensor) -> np.ndarray:
+    """Mean over the tokens of each (head, channel), in the order of the K mean: [H, D] fp32."""
+    return k_mean(x)
+
+
+def quant_v(v: torch.Tensor, v_format: str = "e4m3", mean=None):
+    """V codes [H, D, N_pad] (uint8 E4M3 bytes, or int8 codes) and scales [H, D].
+    mean: None, or the [H, D] fp32 mean taken out of V before quantisation."""
     n, h, d = v.shape
     np_ = pad128(n)
-    codes = np.zeros((h, d, np_), np.uint8)
+    fmt = V_FORMATS[v_format]
+    codes = np.zeros((h, d, np_), np.int8 if fmt else np.uint8)
     scales = np.zeros((h, d), np.float32)
     p, st, sh = _view_args(v)
-    lib().oracle_quant_v(p, n, h, d, st, sh, _ptr(codes), _ptr(scales))
+    if mean is None and not fmt:
+        lib().oracle_quant_v(p, n, h, d, st, sh, _ptr(codes), _ptr(scales))
+    else:
+        mu = None if mean is None else np.ascontiguousarray(mean, dtype=np.float32)
+        lib().oracle_quant_v_fmt(p, n, h, d, st, sh, None if mu is None else _ptr(mu), fmt, _ptr(codes),
+                                 _ptr(scales))
     return codes, scales
 
 
 class Quantized:
-    """Steps 1-4 of the oracle for one set of inputs."""
+    """Steps 1-4 of the oracle for one set of inputs.  v_format "e4m3" (the method's FP8 V) or
+    "int8" (the INT8 P.V variant); smooth_v: take the channel mean out of V first."""
 
-    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_block: int = 128):
+    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_block: int = 128,
+                 v_format: str = "e4m3", smooth_v: bool = False):
         self.n, self.h, self.d = q.shape
         self.q_block = q_block
+        self.v_format = v_format
         self.k_mean = k_mean(k)
         self.q_codes, self.q_scales = quant_q(q, q_block)
         self.k_codes, self.k_scales = quant_k(k, self.k_mean)
-        self.v_codes, self.v_scales = quant_v(v)
+        self.v_mean = channel_mean(v) if smooth_v else None
+        self.v_codes, self.v_scales = quant_v(v, v_format, self.v_mean)
 
 
 def qk_int32(qz: Quantized, head: int, i0: int, j0: int, rows: int, cols: int) -> np.ndarray:
@@ -177,10 +197,13 @@ def attn_sq(qz: Quantized, sm_scale: float, rows, tile: int = 128, score_f32=Non
         score_f32 = tile > 0
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     out = np.zeros((len(rows), qz.h, qz.d), np.float64)
-    lib().oracle_attn_sq_blk(_ptr(qz.q_codes), _ptr(qz.q_scales), int(getattr(qz, "q_block", 128)),
-                             _ptr(qz.k_codes), _ptr(qz.k_scales), _ptr(qz.v_codes), _ptr(qz.v_scales),
-                             qz.n, qz.h, qz.d, float(sm_scale), _ptr(rows), len(rows), int(tile),
-                             int(bool(score_f32)), _ptr(out))
+    v_mean = getattr(qz, "v_mean", None)
+    mu = None if v_mean is None else np.ascontiguousarray(v_mean, dtype=np.float32)
+    lib().oracle_attn_sq_v(_ptr(qz.q_codes), _ptr(qz.q_scales), int(getattr(qz, "q_block", 128)),
+                           _ptr(qz.k_codes), _ptr(qz.k_scales), _ptr(qz.v_codes), _ptr(qz.v_scales),
+                           None if mu is None else _ptr(mu), V_FORMATS[getattr(qz, "v_format", "e4m3")],
+                           qz.n, qz.h, qz.d, float(sm_scale), _ptr(rows), len(rows), int(tile),
+                           int(bool(score_f32)), _ptr(out))
     return out
 
 

@@ -59,34 +59,52 @@ def quant_int8_blocks(x: np.ndarray, block: int):
     return codes.reshape(h, np_, d), scale
 
 
-def quant_v(v: np.ndarray):
-    """v: fp32 [H, N, D] -> E4M3 codes [H, D, N_pad] and scales [H, D] (amax/448)."""
+def quant_v(v: np.ndarray, v_format: str = "e4m3", mean=None):
+    """v: fp32 [H, N, D] -> codes [H, D, N_pad] and scales [H, D]: E4M3 bytes with scale amax/448,
+    or int8 codes with scale amax/127 (round half to even, clamped to +-127).  mean: None or the
+    [H, D] fp32 mean subtracted (in fp32) before the maxima and the codes."""
     h, n, d = v.shape
     np_ = (n + 127) // 128 * 128
-    amax = np.abs(v).max(axis=1).astype(np.float32)
-    scale = (amax / np.float32(448.0)).astype(np.float32)
+    x = v.astype(np.float32)
+    if mean is not None:
+        x = (x - np.asarray(mean, np.float32)[:, None, :]).astype(np.float32)
+    amax = np.abs(x).max(axis=1).astype(np.float32)
+    top = np.float32(127.0 if v_format == "int8" else 448.0)
+    scale = (amax / top).astype(np.float32)
     safe = np.where(scale == 0, np.float32(1), scale)
-    y = (v / safe[:, None, :]).astype(np.float32)
-    codes = np.where(scale[:, None, :] == 0, 0, e4m3_encode(y))
-    out = np.zeros((h, d, np_), np.uint8)
+    y = (x / safe[:, None, :]).astype(np.float32)
+    if v_format == "int8":
+        codes = np.where(scale[:, None, :] == 0, 0, np.clip(np.rint(y), -127, 127)).astype(np.int8)
+        out = np.zeros((h, d, np_), np.int8)
+    else:
+        codes = np.where(scale[:, None, :] == 0, 0, e4m3_encode(y)).astype(np.uint8)
+        out = np.zeros((h, d, np_), np.uint8)
     out[:, :, :n] = np.transpose(codes, (0, 2, 1))
     return out, scale
 
 
-def attn_sq_global(qc, qs, kc, ks, vc, vs, n, sm_scale, q_block=128):
+def attn_sq_global(qc, qs, kc, ks, vc, vs, n, sm_scale, q_block=128, v_format="e4m3", v_mean=None):
     """Global-max same-quantisation attention, all rows: [N, H, D] fp64.  qs holds one scale
-    per (head, q_block consecutive rows)."""
+    per (head, q_block consecutive rows).  v_format "int8": P = rint(127 p), V values are the
+    integer codes; v_mean (or None) is added to the result."""
     h, np_, d = qc.shape
     out = np.zeros((n, h, d))
     qrow_scale = np.repeat(qs, q_block, axis=1)[:, :n]
     krow_scale = np.repeat(ks, 64, axis=1)[:, :n]
+    top = 127.0 if v_format == "int8" else 448.0
     for hh in range(h):
         S = qc[hh, :n].astype(np.int64) @ kc[hh, :n].astype(np.int64).T
         s = S * qrow_scale[hh][:, None].astype(np.float64) * krow_scale[hh][None, :].astype(np.float64) * sm_scale
         p = np.exp(s - s.max(axis=1, keepdims=True))
-        p8 = e4m3_decode(e4m3_encode(448.0 * p))
-        vdec = e4m3_decode(vc[hh, :, :n]).T           # [N, D]
-        out[:, hh, :] = (p8 @ vdec) * vs[hh][None, :].astype(np.float64) / (448.0 * p.sum(axis=1, keepdims=True))
+        if v_format == "int8":
+            p8 = np.rint(top * p)
+            vdec = vc[hh, :, :n].astype(np.float64).T
+        else:
+            p8 = e4m3_decode(e4m3_encode(top * p))
+            vdec = e4m3_decode(vc[hh, :, :n]).T           # [N, D]
+        out[:, hh, :] = (p8 @ vdec) * vs[hh][None, :].astype(np.float64) / (top * p.sum(axis=1, keepdims=True))
+        if v_mean is not None:
+            out[:, hh, :] += np.asarray(v_mean, np.float64)[hh][None, :]
     return out
 
 

@@ -15,8 +15,10 @@
  *                   recorded warp_q of 32 rows, down to per row)           oracle_quant_q_blk
  *   3. K quantise   K~ = K - mu, per (head, 64-row block) INT8             oracle_quant_k
  *   4. V quantise   per (head, channel) FP8 E4M3, fp32 scale               oracle_quant_v
+ *                   (or INT8, and optionally of V - mean(V))                oracle_quant_v_fmt
  *   5. S = Qc Kc^T  exact integer dot products                             oracle_qk_int32
  *   6-8. softmax(S * s_q * s_k * sm_scale) with P held in E4M3, times V    oracle_attn_sq(_blk)
+ *        (P in INT8 when V is INT8; + mean(V) when V was smoothed)         oracle_attn_sq_v
  *   9. exact fp64 softmax attention of the bf16 inputs                     oracle_attn_exact
  *   0. (upstream of 1-4) in-place RMSNorm + rotary embedding of Q / K       oracle_rmsnorm_rope
  *
@@ -42,7 +44,7 @@
 enum { MUT_NONE = 0, MUT_NO_SMOOTH = 1, MUT_RESCALE_SIGN = 2, MUT_SCALE_255 = 3,
        MUT_KEY_INDEX = 4, MUT_V_SCALE_CHANNEL = 5, MUT_DROP_LAST_KEY = 6,
        MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8, MUT_Q_BLOCK_INDEX = 9, MUT_ROPE_SIGN = 10,
-       MUT_RMS_SUM = 11 };
+       MUT_RMS_SUM = 11, MUT_V_MEAN_SIGN = 12, MUT_P_I8_255 = 13 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
 
@@ -218,6 +220,48 @@ void oracle_quant_v(const uint16_t* v, int64_t n, int64_t h, int64_t d, int64_t 
     }
 }
 
+/* 4'. The V path's two options.
+ *  mu != NULL: V smoothing.  x = fl32(v - mu[h][c]) (one fp32 subtraction, mu the channel mean
+ *    of V over the tokens, taken as oracle_k_mean takes the mean of K); softmax rows sum to 1,
+ *    so the attention adds mu back to its output (oracle_attn_sq_v).  mu == NULL: x = v.
+ *  fmt 0: E4M3 as oracle_quant_v: scale = fl32(amax / 448), code = E4M3(fl32(x / scale)).
+ *  fmt 1: INT8: scale = fl32(amax / 127), code = clamp(rint(fl32(x / scale)), -127, 127),
+ *    stored as the int8 byte (two's complement) -- the INT8 P.V variant timed on the
+ *    sampling-component page (v_int8_quantize), quantised like Q and K.
+ * amax over the N tokens of |x|; an all-zero channel has scale 0 and codes 0.
+ * codes [H][D][N_pad] (keys contiguous), scales [H][D]. */
+void oracle_quant_v_fmt(const uint16_t* v, int64_t n, int64_t h, int64_t d, int64_t st, int64_t sh,
+                        const float* mu, int64_t fmt, uint8_t* codes, float* scales) {
+  int64_t np = pad128(n);
+  memset(codes, 0, (size_t)(h * d * np));
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t hh = 0; hh < h; ++hh)
+    for (int64_t c = 0; c < d; ++c) {
+      float m = mu ? mu[hh * d + c] : 0.0f;
+      float amax = 0.0f;
+      for (int64_t t = 0; t < n; ++t) {
+        float a = fabsf(bf16_to_f32(v[t * st + hh * sh + c]) - m);
+        if (a > amax) amax = a;
+      }
+      float scale = fmt ? amax / 127.0f : amax / 448.0f;
+      scales[hh * d + c] = scale;
+      if (scale == 0.0f) continue;
+      for (int64_t t = 0; t < n; ++t) {
+        float y = (bf16_to_f32(v[t * st + hh * sh + c]) - m) / scale;
+        uint8_t code;
+        if (fmt) {
+          float r = rintf(y);
+          if (r > 127.0f) r = 127.0f;
+          if (r < -127.0f) r = -127.0f;
+          code = (uint8_t)(int8_t)r;
+        } else {
+          code = oracle_e4m3_encode((double)y);
+        }
+        codes[(hh * d + c) * np + t] = code;
+      }
+    }
+}
+
 /* 5. S[i][j] = sum_c qc[h][i0+i][c] * kc[h][j0+j][c], exact in int64, stored as int32
  * (|S| <= 128 * 127^2 < 2^31). */
 void oracle_qk_int32(const int8_t* qc, const int8_t* kc, int64_t n, int64_t h, int64_t d,
@@ -252,15 +296,35 @@ void oracle_qk_int32(const int8_t* qc, const int8_t* kc, int64_t n, int64_t h, i
  *   precision: in base 2, x = fma_f32(S, c_b, fl32(log2(448) - m)) with
  *   c_b = fl32(fl32(s_q * fl32(sm_scale * log2 e)) * s_k[b]), m the fp32 running max of
  *   fl32(c_b * max S over each 64-key half), and 448 p = RN_f32(2^x); sums stay in fp64.
+ * The V options of oracle_quant_v_fmt:
+ *   vfmt 1 (INT8 V): P is INT8 too, with the static scale 127 that p <= 1 allows:
+ *     P8_ij = rint(127 p_ij) in [0, 127] (ties to even), l_i = sum_j 127 p_ij, V values are the
+ *     integer codes; in the score_f32 schedule x uses log2(127) and P8 = rint(RN_f32(2^x)).
+ *   vmu != NULL (V smoothed): O_ic += vmu[h][c] after the division by l (each softmax row
+ *     sums to 1, so the mean taken out of V before quantisation comes back whole).
  * out[r][h][c] (fp64).
  * ---------------------------------------------------------------------------------- */
-void oracle_attn_sq_blk(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
-                        const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
-                        double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
-                        int64_t score_f32, double* out) {
+/* Value of one V code: the E4M3 number, or the INT8 integer. */
+static double v_value(uint8_t code, int64_t vfmt) {
+  return vfmt ? (double)(int8_t)code : oracle_e4m3_decode(code);
+}
+
+/* Value of P's code for pp = 448 p (E4M3) or 127 p (INT8, round half to even). */
+static double p_code(double pp, int64_t vfmt) {
+  if (!vfmt) return oracle_e4m3_decode(oracle_e4m3_encode(pp));
+  return rint(g_mutation == MUT_P_I8_255 ? pp * (255.0 / 127.0) : pp);
+}
+
+void oracle_attn_sq_v(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
+                      const uint8_t* vc, const float* vs, const float* vmu, int64_t vfmt, int64_t n,
+                      int64_t h, int64_t d, double sm_scale, const int64_t* rows, int64_t nrows,
+                      int64_t tile, int64_t score_f32, double* out) {
   int64_t np = pad128(n), nbq = np / qb, nbk = np / 64;
   int64_t nkeys = (g_mutation == MUT_DROP_LAST_KEY) ? n - 1 : n;
-  const float kLog2E = 1.4426950408889634f, kLog2_448 = 8.807354922057604f;
+  const float kLog2E = 1.4426950408889634f;
+  /* log2 of P's static scale: log2(448) for E4M3 P, log2(127) for INT8 P */
+  const float kLog2P = vfmt ? 6.988684686772166f : 8.807354922057604f;
+  const double pscale = vfmt ? 127.0 : 448.0;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t rh = 0; rh < nrows * h; ++rh) {
     int64_t r = rh / h, hh = rh % h, i = rows[r];
@@ -306,16 +370,15 @@ void oracle_attn_sq_blk(const int8_t* qc, const float* qs, int64_t qb, const int
           }
           mf = mt;
         }
-        const float bias = kLog2_448 - mf;
+        const float bias = kLog2P - mf;
         for (int64_t j = j0; j < j1; ++j) {
           float cb = cq * ks[hh * nbk + j / 64];
           float x = fmaf((float)S[j], cb, bias);
-          float pp = (float)exp2((double)x);             /* 448 p, rounded to fp32 */
+          float pp = (float)exp2((double)x);             /* 448 p or 127 p, rounded to fp32 */
           l += (double)pp;
-          double p8 = oracle_e4m3_decode(oracle_e4m3_encode((double)pp));
+          double p8 = p_code((double)pp, vfmt);
           if (p8 == 0.0) continue;
-          for (int64_t c = 0; c < d; ++c)
-            o[c] += p8 * oracle_e4m3_decode(vc[(hh * d + c) * np + j]);
+          for (int64_t c = 0; c < d; ++c) o[c] += p8 * v_value(vc[(hh * d + c) * np + j], vfmt);
         }
         continue;
       }
@@ -333,19 +396,29 @@ void oracle_attn_sq_blk(const int8_t* qc, const float* qs, int64_t qb, const int
       }
       for (int64_t j = j0; j < j1; ++j) {
         double p = exp(s[j] - m);
-        l += 448.0 * p;
-        double p8 = oracle_e4m3_decode(oracle_e4m3_encode(448.0 * p));
+        l += pscale * p;
+        double p8 = p_code(pscale * p, vfmt);
         if (p8 == 0.0) continue;
-        for (int64_t c = 0; c < d; ++c)
-          o[c] += p8 * oracle_e4m3_decode(vc[(hh * d + c) * np + j]);
+        for (int64_t c = 0; c < d; ++c) o[c] += p8 * v_value(vc[(hh * d + c) * np + j], vfmt);
       }
     }
-    for (int64_t c = 0; c < d; ++c)
-      out[(r * h + hh) * d + c] = o[c] * (double)vs[hh * d + c] / l;
+    for (int64_t c = 0; c < d; ++c) {
+      double mean = 0.0;
+      if (vmu) mean = (g_mutation == MUT_V_MEAN_SIGN) ? -(double)vmu[hh * d + c] : (double)vmu[hh * d + c];
+      out[(r * h + hh) * d + c] = o[c] * (double)vs[hh * d + c] / l + mean;
+    }
     free(o);
     free(s);
     free(S);
   }
+}
+
+/* E4M3 V as in oracle_quant_v (Q and K scales per qb-row / 64-row block as above). */
+void oracle_attn_sq_blk(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
+                        const uint8_t* vc, const float* vs, int64_t n, int64_t h, int64_t d,
+                        double sm_scale, const int64_t* rows, int64_t nrows, int64_t tile,
+                        int64_t score_f32, double* out) {
+  oracle_attn_sq_v(qc, qs, qb, kc, ks, vc, vs, NULL, 0, n, h, d, sm_scale, rows, nrows, tile, score_f32, out);
 }
 
 /* The method's default: Q scales per 128-row block. */

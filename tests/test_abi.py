@@ -64,8 +64,11 @@ def test_argument_validation_never_launches(L):
     qz = _qz()
     call = lambda *a: L.sage_smooth_quant_qk(*a)
     by = ctypes.byref
-    # null view data
+    # null view data; an empty input
     assert call(by(_view(ptr=0)), by(k), by(qz), 4096, 1 << 30, None) == 1
+    assert call(by(_view(n=0)), by(_view(n=0)), by(qz), 4096, 1 << 30, None) == 1
+    assert L.sage_attn_fwd(by(_view(n=0)), by(_view(n=0)), by(_view(n=0)), 0.1, 4096, 256, 128, 4096, 1 << 34,
+                           None) == 1
     # unsupported head dim
     assert call(by(_view(d=96)), by(_view(d=96)), by(qz), 4096, 1 << 30, None) == 3
     # misaligned pointer / stride

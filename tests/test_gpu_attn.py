@@ -289,3 +289,32 @@ def test_largest_token_count():
     got = out[sel].float().cpu().numpy().astype(np.float64)
     ref = oracle.attn_sq(oz, sm, sel, tile=128)
     assert rel_l2(got, ref) <= SQ_REL and np.abs(got - ref).max() <= SQ_ABS
+
+
+def test_degenerate_scales_give_uniform_attention():
+    """Constant K: smoothing makes every K~ zero, so every K scale is 0, every score 0, and
+    attention uniform: O = the mean of the dequantised V.  Rows 128-255 of Q all zero: their
+    scale is 0 and they attend uniformly too, whatever K is.  Both against the oracle."""
+    n, h, d = 300, 2, 128
+    g = torch.Generator("cpu").manual_seed(41)
+    q = torch.randn(n, h, d, generator=g)
+    q[128:256] = 0.0
+    k = torch.randn(1, h, d, generator=g).expand(n, h, d).contiguous()
+    v = torch.randn(n, h, d, generator=g)
+    qkv = torch.cat([t.reshape(n, h * d) for t in (q, k, v)], dim=1).to(torch.bfloat16)
+    hd = h * d
+    cq, ck, cv = (qkv[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    oz = oracle.Quantized(cq, ck, cv)
+    assert (oz.k_scales == 0).all() and (oz.q_scales[:, 1] == 0).all()
+    st = qkv.cuda()
+    q_, k_, v_ = (st[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    sm = 1.0 / math.sqrt(d)
+    status = sage.status_block()
+    out = sage.sage_attn_fwd_quantized(_gpu_qz({"q": q_, "k": k_, "v": v_}), sm, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = oracle.attn_sq(oz, sm, list(range(n)), tile=128)
+    assert rel_l2(got, ref) <= SQ_REL and np.abs(got - ref).max() <= SQ_ABS
+    vdeq = oracle.brute.e4m3_decode(oz.v_codes[:, :, :n]) * oz.v_scales[:, :, None]     # [H, D, N]
+    mean_v = vdeq.mean(axis=2)                                                           # [H, D]
+    assert np.abs(got - mean_v[None]).max() <= 1e-2 * np.abs(mean_v).max() + 4e-3

@@ -458,6 +458,163 @@ def test_rmsnorm_rope_in_place_on_strided_views(oracle_lib):
     assert torch.equal(inp.q.contiguous().view(torch.int16), ref.view(torch.int16))
 
 
+# ---------------------------------------------------------------- V options: INT8 P.V, V smoothing
+
+def _grid_inputs(n=256, h=2, d=64, seed=11):
+    """Q, K and V whose V values lie on a 2^-4 grid in (-2, 2): with n a power of two, the channel
+    mean of V, of V + c (c in {2, 4, 8}) and every difference v - mean are exact in fp32."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(n, h, d, generator=g).to(torch.bfloat16)
+    k = (torch.randn(n, h, d, generator=g) + 2.0 * torch.randn(1, h, d, generator=g)).to(torch.bfloat16)
+    v = (torch.randint(-31, 32, (n, h, d), generator=g).float() / 16.0).to(torch.bfloat16)
+    return q, k, v
+
+
+def _shift_error(v_format: str) -> float:
+    """|O(V + c) - O(V) - c| for smoothed V, c a per-channel constant: smoothing removes c before
+    quantisation (same codes, same scales) and the attention adds the mean, c included, back."""
+    q, k, v = _grid_inputs()
+    c = torch.tensor([2.0, 4.0, 8.0])[torch.arange(v.shape[2]) % 3]
+    v2 = (v.float() + c).to(torch.bfloat16)
+    assert torch.equal(v2.float() - c, v.float())           # the shift is exact in bf16
+    a = oracle.Quantized(q, k, v, v_format=v_format, smooth_v=True)
+    b = oracle.Quantized(q, k, v2, v_format=v_format, smooth_v=True)
+    assert (a.v_codes == b.v_codes).all() and (a.v_scales == b.v_scales).all()
+    rows = list(range(0, 256, 5))
+    oa = oracle.attn_sq(a, 0.125, rows, tile=128)
+    ob = oracle.attn_sq(b, 0.125, rows, tile=128)
+    return float(np.abs(ob - oa - c.double().numpy()[None, None, :]).max())
+
+
+def _int8_two_level_error() -> float:
+    """Closed form of the INT8 P.V variant: 64 keys score +s0 and 64 score -s0 for every query, so
+    p is 1 or exp(-2 s0) and P's codes are 127 and rint(127 exp(-2 s0)) (= 47 for 2 s0 = 1); with V
+    = +1 on the high keys and -1 on the low ones (codes +-127), every output is
+    (127 - 47) / (127 (1 + exp(-1))) times the dequantised 1."""
+    n, h, d = 128, 1, 64
+    q = torch.zeros(n, h, d)
+    q[:, 0, 0] = 1.0
+    k = torch.zeros(n, h, d)
+    k[:64, 0, 0] = 1.0
+    k[64:, 0, 0] = -1.0
+    v = torch.zeros(n, h, d)
+    v[:64] = 1.0
+    v[64:] = -1.0
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    qz = oracle.Quantized(q, k, v, v_format="int8")
+    s_q, s_k, s_v = float(qz.q_scales[0, 0]), float(qz.k_scales[0, 0]), float(qz.v_scales[0, 0])
+    assert (qz.k_codes[0, :64, 0] == 127).all() and (qz.v_codes[0, :, :64] == 127).all()
+    sm = 0.5 / (127 * 127 * s_q * s_k)                      # s0 = 0.5 up to the fp32 scales
+    s0 = 127 * 127 * s_q * s_k * sm
+    low = math.exp(-2 * s0)
+    code_low = float(np.rint(127 * low))
+    assert code_low == 47.0
+    want = (127 - code_low) * 127 * s_v / (127 * (1 + low))
+    got = oracle.attn_sq(qz, sm, list(range(0, n, 9)), tile=0)
+    err = float(np.abs(got - want).max())
+    tiled = oracle.attn_sq(qz, sm, list(range(0, n, 9)), tile=128, score_f32=False)
+    return max(err, float(np.abs(tiled - want).max()))
+
+
+@pytest.mark.parametrize("smooth", [False, True])
+def test_v_int8_quant_matches_brute(oracle_lib, smooth):
+    inp = small_inputs(n=333, h=2, d=64, layout="nhd")
+    mu = oracle.channel_mean(inp.v) if smooth else None
+    codes, scales = oracle.quant_v(inp.v, "int8", mu)
+    vf = np.ascontiguousarray(inp.v.float().numpy().transpose(1, 0, 2))
+    bc, bs = brute.quant_v(vf, "int8", mu)
+    assert (codes == bc).all() and (scales == bs).all()
+    x = vf - (mu[:, None, :] if smooth else 0)
+    deq = codes[:, :, :333].astype(np.float64) * scales[:, :, None]
+    # half a step, plus the fp32 rounding of the quotient x / scale (|x / scale| <= 127)
+    assert (np.abs(deq - x.transpose(0, 2, 1)) <= (0.5 + 2.0 ** -16) * scales[:, :, None]).all()
+    assert (np.abs(codes[:, :, :333]).max(axis=2) == 127).all() and (codes[:, :, 333:] == 0).all()
+
+
+def test_v_e4m3_smoothed_quant_matches_brute(oracle_lib):
+    inp = small_inputs(n=333, h=2, d=64, layout="qkv")
+    mu = oracle.channel_mean(inp.v)
+    codes, scales = oracle.quant_v(inp.v, "e4m3", mu)
+    bc, bs = brute.quant_v(np.ascontiguousarray(inp.v.float().numpy().transpose(1, 0, 2)), "e4m3", mu)
+    assert (codes == bc).all() and (scales == bs).all()
+    # the unsmoothed call of the same function is the method's default V quantisation
+    c0, s0 = oracle.quant_v(inp.v, "e4m3", None)
+    c1 = np.zeros_like(c0)
+    s1 = np.zeros_like(s0)
+    p, st, sh = inp.v.data_ptr(), inp.v.stride(0), inp.v.stride(1)
+    oracle.lib().oracle_quant_v_fmt(p, 333, 2, 64, st, sh, None, 0, c1.ctypes.data, s1.ctypes.data)
+    assert (c0 == c1).all() and (s0 == s1).all()
+
+
+@pytest.mark.parametrize("v_format", ["e4m3", "int8"])
+def test_v_smoothing_shift_invariance(oracle_lib, v_format):
+    assert _shift_error(v_format) < 1e-12
+
+
+@pytest.mark.parametrize("v_format", ["e4m3", "int8"])
+def test_constant_v_smoothed_gives_the_constant(oracle_lib, v_format):
+    """V constant per channel: V - mean = 0 exactly, so scales and codes are 0 and the output is
+    the constant, whatever the scores."""
+    inp = small_inputs(n=300, h=2, d=64, layout="nhd")
+    v = inp.v[5:6].expand(300, 2, 64).contiguous()
+    qz = oracle.Quantized(inp.q, inp.k, v, v_format=v_format, smooth_v=True)
+    assert (qz.v_scales == 0).all() and (qz.v_codes == 0).all()
+    o = oracle.attn_sq(qz, 0.125, [0, 150, 299], tile=128)
+    assert (o == v[0].double().numpy()[None]).all()
+
+
+@pytest.mark.parametrize("smooth", [False, True])
+def test_int8_pv_attn_matches_brute_global(oracle_lib, smooth):
+    inp = small_inputs(n=300, h=2, d=64, layout="qkv")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v, v_format="int8", smooth_v=smooth)
+    rows = list(range(300))
+    a = oracle.attn_sq(qz, 0.125, rows, tile=0)
+    b = brute.attn_sq_global(qz.q_codes, qz.q_scales, qz.k_codes, qz.k_scales, qz.v_codes, qz.v_scales,
+                             300, 0.125, v_format="int8", v_mean=qz.v_mean)
+    assert np.abs(a - b).max() < 1e-12
+
+
+def test_int8_pv_uniform_attention(oracle_lib):
+    """Constant K: K~ = 0, every score 0, p = 1, every P code 127 and l = 127 N: the output is the
+    mean of the dequantised INT8 V."""
+    inp = small_inputs(n=300, h=2, d=64, layout="nhd")
+    k = inp.k[3:4].expand(300, 2, 64).contiguous()
+    qz = oracle.Quantized(inp.q, k, inp.v, v_format="int8")
+    o = oracle.attn_sq(qz, 0.125, [0, 150, 299], tile=128)
+    vdeq = qz.v_codes[:, :, :300].astype(np.float64) * qz.v_scales[:, :, None]
+    assert np.abs(o - vdeq.mean(axis=2)[None]).max() < 1e-12
+
+
+def test_int8_pv_two_level_closed_form(oracle_lib):
+    assert _int8_two_level_error() < 1e-12
+
+
+@pytest.mark.parametrize("v_format", ["e4m3", "int8"])
+def test_tiled_schedule_close_to_global(oracle_lib, v_format):
+    """The online schedule (P coded against the running max, fp32 scores) against the one-pass
+    definition: the difference is P's coding noise only."""
+    inp = small_inputs(n=600, h=2, d=64, layout="qkv")
+    qz = oracle.Quantized(inp.q, inp.k, inp.v, v_format=v_format, smooth_v=True)
+    rows = list(range(0, 600, 7))
+    assert rel_l2(oracle.attn_sq(qz, 0.125, rows, tile=128), oracle.attn_sq(qz, 0.125, rows, tile=0)) < 2e-2
+
+
+def test_v_smoothing_lowers_error_on_offset_v(oracle_lib):
+    """A large per-channel offset in V costs E4M3 precision on the part that varies; taking the
+    mean out first brings the quantised output closer to exact attention."""
+    inp = small_inputs(n=400, h=2, d=64, layout="nhd")
+    g = torch.Generator().manual_seed(3)
+    v = (inp.v.float() + 20.0 * torch.randn(1, 2, 64, generator=g)).to(torch.bfloat16)
+    rows = list(range(0, 400, 11))
+    exact = oracle.attn_exact(inp.q, inp.k, v, 0.125, rows)
+    plain = oracle.attn_sq(oracle.Quantized(inp.q, inp.k, v), 0.125, rows, tile=128)
+    smooth = oracle.attn_sq(oracle.Quantized(inp.q, inp.k, v, smooth_v=True), 0.125, rows, tile=128)
+    centred = exact - v.double().mean(dim=0).numpy()[None]
+    e_plain = np.linalg.norm(plain - exact) / np.linalg.norm(centred)
+    e_smooth = np.linalg.norm(smooth - exact) / np.linalg.norm(centred)
+    assert e_smooth < 0.5 * e_plain, (e_smooth, e_plain)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _pins_pass(inp) -> bool:
@@ -494,6 +651,18 @@ def _pins_pass(inp) -> bool:
     if not np.abs(oracle.attn_sq(q32, 0.125, rows, tile=0) - g32).max() < 1e-12:
         return False
     if not _rr_closed_forms_hold():
+        return False
+    # the V options: INT8 P.V against the brute-force definition and its closed form, and the
+    # shift invariance of smoothed V
+    q8 = oracle.Quantized(inp.q, inp.k, inp.v, v_format="int8", smooth_v=True)
+    bv8, bvs8 = brute.quant_v(np.ascontiguousarray(inp.v.float().numpy().transpose(1, 0, 2)), "int8", q8.v_mean)
+    if not ((bv8 == q8.v_codes).all() and (bvs8 == q8.v_scales).all()):
+        return False
+    g8 = brute.attn_sq_global(q8.q_codes, q8.q_scales, q8.k_codes, q8.k_scales, q8.v_codes, q8.v_scales,
+                              n, 0.125, v_format="int8", v_mean=q8.v_mean)
+    if not np.abs(oracle.attn_sq(q8, 0.125, rows, tile=0) - g8).max() < 1e-12:
+        return False
+    if not (_int8_two_level_error() < 1e-12 and _shift_error("e4m3") < 1e-12):
         return False
     e = oracle.attn_exact(inp.q, inp.k, inp.v, 0.125, rows)
     b = brute.attn_exact(inp.q.float().numpy(), inp.k.float().numpy(), inp.v.float().numpy(), 0.125)
