@@ -333,6 +333,39 @@ def run_gpu(args):
                         "gbs": round(t_bytes / (t_ms * 1e-3) / 1e9, 1), "calls": 20}
         del buf
 
+    # ---- the V options of the path at the same size and inputs, outside the timed region: the
+    # INT8 P.V variant (INT8 V, P = rint(127 p), fp16-code MMAs) and V smoothing (the channel
+    # mean taken out of V, added back in the epilogue).  3 warm-up steps, then 10 steps with
+    # CUDA events around the quantisation (Q, K and V) and around the attention launch.
+    variants = None
+    if not args.no_variants:
+        variants = {}
+        for vname, fmt, smooth in (("int8_pv", "int8", False), ("e4m3_smooth_v", "e4m3", True),
+                                   ("int8_pv_smooth_v", "int8", True)):
+            vz = sage.Quantized(n, h, d, dev, v_format=fmt, smooth_v=smooth)
+            vev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(10)]
+            for i in range(13):
+                e_ = vev[i - 3] if i >= 3 else None
+                if e_ is not None:
+                    e_[0].record(stream)
+                sage.sage_smooth_quant_qk(q, k, vz, scratch, stream)
+                sage.sage_quant_v(v, vz, scratch, stream)
+                if e_ is not None:
+                    e_[1].record(stream)
+                sage.sage_attn_fwd_quantized(vz, sm_scale, out, status, stream)
+                if e_ is not None:
+                    e_[2].record(stream)
+            torch.cuda.synchronize()
+            code, where = sage.sage_check_device_status(status, stream)
+            if code != 0:
+                raise RuntimeError(f"device status {code} at {where} ({vname})")
+            v_attn = statistics.mean(e_[1].elapsed_time(e_[2]) for e_ in vev)
+            v_quant = statistics.mean(e_[0].elapsed_time(e_[1]) for e_ in vev)
+            variants[vname] = {"quantise_ms": round(v_quant, 4), "attention_ms": round(v_attn, 3),
+                               "attention_tflops": round(flops / (v_attn * 1e-3) / 1e12, 1),
+                               "step_ms": round(v_quant + v_attn, 3)}
+            del vz
+
     bf16_burst, bf16_sus, hbm, peak_src = _peaks()
     if qk_transform is not None:
         qk_transform["hbm_frac"] = round(qk_transform["gbs"] / hbm, 4)
@@ -347,6 +380,10 @@ def run_gpu(args):
     p16 = bf16_burst if full_clock else bf16_sus
     p8 = 2 * p16
     composite = 1.0 / (0.5 / p16 + 0.5 / p8)
+    for vname, vv_ in (variants or {}).items():
+        # INT8 P.V runs both contractions on fp16 operands, so the 16-bit peak is its roofline;
+        # the E4M3 variant has the default path's composite roofline.
+        vv_["roofline_frac"] = round(vv_["attention_tflops"] / (p16 if vname.startswith("int8") else composite), 4)
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
     traffic = _traffic_per_launch()
@@ -381,6 +418,7 @@ def run_gpu(args):
                 "pipelined_runs_ms": [round(x, 3) for x in e2e_runs] if e2e_steps else []},
         "call_timing": call_timing,
         "qk_transform": qk_transform,
+        "variants": variants,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -479,6 +517,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-call-timing", action="store_true",
                     help="skip the 5 x 10 per-call timing of sage_attn_fwd")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the timing of the INT8 P.V variant and of V smoothing")
     ap.add_argument("--no-qk-transform", action="store_true",
                     help="skip the timing of the in-place RMSNorm + rotary stage")
     ap.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS with qkv layout")

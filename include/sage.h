@@ -76,7 +76,9 @@ typedef struct sage_view {
  *   k_codes  [H][N_pad][D]  as q_codes, codes of K - k_mean
  *   k_scales [H][N_pad/64]  fp32
  *   k_mean   [H][D]         fp32
- *   v_codes  [H][D][N_pad]  FP8 E4M3 bytes, keys contiguous (the K-major B operand of P.V)
+ *   v_codes  [H][D][N_pad]  keys contiguous (the K-major B operand of P.V): FP8 E4M3 bytes
+ *            (v_format 0), or INT8 codes in [-127, 127] held as fp16 (v_format 1; the buffer
+ *            then holds 2 * H * D * N_pad bytes)
  *   v_scales [H][D]         fp32
  *   q_block  rows per Q scale: 0 or 128 (the method's default, one scale per 128-row block
  *            as in the pages' call), or 64, 32, 16, 8, 4, 2, 1.  32 is the per-warp
@@ -86,6 +88,17 @@ typedef struct sage_view {
  *            thread owns one row) and lower the quantisation error of Q on inputs with
  *            outlier rows.  Any other value: SAGE_ERR_INVALID_ARG.  sage_attn_fwd always
  *            uses 128.
+ *   v_format 0: the method's FP8 path (E4M3 V, P = E4M3(448 p), kind::f8f6f4 P.V).
+ *            1: the INT8 P.V variant timed on the sampling-component page
+ *            (sol_int8_qk_pv_*, v_int8_quantize): V as INT8 codes with scale amax / 127 and
+ *            P = rint(127 p) in [0, 127], both held as fp16 and multiplied with the fp16 MMA;
+ *            every integer product sum of one 16-key step is exact in the fp32 accumulator.
+ *            Any other value: SAGE_ERR_INVALID_ARG.  sage_attn_fwd always uses 0.
+ *   v_mean   NULL: V is quantised as it is.  Otherwise [H][D] fp32, written by sage_quant_v:
+ *            V smoothing -- the channel mean of V (summed in the order of the K mean) is
+ *            taken out of V before its scales and codes are formed, and the attention adds it
+ *            back to every output row (softmax rows sum to 1).  It lowers the quantisation
+ *            error of V with a large per-channel offset.  sage_attn_fwd leaves it NULL.
  * All of these pointers must be 16-byte aligned. */
 typedef struct sage_quantized {
   uint16_t* q_codes;
@@ -96,6 +109,8 @@ typedef struct sage_quantized {
   uint8_t* v_codes;
   float* v_scales;
   int64_t q_block;
+  int64_t v_format;
+  float* v_mean;
 } sage_quantized;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -146,10 +161,16 @@ sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const s
 sage_status sage_smooth_quant_qk_noalloc(const sage_view* q, const sage_view* k, const sage_quantized* qz,
                                          void* stream);
 
-/* FP8 E4M3 quantisation of V (the pages' v_quantize stage): per (h, c) scale =
- * fl32(max_t |v| / 448), code = E4M3 round-to-nearest-even, saturating, of fl32(v / scale);
- * an all-zero channel has scale 0 and codes 0.  Writes qz->v_codes (transposed to
- * [H][D][N_pad]) and qz->v_scales.  ws as for sage_smooth_quant_qk. */
+/* Quantisation of V (the pages' v_quantize stage), per (h, c) over the N tokens, of
+ * x = v (qz->v_mean NULL) or x = fl32(v - mean[h][c]) (V smoothing: qz->v_mean receives the
+ * mean first, computed exactly as k_mean is):
+ *   v_format 0: scale = fl32(max_t |x| / 448), code = E4M3 round-to-nearest-even, saturating,
+ *               of fl32(x / scale);
+ *   v_format 1: scale = fl32(max_t |x| / 127), code = clamp(rint(fl32(x / scale)), -127, 127)
+ *               held as fp16;
+ * an all-zero channel has scale 0 and codes 0; IEEE division.  Writes qz->v_codes (transposed
+ * to [H][D][N_pad]), qz->v_scales and, with smoothing, qz->v_mean.  ws as for
+ * sage_smooth_quant_qk. */
 sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws, size_t ws_bytes,
                          void* stream);
 
@@ -158,6 +179,8 @@ sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws,
  *   running row max m over 128-key tiles; p = exp(s - m); P8 = E4M3(448 p);
  *   l = sum of fp32 p; O and l are multiplied by exp(m_old - m_new) whenever m rises;
  *   out[i][h][c] = bf16_rn( (sum_j P8_ij * v_codes[h][c][j]) * v_scales[h][c] / (448 l) ).
+ * With v_format 1: P8 = rint(127 p) and the division is by 127 l.  With v_mean set:
+ * + v_mean[h][c] inside the rounding.
  * out: bf16, element (t, h, c) at out[t * out_stride_token + h * out_stride_head + c];
  * 16-byte aligned, strides multiples of 8 elements; rows >= n_tokens are never written.
  * status_block: >= sage_status_block_bytes() bytes of device memory, zeroed by the caller

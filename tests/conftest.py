@@ -33,6 +33,9 @@ def gpu_case(name: str):
             base = gpu_case(name[: -len("_hndcopy")])
             inp = synth.to_hnd(base["inp"])
             qz = base["qz"]
+        elif name.endswith("_voff"):
+            inp = synth.with_v_offset(synth.make_inputs(name[: -len("_voff")]))
+            qz = oracle.Quantized(inp.q, inp.k, inp.v)
         else:
             inp = synth.make_inputs(name)
             qz = oracle.Quantized(inp.q, inp.k, inp.v)

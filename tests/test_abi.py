@@ -97,6 +97,16 @@ def test_argument_validation_never_launches(L):
         qb.q_block = bad
         assert call(by(q), by(k), by(qb), 4096, 1 << 30, None) == 1, bad
         assert L.sage_attn_fwd_quantized(256, 2, 128, by(qb), 0.1, 4096, 256, 128, 4096, None) == 1, bad
+    # V options: format 0 (E4M3) or 1 (INT8 held as fp16) only; a V mean pointer 16-byte aligned
+    for bad in (2, -1):
+        vb = _qz()
+        vb.v_format = bad
+        assert L.sage_quant_v(by(v), by(vb), 4096, 1 << 30, None) == 1, bad
+        assert L.sage_attn_fwd_quantized(256, 2, 128, by(vb), 0.1, 4096, 256, 128, 4096, None) == 1, bad
+    vb = _qz()
+    vb.v_mean = 4100
+    assert L.sage_quant_v(by(v), by(vb), 4096, 1 << 30, None) == 2
+    assert L.sage_attn_fwd_quantized(256, 2, 128, by(vb), 0.1, 4096, 256, 128, 4096, None) == 2
     # in-place RMSNorm + RoPE: null tables, misaligned weights, bad eps, mismatched views
     rr = L.sage_qk_rmsnorm_rope
     assert rr(by(q), by(k), 4096, 4096, 0, 4096, 1e-6, None) == 1

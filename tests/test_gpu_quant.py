@@ -1,5 +1,6 @@
 """GPU parity of the smoothing / quantisation kernels against the CPU oracle: the K mean,
-every INT8 Q/K code, every E4M3 V code and every scale must be bit-identical."""
+every INT8 Q/K code, every E4M3 V code and every scale must be bit-identical; so must the
+INT8 V codes of the INT8 P.V variant, the V mean and the codes of smoothed V."""
 import numpy as np
 import pytest
 import torch
@@ -80,6 +81,41 @@ def test_q_block_bit_exact(name, q_block):
     assert np.array_equal(qz.k_scales.cpu().numpy().view(np.uint32), oq.k_scales.view(np.uint32))
 
 
+V_OPTIONS = [("int8", False), ("int8", True), ("e4m3", True)]
+
+
+def _quant_v_both(case, v_format, smooth):
+    import oracle
+    inp = case["inp"]
+    n, h, d = inp.v.shape
+    mean = oracle.channel_mean(inp.v) if smooth else None
+    oc, osc = oracle.quant_v(inp.v, v_format, mean)
+    gz = sage.Quantized(n, h, d, "cuda", v_format=v_format, smooth_v=smooth)
+    sage.sage_quant_v(case["v"], gz)
+    torch.cuda.synchronize()
+    return gz, oc, osc, mean
+
+
+def _assert_v_same(gz, oc, osc, mean, n):
+    if mean is not None:
+        assert np.array_equal(gz.v_mean.cpu().numpy().view(np.uint32), mean.view(np.uint32))
+    assert np.array_equal(gz.v_scales.cpu().numpy().view(np.uint32), osc.view(np.uint32))
+    if gz.v_format == "int8":
+        got = gz.v_codes.cpu().float().numpy()
+        assert np.array_equal(got, oc.astype(np.float32))      # the integer codes (+0 and -0 alike)
+    else:
+        got = gz.v_codes.cpu().numpy()
+        assert np.array_equal(got, oc)
+    assert not got[:, :, n:].any()
+
+
+@pytest.mark.parametrize("name", ["tiny", "tails_voff", "strided64"])
+@pytest.mark.parametrize("v_format,smooth", V_OPTIONS)
+def test_v_options_bit_exact(name, v_format, smooth):
+    case = gpu_case(name)
+    _assert_v_same(*_quant_v_both(case, v_format, smooth), case["q"].shape[0])
+
+
 def test_tiny_values_take_ieee_division():
     """A row, block or channel of values so small that its scale is subnormal (no finite
     reciprocal) still quantises exactly like the oracle's IEEE division.  The scaled rows
@@ -106,3 +142,12 @@ def test_tiny_values_take_ieee_division():
     assert np.array_equal(gz.q_codes.cpu().float().numpy(), oz.q_codes.astype(np.float32))
     assert np.array_equal(gz.v_scales.cpu().numpy().view(np.uint32), oz.v_scales.view(np.uint32))
     assert np.array_equal(gz.v_codes.cpu().numpy(), oz.v_codes)
+    # the V options: the tiny channel's scale stays subnormal and takes the same IEEE route
+    for fmt, smooth in V_OPTIONS:
+        mean = oracle.channel_mean(v) if smooth else None
+        oc, osc = oracle.quant_v(v, fmt, mean)
+        assert 0 < osc[0, 5] < 2.0 ** -126, (fmt, smooth)
+        gv = sage.Quantized(256, 2, 128, "cuda", v_format=fmt, smooth_v=smooth)
+        sage.sage_quant_v(dv, gv)
+        torch.cuda.synchronize()
+        _assert_v_same(gv, oc, osc, mean, 256)

@@ -38,7 +38,10 @@ class SageView(ctypes.Structure):
 class SageQuantizedC(ctypes.Structure):
     _fields_ = [("q_codes", ctypes.c_void_p), ("q_scales", ctypes.c_void_p), ("k_codes", ctypes.c_void_p),
                 ("k_scales", ctypes.c_void_p), ("k_mean", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("v_scales", ctypes.c_void_p), ("q_block", ctypes.c_int64)]
+                ("v_scales", ctypes.c_void_p), ("q_block", ctypes.c_int64), ("v_format", ctypes.c_int64),
+                ("v_mean", ctypes.c_void_p)]
+
+V_FORMATS = {"e4m3": 0, "int8": 1}
 
 
 _lib = None
@@ -109,15 +112,22 @@ def pad128(n: int) -> int:
 class Quantized:
     """Device buffers of the quantised operands (layouts of sage_quantized in include/sage.h)."""
 
-    def __init__(self, n: int, h: int, d: int, device="cuda", q_block: int = 128):
-        """q_block: rows per Q scale (128, the method's default, or a smaller power of two)."""
+    def __init__(self, n: int, h: int, d: int, device="cuda", q_block: int = 128, v_format: str = "e4m3",
+                 smooth_v: bool = False):
+        """q_block: rows per Q scale (128, the method's default, or a smaller power of two).
+        v_format: "e4m3" (the method's FP8 V and P) or "int8" (the INT8 P.V variant; codes held
+        as fp16).  smooth_v: quantise V minus its channel mean and add the mean back."""
         np_ = pad128(n)
         if q_block not in (1, 2, 4, 8, 16, 32, 64, 128):
             raise ValueError(f"q_block must be a power of two <= 128, got {q_block}")
-        self.n, self.h, self.d, self.q_block = n, h, d, q_block
+        if v_format not in V_FORMATS:
+            raise ValueError(f"v_format must be one of {sorted(V_FORMATS)}, got {v_format!r}")
+        self.n, self.h, self.d, self.q_block, self.v_format = n, h, d, q_block, v_format
         self.q_codes = torch.empty((h, np_, d), dtype=torch.float16, device=device)
         self.k_codes = torch.empty((h, np_, d), dtype=torch.float16, device=device)
-        self.v_codes = torch.empty((h, d, np_), dtype=torch.uint8, device=device)
+        self.v_codes = torch.empty((h, d, np_), dtype=torch.float16 if v_format == "int8" else torch.uint8,
+                                   device=device)
+        self.v_mean = torch.empty((h, d), dtype=torch.float32, device=device) if smooth_v else None
         self.q_scales = torch.empty((h, np_ // q_block), dtype=torch.float32, device=device)
         self.k_scales = torch.empty((h, np_ // 64), dtype=torch.float32, device=device)
         self.k_mean = torch.empty((h, d), dtype=torch.float32, device=device)
@@ -126,7 +136,8 @@ class Quantized:
     def c(self) -> SageQuantizedC:
         return SageQuantizedC(self.q_codes.data_ptr(), self.q_scales.data_ptr(), self.k_codes.data_ptr(),
                               self.k_scales.data_ptr(), self.k_mean.data_ptr(), self.v_codes.data_ptr(),
-                              self.v_scales.data_ptr(), self.q_block)
+                              self.v_scales.data_ptr(), self.q_block, V_FORMATS[self.v_format],
+                              None if self.v_mean is None else self.v_mean.data_ptr())
 
 
 def quant_scratch(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
@@ -147,9 +158,12 @@ def workspace(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
 
 
 def sage_smooth_quant_qk(q: torch.Tensor, k: torch.Tensor, qz: Optional[Quantized] = None,
-                         scratch: Optional[torch.Tensor] = None, stream=None, q_block: int = 128) -> Quantized:
+                         scratch: Optional[torch.Tensor] = None, stream=None, q_block: int = 128,
+                         v_format: str = "e4m3", smooth_v: bool = False) -> Quantized:
+    """When qz is None a Quantized is made here; q_block, v_format and smooth_v set it up
+    (the V options take effect in sage_quant_v and the attention)."""
     n, h, d = q.shape
-    qz = qz or Quantized(n, h, d, q.device, q_block)
+    qz = qz or Quantized(n, h, d, q.device, q_block, v_format, smooth_v)
     scratch = scratch if scratch is not None else quant_scratch(n, h, d, q.device)
     vq, vk, c = make_view(q), make_view(k), qz.c()
     _check(lib().sage_smooth_quant_qk(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(c), scratch.data_ptr(),

@@ -21,6 +21,14 @@
 // P_t (E4M3, 4 keys per 32-bit column) overwrites columns [0,32) of S_t and is the A
 // operand of the P.V MMA straight from TMEM.
 //
+// The INT8 P.V variant (kPv16; the sampling-component page's sol_int8_qk_pv_* /
+// v_int8_quantize) keeps the same schedule with V as INT8 codes and P = rint(127 p), both held
+// as fp16 (integers |c| <= 127 are exact): P_t takes columns [0,64) of S_t, P.V is 8 kind::f16
+// MMAs of K = 16 per tile (each 16-key partial sum <= 16 * 127^2 is exact in fp32), and a V
+// tile is two 64-key panels, so the K/V ring holds 2 stages at D = 128.
+//
+// V smoothing (v_mean set): the epilogue adds the channel mean taken out of V.
+//
 // Online softmax with P in E4M3: P is encoded against the current running max, so p <= 1
 // and 448 p never overflows; whenever a row's max rises, O and l of that row are
 // multiplied by exp2(m_old - m_new) before the next P.V is issued (an exact rescale on
@@ -49,20 +57,31 @@ constexpr int kBM = 128;   // query rows per tile
 // granted.
 constexpr int kRegsLaunch = 168, kRegsRoles = 56, kRegsSoftmax = 224;
 static_assert(128 * kRegsRoles + 256 * kRegsSoftmax <= 384 * kRegsLaunch, "register split exceeds launch");
+// The INT8 P.V variant's producer (two V panels) and issuer (eight P.V MMAs) spill at 56; its
+// split is 72 / 208: 128 x 72 + 256 x 208 = 62464 <= 64512.
+constexpr int kRegsRolesPv16 = 72, kRegsSoftmaxPv16 = 208;
+static_assert(128 * kRegsRolesPv16 + 256 * kRegsSoftmaxPv16 <= 384 * kRegsLaunch, "register split exceeds launch");
 constexpr int kBN = 128;   // keys per tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2_448 = 8.807354922057604f;     // log2(448): P is encoded as E4M3(448 p)
+constexpr float kLog2_127 = 6.988684686772166f;     // log2(127): INT8 P = rint(127 p)
+// 2^23 + 0x6400: in [2^23, 2^24) the fp32 ulp is 1, so fl32(x + kRintMagic) = kRintMagic +
+// rint(x) for 0 <= x < 2^15 (ties to even: kRintMagic is even), and its low 16 bits are then
+// 0x6400 + rint(x), the fp16 number 1024 + rint(x) for rint(x) < 1024.
+constexpr float kRintMagic = 8414208.0f;
 
-template <int D>
+// kPv16: the INT8 P.V variant -- V codes held as fp16 (2 bytes per key), P as fp16 codes.
+template <int D, bool kPv16 = false>
 struct Cfg {
   static constexpr int kPanels = D / 64;                 // 128-byte swizzle panels per fp16 row
   static constexpr int kPanelBytes = 128 * 128;          // 128 rows x 128 B
   static constexpr int kQTileBytes = kBM * D * 2;
   static constexpr int kKTileBytes = kBN * D * 2;
-  static constexpr int kVTileBytes = D * kBN;
+  static constexpr int kVPanelBytes = D * 128;           // D channel rows x 128 B (64 fp16 keys)
+  static constexpr int kVTileBytes = D * kBN * (kPv16 ? 2 : 1);
   static constexpr int kStageBytes = kKTileBytes + kVTileBytes;
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kStages = D == 128 ? (kPv16 ? 2 : 3) : 4;
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
@@ -76,6 +95,7 @@ struct AttnParams {
   const float* q_scales;   // [H][npad >> q_shift]
   const float* k_scales;   // [H][npad/64]
   const float* v_scales;   // [H][D]
+  const float* v_mean;     // [H][D] or null: added to every output row (V smoothing)
   float sm_scale_log2;     // sm_scale * log2(e)
   uint16_t* out;           // bf16
   int64_t ost, osh;
@@ -123,22 +143,44 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
   }
 }
 
-// O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3).
-template <int D>
+// O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3), or with kPv16 8 MMAs of
+// 128 x D x 16 on fp16 codes (P: 16 keys per 8 TMEM columns; V: two 64-key panels).
+template <int D, bool kPv16>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, D);
+  if (kPv16) {
 #pragma unroll
-  for (int kk = 0; kk < kBN / 32; ++kk)
-    mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
+    for (int kk = 0; kk < kBN / 16; ++kk)
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + (kk >> 2) * Cfg<D, true>::kVPanelBytes + (kk & 3) * 32),
+                 idesc, (first && kk == 0) ? 0u : 1u);
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < kBN / 32; ++kk)
+      mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
+  }
+}
+
+// Four INT8 P codes rint(p'_k) (p' = 127 p) as two fp16x2 words, the lower key in the low half.
+__device__ __forceinline__ void p_codes_f16(const float pp[4], uint64_t magic2, uint32_t& w01, uint32_t& w23) {
+  float a0, a1, a2, a3;
+  f2_unpack(f2_add(f2_pack(pp[0], pp[1]), magic2), a0, a1);
+  f2_unpack(f2_add(f2_pack(pp[2], pp[3]), magic2), a2, a3);
+  uint32_t h01, h23;
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(h01) : "r"(__float_as_uint(a0)), "r"(__float_as_uint(a1)));
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(h23) : "r"(__float_as_uint(a2)), "r"(__float_as_uint(a3)));
+  // (1024 + c) - 1024 in fp16: exact.
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(w01) : "r"(h01), "r"(0x64006400u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(w23) : "r"(h23), "r"(0x64006400u));
 }
 
 // One 128-key tile of the online softmax for the calling thread's row (= TMEM lane):
 //   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
 //   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
-//   p = exp2(S c - m_new) into the first 32 columns of S; l = alpha l + sum p; and, if any row
-//   of the warp saw its max rise, multiplies that row's O by alpha = exp2(m_old - m_new).
+//   p = exp2(S c - m_new) into the first 32 columns of S (kPv16: P = rint(127 p) as fp16 into
+//   the first 64); l = alpha l + sum p; and, if any row of the warp saw its max rise,
+//   multiplies that row's O by alpha = exp2(m_old - m_new).
 // kTail: keys >= kvalid are excluded from the max and get p = 0.
-template <int D, bool kTail>
+template <int D, bool kTail, bool kPv16>
 __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0, float c1, int kvalid, bool first,
                                              float& m, float& l) {
   uint32_t sr[128];
@@ -165,8 +207,10 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
   const bool rise = !first && (m_new > m);
   const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
   m = m_new;
-  // p' = 448 p = exp2(S c + log2(448) - m), two keys per fp32x2 FMA.
-  const uint64_t bias2 = f2_pack(kLog2_448 - m_new, kLog2_448 - m_new);
+  // p' = 448 p = exp2(S c + log2(448) - m) (127 p with kPv16), two keys per fp32x2 FMA.
+  constexpr float kLog2P = kPv16 ? kLog2_127 : kLog2_448;
+  const uint64_t bias2 = f2_pack(kLog2P - m_new, kLog2P - m_new);
+  const uint64_t magic2 = f2_pack(kRintMagic, kRintMagic);
   // Partial sums of p': one per (32-key chunk, key pair parity), so no add waits on more than
   // eight earlier ones.
   uint64_t l2[4][2];
@@ -174,7 +218,7 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
   for (int cch = 0; cch < 4; ++cch) {
     const float cb = cch < 2 ? c0 : c1;
     const uint64_t cb2 = f2_pack(cb, cb);
-    uint32_t pw[8];
+    uint32_t pw[kPv16 ? 16 : 8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const int k = cch * 32 + w * 4;
@@ -193,9 +237,16 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
         l2[cch][0] = f2_add(l2[cch][0], f2_pack(pp[0], pp[1]));
         l2[cch][1] = f2_add(l2[cch][1], f2_pack(pp[2], pp[3]));
       }
-      pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
+      if (kPv16)
+        p_codes_f16(pp, magic2, pw[2 * w], pw[2 * w + 1]);
+      else
+        pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
     }
-    SAGE_TMEM_ST8(tS + cch * 8, pw);
+    // All of S is in registers (tmem_wait_ld above), so P may overwrite its columns.
+    if (kPv16)
+      SAGE_TMEM_ST16(tS + cch * 16, pw);
+    else
+      SAGE_TMEM_ST8(tS + cch * 8, pw);
   }
   const uint64_t la = f2_add(f2_add(l2[0][0], l2[0][1]), f2_add(l2[1][0], l2[1][1]));
   const uint64_t lb = f2_add(f2_add(l2[2][0], l2[2][1]), f2_add(l2[3][0], l2[3][1]));
@@ -227,11 +278,13 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
 // kRowQ: Q scales per 2^q_shift < 128 rows, so each softmax thread reads its own row's scale;
 // otherwise one scale per 128-row tile.  Two instantiations keep the default one's code as it
 // was: the per-row lookup alone measured 0.7 % slower there.
-template <int D, bool kRowQ>
+// kMean: V was smoothed, the epilogue adds p.v_mean (a separate instantiation keeps the
+// default epilogue free of the extra loads).
+template <int D, bool kRowQ, bool kPv16, bool kMean>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kPv16>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_skip;
   __shared__ volatile int s_abort;
@@ -281,7 +334,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
   if (warp < 4) {
-    regs_dec<kRegsRoles>();
+    regs_dec<(kPv16 ? kRegsRolesPv16 : kRegsRoles)>();
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -304,7 +357,12 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(kv_full + s, C::kStageBytes);
           for (int pn = 0; pn < C::kPanels; ++pn)
             tma_load_2d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh * p.npad + j * kBN);
-          tma_load_2d(sk + C::kKTileBytes, &vmap, kv_full + s, j * kBN, hh * D);
+          if (kPv16) {
+            for (int pn = 0; pn < 2; ++pn)
+              tma_load_2d(sk + C::kKTileBytes + pn * C::kVPanelBytes, &vmap, kv_full + s, j * kBN + pn * 64, hh * D);
+          } else {
+            tma_load_2d(sk + C::kKTileBytes, &vmap, kv_full + s, j * kBN, hh * D);
+          }
         }
       }
     } else if (warp == 1) {
@@ -333,7 +391,7 @@ __global__ void __launch_bounds__(384, 1)
               break;
             }
             tc_fence_after();
-            issue_pv<D>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            issue_pv<D, kPv16>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
             tc_commit(pv_done + t);
             if (t == 1) tc_commit(kv_empty + s);
             if (j + 1 < ntiles) {
@@ -360,7 +418,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else {
-    regs_inc<kRegsSoftmax>();
+    regs_inc<(kPv16 ? kRegsSoftmaxPv16 : kRegsSoftmax)>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                     // TMEM lane quarter this warp may access
@@ -398,9 +456,9 @@ __global__ void __launch_bounds__(384, 1)
       const float c0 = cq * ks0, c1 = cq * ks1;
       const int kvalid = min(kBN, p.n - j * kBN);
       if (kvalid == kBN)
-        softmax_step<D, false>(tS, tO, c0, c1, kBN, j == 0, m, l);
+        softmax_step<D, false, kPv16>(tS, tO, c0, c1, kBN, j == 0, m, l);
       else
-        softmax_step<D, true>(tS, tO, c0, c1, kvalid, j == 0, m, l);
+        softmax_step<D, true, kPv16>(tS, tO, c0, c1, kvalid, j == 0, m, l);
       tc_fence_before();
       mbar_arrive(p_full + t);
     }
@@ -408,6 +466,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const float* vs = p.v_scales + hh * D;
+      const float* vm = p.v_mean + hh * D;
       uint16_t* orow = p.out + static_cast<int64_t>(row) * p.ost + static_cast<int64_t>(hh) * p.osh;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -421,8 +480,12 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int k = v8 * 8 + u * 2;
-              const float a = __uint_as_float(o[k]) * vs[c + k] * inv_l;
-              const float b = __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
+              float a = __uint_as_float(o[k]) * vs[c + k] * inv_l;
+              float b = __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
+              if (kMean) {
+                a += vm[c + k];
+                b += vm[c + k + 1];
+              }
               w[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
             }
@@ -450,7 +513,7 @@ template <int D>
 __global__ void __launch_bounds__(128, 1)
     debug_qk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, int npad,
                     int head, int i0, int j0, int32_t* out, int ldo, int32_t* status, uint64_t limit) {
-  using C = Cfg<D>;
+  using C = Cfg<D, false>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ volatile int s_abort;
   __shared__ uint32_t tmem_slot;
@@ -559,24 +622,41 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
   return r == CUDA_SUCCESS;
 }
 
+template <int D, bool kRowQ, bool kPv16, bool kMean>
+cudaError_t launch_variant(dim3 grid, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const AttnParams& p, cudaStream_t s) {
+  constexpr int kSmem = Cfg<D, kPv16>::kSmemBytes;
+  static bool attr_set = false;   // per instantiation
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kRowQ, kPv16, kMean>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  attn_fwd_kernel<D, kRowQ, kPv16, kMean><<<grid, 384, kSmem, s>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool kRowQ, bool kPv16>
+cudaError_t launch_mean(dim3 grid, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        const AttnParams& p, cudaStream_t s) {
+  return p.v_mean ? launch_variant<D, kRowQ, kPv16, true>(grid, qmap, kmap, vmap, p, s)
+                  : launch_variant<D, kRowQ, kPv16, false>(grid, qmap, kmap, vmap, p, s);
+}
+
 template <int D>
 cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_block, float sm_scale, void* out,
                               int64_t ost, int64_t osh, int32_t* status, cudaStream_t s) {
-  using C = Cfg<D>;
   const int npad = static_cast<int>(pad128(n));
+  const bool pv16 = qz.v_format == 1;
   CUtensorMap qmap, kmap, vmap;
+  const bool vmap_ok =
+      pv16 ? make_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.v_codes, npad, static_cast<uint64_t>(h) * D, 64, D)
+           : make_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qz.v_codes, npad, static_cast<uint64_t>(h) * D, 128, D);
   if (!make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.q_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||
       !make_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.k_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||
-      !make_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qz.v_codes, npad, static_cast<uint64_t>(h) * D, 128, D))
+      !vmap_ok)
     return cudaErrorInvalidValue;
-  static bool attr_set[2] = {false, false};
-  const bool row_q = q_block != 128;
-  if (!attr_set[row_q]) {
-    cudaError_t e = cudaFuncSetAttribute(row_q ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[row_q] = true;
-  }
   AttnParams p;
   p.n = n;
   p.npad = npad;
@@ -586,24 +666,26 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_bloc
   while ((1 << p.q_shift) < q_block) ++p.q_shift;
   p.k_scales = qz.k_scales;
   p.v_scales = qz.v_scales;
+  p.v_mean = qz.v_mean;
   p.sm_scale_log2 = sm_scale * kLog2e;
   p.out = static_cast<uint16_t*>(out);
   p.ost = ost;
   p.osh = osh;
   p.status = status;
   p.wait_limit_ns = kWaitLimitNs;
-  dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
-  if (row_q)
-    attn_fwd_kernel<D, true><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
-  else
-    attn_fwd_kernel<D, false><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, p);
-  return cudaGetLastError();
+  const dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
+  const bool row_q = q_block != 128;
+  if (pv16)
+    return row_q ? launch_mean<D, true, true>(grid, qmap, kmap, vmap, p, s)
+                 : launch_mean<D, false, true>(grid, qmap, kmap, vmap, p, s);
+  return row_q ? launch_mean<D, true, false>(grid, qmap, kmap, vmap, p, s)
+               : launch_mean<D, false, false>(grid, qmap, kmap, vmap, p, s);
 }
 
 template <int D>
 cudaError_t launch_debug_qk_t(int n, int h, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
                               int col_tiles, int32_t* out, int32_t* status, cudaStream_t s) {
-  using C = Cfg<D>;
+  using C = Cfg<D, false>;
   const int npad = static_cast<int>(pad128(n));
   CUtensorMap qmap, kmap;
   if (!make_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qz.q_codes, D, static_cast<uint64_t>(h) * npad, 64, 128) ||

@@ -47,11 +47,12 @@ __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
 
 // ---------------------------------------------------------------------------- kernel R
 // One thread per (chunk of 128 tokens, 8 consecutive columns of one head).  Sum mode adds
-// the chunk's tokens in ascending order in fp32; absmax mode keeps max |x|.
-// partials[chunk][h*D + c].
-template <bool kAbsMax>
+// the chunk's tokens in ascending order in fp32; absmax mode keeps max |x|, or with kSubMean
+// max |fl32(x - mean[h][c])| (the maxima of smoothed V).  partials[chunk][h*D + c].
+template <bool kAbsMax, bool kSubMean = false>
 __global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
-                                                        int n, int h, int d, float* __restrict__ partials) {
+                                                        int n, int h, int d, const float* __restrict__ mean,
+                                                        float* __restrict__ partials) {
   const int vpr = d >> 3;  // 16-byte vectors per (token, head) row
   const int g = blockIdx.y * blockDim.x + threadIdx.x;
   if (g >= h * vpr) return;
@@ -59,9 +60,12 @@ __global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restri
   const int t0 = blockIdx.x * 128;
   const int t1 = min(t0 + 128, n);
   const uint16_t* base = x + hh * sh + c8 * 8;
-  float acc[8];
+  float acc[8], mu[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    acc[j] = 0.0f;
+    mu[j] = kSubMean ? mean[hh * d + c8 * 8 + j] : 0.0f;
+  }
   for (int t = t0; t < t1; t += 8) {
     uint4 v[8];
 #pragma unroll
@@ -73,7 +77,10 @@ __global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restri
         float f[8];
         unpack8(v[u], f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = kAbsMax ? fmaxf(acc[j], fabsf(f[j])) : acc[j] + f[j];
+        for (int j = 0; j < 8; ++j) {
+          if (kSubMean) f[j] = __fsub_rn(f[j], mu[j]);
+          acc[j] = kAbsMax ? fmaxf(acc[j], fabsf(f[j])) : acc[j] + f[j];
+        }
       }
     }
   }
@@ -85,10 +92,11 @@ __global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restri
 // ---------------------------------------------------------------------------- finalise
 // 32 columns per CTA.  The chunk partials are split into 8 groups of G = ceil(nchunk / 8)
 // consecutive chunks; warp w folds group w in ascending chunk order (fp64 for sums), then
-// warp 0 folds the 8 group results in ascending group order.  Mean = fp32(total / N).
+// warp 0 folds the 8 group results in ascending group order.  Mean = fp32(total / N); in
+// absmax mode out = fl32(max / amax_div) (448 for E4M3 scales, 127 for INT8), IEEE division.
 template <bool kAbsMax>
 __global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__ partials, int nchunk, int cols,
-                                                       int n, float* __restrict__ out) {
+                                                       int n, float amax_div, float* __restrict__ out) {
   __shared__ double gsum[8][32];
   __shared__ float gmax[8][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__
       t += gsum[w][lane];
       m = fmaxf(m, gmax[w][lane]);
     }
-    out[col] = kAbsMax ? m / 448.0f : static_cast<float>(t / static_cast<double>(n));
+    out[col] = kAbsMax ? __fdiv_rn(m, amax_div) : static_cast<float>(t / static_cast<double>(n));
   }
 }
 
@@ -372,18 +380,23 @@ __global__ void __launch_bounds__(256) quant_q_grouped_kernel(const uint16_t* __
 }
 
 // ---------------------------------------------------------------------------- kernel V
-// One CTA per (128-token block, head).  Phase 1: each work item loads 4 tokens x 8 channels,
-// encodes them and stores, per channel, one 32-bit word of 4 consecutive tokens into a
-// [D][33]-word shared tile.  Phase 2: 8 threads write each channel's 128 contiguous bytes
-// of v_codes[h][c][block] with 16-byte stores.
-template <int D>
+// One CTA per (head, 128-token block).  Phase 1: each work item loads 4 tokens x 8 channels,
+// encodes them and stores, per channel, the codes of its 4 consecutive tokens into a
+// [D][kWords + 1]-word shared tile (kWords words hold a channel's 128 codes).  Phase 2: each
+// channel's 128 contiguous codes of v_codes[h][c][block] leave with 16-byte stores.
+//   kI8 = false: E4M3 bytes, scale = max / 448.  kI8 = true: INT8 codes held as fp16 (the INT8
+//   P.V variant), scale = max / 127, code = clamp(rint(x / scale), -127, 127).
+//   kMean: the codes of x = fl32(v - v_mean[h][c]) (V smoothing); otherwise x = v.
 // The codes of a channel with a subnormal scale (no finite reciprocal) come out wrong here and
 // are rewritten by quant_v_fixup_kernel, so the loop below stays free of that case.
+template <int D, bool kI8, bool kMean>
 __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict__ v, int64_t st, int64_t sh,
-                                                      const float* __restrict__ v_scales, int n, int npad,
-                                                      uint8_t* __restrict__ v_codes) {
+                                                      const float* __restrict__ v_scales,
+                                                      const float* __restrict__ v_mean, int n, int npad,
+                                                      void* __restrict__ v_codes) {
   constexpr int VPR = D / 8;
-  __shared__ uint32_t tile[D][33];
+  constexpr int kWords = kI8 ? 64 : 32;
+  __shared__ uint32_t tile[D][kWords + 1];
   const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
   const int t_base = b * 128;
   constexpr int kItems = VPR * 32 / 256;   // work items per thread: 2 at D = 128, 1 at D = 64
@@ -404,6 +417,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
     const int c8 = it % VPR, tg = it / VPR;
     uint64_t ns2[4], r2[4];
     bool zero[8];
+    float mu[8];
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
       const float s0 = v_scales[hh * D + c8 * 8 + j], s1 = v_scales[hh * D + c8 * 8 + j + 1];
@@ -412,12 +426,19 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
       ns2[j / 2] = f2_pack(-s0, -s1);
       r2[j / 2] = f2_pack(1.0f / s0, 1.0f / s1);   // IEEE; unused when the scale is 0
     }
-    uint32_t bytes[4][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mu[j] = kMean ? v_mean[hh * D + c8 * 8 + j] : 0.0f;
+    uint32_t bytes[4][8];   // E4M3 codes
+    float cq[4][8];         // INT8 codes
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = t_base + tg * 4 + u;
       float f[8];
       unpack8(raw[i][u], f);
+      if (kMean) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __fsub_rn(f[j], mu[j]);
+      }
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
         float y0, y1;
@@ -428,29 +449,49 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint16_t* __restrict
         y1 = copysignf(y1, f[j + 1]);
         if (t >= n || zero[j]) y0 = 0.0f;
         if (t >= n || zero[j + 1]) y1 = 0.0f;
-        const uint32_t pr = e4m3x2(y0, y1);
-        bytes[u][j] = pr & 0xFFu;
-        bytes[u][j + 1] = pr >> 8;
+        if (kI8) {
+          cq[u][j] = fminf(fmaxf(rintf(y0), -127.0f), 127.0f);
+          cq[u][j + 1] = fminf(fmaxf(rintf(y1), -127.0f), 127.0f);
+        } else {
+          const uint32_t pr = e4m3x2(y0, y1);
+          bytes[u][j] = pr & 0xFFu;
+          bytes[u][j + 1] = pr >> 8;
+        }
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      tile[c8 * 8 + j][tg] = bytes[0][j] | (bytes[1][j] << 8) | (bytes[2][j] << 16) | (bytes[3][j] << 24);
+    for (int j = 0; j < 8; ++j) {
+      if (kI8) {
+        uint32_t w0, w1;   // integers |c| <= 127: exact in fp16; the earlier token in the low half
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w0) : "f"(cq[1][j]), "f"(cq[0][j]));
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w1) : "f"(cq[3][j]), "f"(cq[2][j]));
+        tile[c8 * 8 + j][tg * 2] = w0;
+        tile[c8 * 8 + j][tg * 2 + 1] = w1;
+      } else {
+        tile[c8 * 8 + j][tg] = bytes[0][j] | (bytes[1][j] << 8) | (bytes[2][j] << 16) | (bytes[3][j] << 24);
+      }
+    }
   }
   __syncthreads();
-  for (int o = threadIdx.x; o < D * 8; o += 256) {
-    const int c = o >> 3, seg = o & 7;
+  constexpr int kSegs = kWords / 4;   // 16-byte segments per channel
+  for (int o = threadIdx.x; o < D * kSegs; o += 256) {
+    const int c = o / kSegs, seg = o % kSegs;
     const uint4 w = make_uint4(tile[c][seg * 4], tile[c][seg * 4 + 1], tile[c][seg * 4 + 2], tile[c][seg * 4 + 3]);
-    *reinterpret_cast<uint4*>(v_codes + (static_cast<int64_t>(hh) * D + c) * npad + t_base + seg * 16) = w;
+    const int64_t row = (static_cast<int64_t>(hh) * D + c) * npad + t_base;
+    if (kI8)
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(v_codes) + row + seg * 8) = w;
+    else
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(v_codes) + row + seg * 16) = w;
   }
 }
 
-// One CTA per head: if a channel of the head has a subnormal scale (all |v| of the channel
+// One CTA per head: if a channel of the head has a subnormal scale (all |x| of the channel
 // below ~2^-117), its codes are recomputed with IEEE division; otherwise the CTA exits at once.
-template <int D>
+template <int D, bool kI8, bool kMean>
 __global__ void __launch_bounds__(256) quant_v_fixup_kernel(const uint16_t* __restrict__ v, int64_t st, int64_t sh,
-                                                            const float* __restrict__ v_scales, int n, int npad,
-                                                            uint8_t* __restrict__ v_codes) {
+                                                            const float* __restrict__ v_scales,
+                                                            const float* __restrict__ v_mean, int n, int npad,
+                                                            void* __restrict__ v_codes) {
   const int hh = blockIdx.x;
   bool sub = false;
   for (int c = threadIdx.x; c < D; c += 256) sub = sub || subnormal_scale(v_scales[hh * D + c]);
@@ -458,34 +499,65 @@ __global__ void __launch_bounds__(256) quant_v_fixup_kernel(const uint16_t* __re
   for (int c = 0; c < D; ++c) {
     const float sc = v_scales[hh * D + c];
     if (!subnormal_scale(sc)) continue;
+    const float mu = kMean ? v_mean[hh * D + c] : 0.0f;
     for (int t = threadIdx.x; t < n; t += 256) {
-      const float x = __uint_as_float(static_cast<uint32_t>(v[static_cast<int64_t>(t) * st + hh * sh + c]) << 16);
-      v_codes[(static_cast<int64_t>(hh) * D + c) * npad + t] = static_cast<uint8_t>(e4m3x2(__fdiv_rn(x, sc), 0.0f) & 0xFFu);
+      float x = __uint_as_float(static_cast<uint32_t>(v[static_cast<int64_t>(t) * st + hh * sh + c]) << 16);
+      if (kMean) x = __fsub_rn(x, mu);
+      const float q = __fdiv_rn(x, sc);
+      const int64_t idx = (static_cast<int64_t>(hh) * D + c) * npad + t;
+      if (kI8)
+        static_cast<uint16_t*>(v_codes)[idx] = __half_as_ushort(__float2half_rn(fminf(fmaxf(rintf(q), -127.0f), 127.0f)));
+      else
+        static_cast<uint8_t*>(v_codes)[idx] = static_cast<uint8_t>(e4m3x2(q, 0.0f) & 0xFFu);
     }
   }
 }
 
-}  // namespace
-
-cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, float* partials,
-                             cudaStream_t s) {
-  const int nchunk = (n + 127) / 128;
-  const int groups = h * (d / 8);
-  dim3 grid(nchunk, (groups + 127) / 128);
-  if (absmax)
-    colreduce_kernel<true><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, partials);
-  else
-    colreduce_kernel<false><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, partials);
+template <int D, bool kI8, bool kMean>
+cudaError_t launch_quant_v_t(const StridedView& v, const float* v_scales, const float* v_mean, int n, int h,
+                             void* v_codes, cudaStream_t s) {
+  const int npad = static_cast<int>(pad128(n));
+  quant_v_kernel<D, kI8, kMean><<<dim3(h, npad / 128), 256, 0, s>>>(v.data, v.st, v.sh, v_scales, v_mean, n, npad,
+                                                                     v_codes);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  quant_v_fixup_kernel<D, kI8, kMean><<<h, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, v_mean, n, npad, v_codes);
   return cudaGetLastError();
 }
 
-cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, bool absmax, float* out,
+template <int D>
+cudaError_t launch_quant_v_d(const StridedView& v, const float* v_scales, const float* v_mean, int v_format, int n,
+                             int h, void* v_codes, cudaStream_t s) {
+  if (v_format == 1)
+    return v_mean ? launch_quant_v_t<D, true, true>(v, v_scales, v_mean, n, h, v_codes, s)
+                  : launch_quant_v_t<D, true, false>(v, v_scales, v_mean, n, h, v_codes, s);
+  return v_mean ? launch_quant_v_t<D, false, true>(v, v_scales, v_mean, n, h, v_codes, s)
+                : launch_quant_v_t<D, false, false>(v, v_scales, v_mean, n, h, v_codes, s);
+}
+
+}  // namespace
+
+cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, const float* mean,
+                             float* partials, cudaStream_t s) {
+  const int nchunk = (n + 127) / 128;
+  const int groups = h * (d / 8);
+  dim3 grid(nchunk, (groups + 127) / 128);
+  if (absmax && mean)
+    colreduce_kernel<true, true><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, mean, partials);
+  else if (absmax)
+    colreduce_kernel<true><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, nullptr, partials);
+  else
+    colreduce_kernel<false><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, nullptr, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, float amax_div, float* out,
                             cudaStream_t s) {
   dim3 grid((cols + 31) / 32);
-  if (absmax)
-    colfinal_kernel<true><<<grid, 256, 0, s>>>(partials, nchunk, cols, n, out);
+  if (amax_div != 0.0f)
+    colfinal_kernel<true><<<grid, 256, 0, s>>>(partials, nchunk, cols, n, amax_div, out);
   else
-    colfinal_kernel<false><<<grid, 256, 0, s>>>(partials, nchunk, cols, n, out);
+    colfinal_kernel<false><<<grid, 256, 0, s>>>(partials, nchunk, cols, n, 0.0f, out);
   return cudaGetLastError();
 }
 
@@ -513,21 +585,10 @@ cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const fl
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, int h, int d, uint8_t* v_codes,
-                           cudaStream_t s) {
-  const int npad = static_cast<int>(pad128(n));
-  dim3 grid(h, npad / 128);
-  if (d == 128)
-    quant_v_kernel<128><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
-  else
-    quant_v_kernel<64><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (d == 128)
-    quant_v_fixup_kernel<128><<<h, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
-  else
-    quant_v_fixup_kernel<64><<<h, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, n, npad, v_codes);
-  return cudaGetLastError();
+cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, const float* v_mean, int v_format, int n,
+                           int h, int d, void* v_codes, cudaStream_t s) {
+  return d == 128 ? launch_quant_v_d<128>(v, v_scales, v_mean, v_format, n, h, v_codes, s)
+                  : launch_quant_v_d<64>(v, v_scales, v_mean, v_format, n, h, v_codes, s);
 }
 
 }  // namespace sage

@@ -65,7 +65,8 @@ sage_status check_qz(const sage_quantized* qz, bool need_qk, bool need_v) {
   }
   if (need_v) {
     if (!qz->v_codes || !qz->v_scales) return SAGE_ERR_INVALID_ARG;
-    if (!aligned16(qz->v_codes) || !aligned16(qz->v_scales)) return SAGE_ERR_ALIGNMENT;
+    if (qz->v_format != 0 && qz->v_format != 1) return SAGE_ERR_INVALID_ARG;
+    if (!aligned16(qz->v_codes) || !aligned16(qz->v_scales) || !aligned16(qz->v_mean)) return SAGE_ERR_ALIGNMENT;
   }
   return SAGE_OK;
 }
@@ -102,6 +103,8 @@ Carve carve(void* base, int64_t n, int64_t h, int64_t d) {
   c.qz.k_scales = reinterpret_cast<float*>(take(size_t(h) * (np / 64) * 4));
   c.qz.k_mean = reinterpret_cast<float*>(take(size_t(h) * d * 4));
   c.qz.v_scales = reinterpret_cast<float*>(take(size_t(h) * d * 4));
+  c.qz.v_format = 0;
+  c.qz.v_mean = nullptr;
   c.scratch = reinterpret_cast<float*>(take(scratch_bytes(n, h, d)));
   c.total = off;
   return c;
@@ -148,8 +151,8 @@ sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const s
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(ws);
   const int nchunk = static_cast<int>((n + 127) / 128);
-  cudaError_t e = sage::launch_colreduce(sv(k), int(n), int(h), int(d), false, part, s);
-  if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), false, qz->k_mean, s);
+  cudaError_t e = sage::launch_colreduce(sv(k), int(n), int(h), int(d), false, nullptr, part, s);
+  if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), 0.0f, qz->k_mean, s);
   if (e == cudaSuccess)
     e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), q_block_of(qz), qz->q_codes,
                               qz->q_scales, qz->k_codes, qz->k_scales, s);
@@ -166,9 +169,18 @@ sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(ws);
   const int nchunk = static_cast<int>((n + 127) / 128);
-  cudaError_t e = sage::launch_colreduce(sv(v), int(n), int(h), int(d), true, part, s);
-  if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), true, qz->v_scales, s);
-  if (e == cudaSuccess) e = sage::launch_quant_v(sv(v), qz->v_scales, int(n), int(h), int(d), qz->v_codes, s);
+  cudaError_t e = cudaSuccess;
+  if (qz->v_mean) {   // V smoothing: the channel mean first, as for K
+    e = sage::launch_colreduce(sv(v), int(n), int(h), int(d), false, nullptr, part, s);
+    if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), 0.0f, qz->v_mean, s);
+  }
+  // Maxima of |v| (or |v - mean|), then scale = max / 448 (E4M3) or max / 127 (INT8).
+  if (e == cudaSuccess) e = sage::launch_colreduce(sv(v), int(n), int(h), int(d), true, qz->v_mean, part, s);
+  if (e == cudaSuccess)
+    e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), qz->v_format ? 127.0f : 448.0f, qz->v_scales, s);
+  if (e == cudaSuccess)
+    e = sage::launch_quant_v(sv(v), qz->v_scales, qz->v_mean, int(qz->v_format), int(n), int(h), int(d),
+                             qz->v_codes, s);
   return cuda_status(e);
 }
 

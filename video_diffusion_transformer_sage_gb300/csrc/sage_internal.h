@@ -30,16 +30,19 @@ struct StridedView {
 inline int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
 
 // quant.cu
-cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, float* partials,
-                             cudaStream_t s);
-cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, bool absmax, float* out,
+// Per-128-token column partials: sums, or maxima of |x| (of |fl32(x - mean)| when mean is set).
+cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, const float* mean,
+                             float* partials, cudaStream_t s);
+// amax_div == 0: out = the column mean; otherwise out = fl32(column max / amax_div).
+cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, float amax_div, float* out,
                             cudaStream_t s);
 // q_block: rows per Q scale, a power of two <= 128.
 cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
                             int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                             cudaStream_t s);
-cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, int n, int h, int d, uint8_t* v_codes,
-                           cudaStream_t s);
+// v_format 0: E4M3 bytes; 1: INT8 codes held as fp16.  v_mean: NULL or the mean to subtract.
+cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, const float* v_mean, int v_format, int n,
+                           int h, int d, void* v_codes, cudaStream_t s);
 
 // qk_transform.cu: in place on the Q and K views.
 cudaError_t launch_rmsnorm_rope(const StridedView& q, const StridedView& k, int n, int h, int d,

@@ -137,6 +137,23 @@ def to_hnd(inp: Inputs) -> Inputs:
     return Inputs(w, storage, views[0], views[1], views[2])
 
 
+def with_v_offset(inp: Inputs, std: float = 8.0, seed: int = 17) -> Inputs:
+    """A copy of `inp` (same layout and strides) whose V carries a per-(head, channel) offset
+    ~ N(0, std^2) shared by all tokens, drawn from its own generator: the input that V
+    smoothing is for.  Q and K are unchanged."""
+    storage = inp.storage.clone()
+
+    def view(t: torch.Tensor) -> torch.Tensor:
+        return storage.as_strided(t.shape, t.stride(), t.storage_offset())
+
+    q, k, v = view(inp.q), view(inp.k), view(inp.v)
+    g = torch.Generator("cpu").manual_seed(seed)
+    off = torch.randn((inp.v.shape[1], inp.v.shape[2]), generator=g) * std
+    v.copy_((inp.v.float() + off).to(torch.bfloat16))
+    w = dataclasses.replace(inp.workload, name=inp.workload.name + "_voff")
+    return Inputs(w, storage, q, k, v)
+
+
 def sample_rows(n_tokens: int, count: int, seed: int) -> list:
     """Seeded query-row sample that always includes both ends, the last 128-row tile and,
     where present, the text / conditioning / video segment borders (99/100, 513/514)."""
