@@ -400,7 +400,7 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (1.63 GB QKV buffer)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(composite, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / composite, 4), "traffic": traffic,
-                     "kernel": "attn_fwd_kernel<128, false>",
+                     "kernel": "attn_fwd_kernel<128, false, false, false>",
                      "peak_note": f"composite of the {peak_src} {'burst' if full_clock else 'sustained'} bf16 "
                                   f"{p16} TFLOP/s (QK^T, fp16 operands) and 2x that for E4M3 (PV)",
                      "frac_of_e4m3_peak": round(achieved / p8, 4),
