@@ -174,12 +174,16 @@ def run_gpu(args):
 
     q, k, v = views(storage)
     sm_scale = 1.0 / math.sqrt(d)
-    qz = sage.Quantized(n, h, d, dev)
+    # The timed path: the method's default (E4M3 V and P), or one of its V options.
+    default_path = args.v_format == "e4m3" and not args.smooth_v
+    qz = sage.Quantized(n, h, d, dev, v_format=args.v_format, smooth_v=args.smooth_v)
     scratch = sage.quant_scratch(n, h, d, dev)
     status = sage.status_block(dev)
     out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 8   # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, quant_v_fixup, attention
+    # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, quant_v_fixup, attention;
+    # V smoothing adds colreduce+colfinal for the V mean.
+    launches_per_step = 8 + (2 if args.smooth_v else 0)
 
     def step(ev=None):
         if ev is not None:
@@ -226,7 +230,9 @@ def run_gpu(args):
     # output back to pinned host memory (D2H).  Copies run on their own streams, double
     # buffered, so step i's compute overlaps step i+1's H2D and step i-1's D2H -- a serving
     # loop.  The serial variant (copy, compute, copy, in order) is reported beside it.
-    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 10))
+    # e2e and the per-call distribution time the public whole-path call (sage_attn_fwd), which
+    # runs the default path: skipped when a V option is timed.
+    e2e_steps = 0 if (args.no_e2e or not default_path) else max(3, min(args.steps, 10))
     e2e_ms = e2e_serial_ms = float("nan")
     e2e_runs = []
     host_out = [torch.empty((n, h, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -288,7 +294,7 @@ def run_gpu(args):
     # above, 5 rounds x 10 calls of sage_attn_fwd (steps a1-a8 from the strided views), each
     # call bracketed by its own CUDA events on the launching stream.
     call_timing = None
-    if not args.no_call_timing:
+    if not args.no_call_timing and default_path:
         ws_c = sage.workspace(n, h, d, dev)
         rounds = []
         for _ in range(5):
@@ -386,23 +392,34 @@ def run_gpu(args):
         vv_["roofline_frac"] = round(vv_["attention_tflops"] / (p16 if vname.startswith("int8") else composite), 4)
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
+    # INT8 P.V runs both contractions on 16-bit operands: the bf16 peak is its roofline.
+    attn_peak = p16 if args.v_format == "int8" else composite
+    kname = "attn_fwd_kernel<128, false, %s, %s>" % ("true" if args.v_format == "int8" else "false",
+                                                     "true" if args.smooth_v else "false")
     traffic = _traffic_per_launch()
     quant_avg = statistics.mean(quant_ms)
     quant_bytes = 13 * n * h * d
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp16(int8 codes)xfp16 + e4m3xe4m3 -> fp32, bf16 io",
+        "scaling": "weak", "vs_baseline": None, "dtype": ("fp16(int8 codes)xfp16 + fp16(int8 codes)xfp16 -> fp32, bf16 io" if args.v_format == "int8"
+                                        else "fp16(int8 codes)xfp16 + e4m3xe4m3 -> fp32, bf16 io"),
         "data": "synthetic (seeded, distributions of the pages' workload)",
         "config": {"workload": f"{w.name}: N={n}, H={h}, D={d}, batch 1, non-causal, " + (
                                "HND-contiguous bf16 Q, K, V" if w.layout == "hnd" else
                                f"strided NHD views of a [{n}, {3 * h * d}] bf16 QKV buffer"),
-                   "l2": "inputs larger than L2 (1.63 GB QKV buffer)", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(composite, 1),
-                     "unit": "TFLOP/s", "frac": round(achieved / composite, 4), "traffic": traffic,
-                     "kernel": "attn_fwd_kernel<128, false, false, false>",
-                     "peak_note": f"composite of the {peak_src} {'burst' if full_clock else 'sustained'} bf16 "
-                                  f"{p16} TFLOP/s (QK^T, fp16 operands) and 2x that for E4M3 (PV)",
+                   "path": ("INT8 P.V (INT8 V, P = rint(127 p))" if args.v_format == "int8" else
+                            "E4M3 V and P") + (", V mean smoothing" if args.smooth_v else ""),
+                   "l2": f"inputs larger than L2 ({host.numel() * 2 / 1e9:.2f} GB QKV buffer)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(attn_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / attn_peak, 4),
+                     "traffic": traffic if default_path else None,
+                     "kernel": kname,
+                     "peak_note": (f"the {peak_src} {'burst' if full_clock else 'sustained'} bf16 {p16} TFLOP/s "
+                                   "(both contractions on fp16 operands)" if args.v_format == "int8" else
+                                   f"composite of the {peak_src} {'burst' if full_clock else 'sustained'} bf16 "
+                                   f"{p16} TFLOP/s (QK^T, fp16 operands) and 2x that for E4M3 (PV)"),
                      "frac_of_e4m3_peak": round(achieved / p8, 4),
                      "frac_of_bf16_peak": round(achieved / p16, 4)},
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
@@ -423,7 +440,8 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_budget, v_format=args.v_format,
+                                            smooth_v=args.smooth_v)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:
@@ -454,15 +472,16 @@ def call_stats(rounds):
     return st
 
 
-def cpu_baseline(inp, budget_s: float = 20.0, rows_per_step: int = 8, steps: int = 0):
+def cpu_baseline(inp, budget_s: float = 20.0, rows_per_step: int = 8, steps: int = 0, v_format: str = "e4m3",
+                 smooth_v: bool = False):
     """The oracle as it stands on the host cores: quantisation (steps 1-4) in full, then
     same-quantisation attention for sampled query rows (all heads) until `budget_s` is spent;
-    time per call extrapolated as t_quant + N * t_row."""
+    time per call extrapolated as t_quant + N * t_row.  v_format / smooth_v: the path timed."""
     import oracle
     w = inp.workload
     n, h, d = w.n_tokens, w.n_heads, w.head_dim
     t = time.perf_counter()
-    qz = oracle.Quantized(inp.q, inp.k, inp.v)
+    qz = oracle.Quantized(inp.q, inp.k, inp.v, v_format=v_format, smooth_v=smooth_v)
     t_quant = time.perf_counter() - t
     from video_diffusion_transformer_sage_gb300 import synth
     pool = synth.sample_rows(n, 4096, 17)
@@ -494,7 +513,8 @@ def run_reference(args):
     w = synth.WORKLOADS[args.workload]
     inp = synth.make_inputs(w)
     rows_per_step = 4
-    cb = cpu_baseline(inp, rows_per_step=rows_per_step, steps=args.warmup + args.steps)
+    cb = cpu_baseline(inp, rows_per_step=rows_per_step, steps=args.warmup + args.steps, v_format=args.v_format,
+                      smooth_v=args.smooth_v)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
@@ -517,6 +537,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-call-timing", action="store_true",
                     help="skip the 5 x 10 per-call timing of sage_attn_fwd")
+    ap.add_argument("--v-format", default="e4m3", choices=["e4m3", "int8"],
+                    help="the timed path's V and P codes: e4m3 (the method's default) or int8 (INT8 P.V)")
+    ap.add_argument("--smooth-v", action="store_true", help="time the path with V mean smoothing")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the timing of the INT8 P.V variant and of V smoothing")
     ap.add_argument("--no-qk-transform", action="store_true",
