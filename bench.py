@@ -337,7 +337,36 @@ def run_gpu(args):
                  else "rmsnorm_rope_kernel<%d>") % d
         qk_transform = {"kernel": kname, "ms": round(t_ms, 4), "bytes": t_bytes,
                         "gbs": round(t_bytes / (t_ms * 1e-3) / 1e9, 1), "calls": 20}
-        del buf
+
+        # The same transform fused into the K mean and the Q / K quantisation
+        # (sage_smooth_quant_qk_rmsnorm_rope: Q and K only read), against the unfused pair
+        # (the in-place transform, then sage_smooth_quant_qk) on the same data; 3 warm-up calls,
+        # then 20 calls each, CUDA events per call.  Algorithmic bytes of the fused call: K read
+        # twice (mean, codes) and Q once (6 N H D), fp16 codes written (4 N H D), the table (4 N D).
+        fz = sage.Quantized(n, h, d, dev)
+
+        def timed(fn, calls=20):
+            for _ in range(3):
+                fn()
+            evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+            torch.cuda.synchronize()
+            for a_, b_ in evp:
+                a_.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evp)
+
+        fused_ms = timed(lambda: sage.sage_smooth_quant_qk_rmsnorm_rope(q, k, gq, gk, cos, sin, 1e-6, fz, scratch,
+                                                                        stream))
+        pair_ms = timed(lambda: (sage.sage_qk_rmsnorm_rope(tq, tk, gq, gk, cos, sin, 1e-6, stream),
+                                 sage.sage_smooth_quant_qk(tq, tk, fz, scratch, stream)))
+        f_bytes = 10 * n * h * d + 4 * n * d
+        qk_transform["fused_with_quantise"] = {
+            "call": "sage_smooth_quant_qk_rmsnorm_rope", "ms": round(fused_ms, 4), "bytes": f_bytes,
+            "gbs": round(f_bytes / (fused_ms * 1e-3) / 1e9, 1), "unfused_pair_ms": round(pair_ms, 4),
+            "saved_ms": round(pair_ms - fused_ms, 4)}
+        del buf, fz
 
     # ---- the V options of the path at the same size and inputs, outside the timed region: the
     # INT8 P.V variant (INT8 V, P = rint(127 p), fp16-code MMAs) and V smoothing (the channel
@@ -375,6 +404,7 @@ def run_gpu(args):
     bf16_burst, bf16_sus, hbm, peak_src = _peaks()
     if qk_transform is not None:
         qk_transform["hbm_frac"] = round(qk_transform["gbs"] / hbm, 4)
+        qk_transform["fused_with_quantise"]["hbm_frac"] = round(qk_transform["fused_with_quantise"]["gbs"] / hbm, 4)
     # The fused kernel does half its FLOPs as fp16 MMAs (QK^T on INT8 codes held in fp16)
     # and half as E4M3 MMAs (PV); the E4M3 rate is twice the 16-bit rate.  Its roofline is
     # the time of both halves at their own peaks.  The burst bf16 figure applies when the

@@ -212,6 +212,18 @@ sage_status sage_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const f
                                  const float* gamma_k, const float* rope_cos, const float* rope_sin,
                                  float eps, void* stream);
 
+/* The qk_transform fused into the K smoothing and Q / K quantisation: the same outputs, bit for
+ * bit, as sage_qk_rmsnorm_rope(q, k, ...) followed by sage_smooth_quant_qk(q, k, qz, ...), but
+ * q and k are only READ.  The transform is applied to each row as the quantise kernels load
+ * it (and as the K-mean pass sums it); the transformed Q and K are never written, which saves
+ * their write and re-read (4 N H D bytes each) -- the fusion of the rms_rope stage into the
+ * quantisation prologue.  Arguments: q, k, gamma_*, rope_*, eps as for sage_qk_rmsnorm_rope;
+ * qz, ws, ws_bytes as for sage_smooth_quant_qk (any q_block).  Errors as for both. */
+sage_status sage_smooth_quant_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const float* gamma_q,
+                                              const float* gamma_k, const float* rope_cos, const float* rope_sin,
+                                              float eps, const sage_quantized* qz, void* ws, size_t ws_bytes,
+                                              void* stream);
+
 /* The whole path: sage_smooth_quant_qk, sage_quant_v and sage_attn_fwd_quantized on
  * buffers carved from ws (>= sage_workspace_bytes, 256-byte aligned; the status block at
  * its start must be zeroed once by the caller before first use). */

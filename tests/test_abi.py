@@ -11,7 +11,8 @@ from video_diffusion_transformer_sage_gb300 import _lib
 EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_bytes", "sage_status_block_bytes",
             "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
             "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
-            "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout", "sage_qk_rmsnorm_rope"}
+            "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout", "sage_qk_rmsnorm_rope",
+            "sage_smooth_quant_qk_rmsnorm_rope"}
 
 
 @pytest.fixture(scope="module")
@@ -114,6 +115,15 @@ def test_argument_validation_never_launches(L):
     assert rr(by(q), by(k), 4096, 4096, 4096, 4096, -1.0, None) == 1
     assert rr(by(q), by(k), 4096, 4096, 4096, 4096, float("nan"), None) == 1
     assert rr(by(q), by(_view(h=3)), 4096, 4096, 4096, 4096, 1e-6, None) == 1
+    # the same transform fused into the quantisation: its own checks and those of the quantisation
+    fq = L.sage_smooth_quant_qk_rmsnorm_rope
+    assert fq(by(q), by(k), 4096, 4096, 0, 4096, 1e-6, by(qz), 4096, 1 << 30, None) == 1
+    assert fq(by(q), by(k), 4096, 4100, 4096, 4096, 1e-6, by(qz), 4096, 1 << 30, None) == 2
+    assert fq(by(q), by(k), 4096, 4096, 4096, 4096, float("inf"), by(qz), 4096, 1 << 30, None) == 1
+    assert fq(by(q), by(_view(n=255)), 4096, 4096, 4096, 4096, 1e-6, by(qz), 4096, 1 << 30, None) == 1
+    assert fq(by(q), by(k), 4096, 4096, 4096, 4096, 1e-6, by(qz), 4096, 16, None) == 4
+    assert fq(by(q), by(k), 4096, 4096, 4096, 4096, 1e-6, by(_qz(ptr=4100)), 4096, 1 << 30, None) == 2
+    assert fq(by(_view(d=96)), by(_view(d=96)), 4096, 4096, 4096, 4096, 1e-6, by(qz), 4096, 1 << 30, None) == 3
     assert L.sage_check_device_status(0, None, None) == 1
     assert L.sage_debug_wait_timeout(0, 1000, None) == 1
     assert L.sage_debug_wait_timeout(4096, 0, None) == 1

@@ -91,3 +91,61 @@ def test_rmsnorm_rope_hnd_layout():
     assert inp.q.stride(1) == 700 * 128
     want, got = _run_both(inp, n_text=50, grid=(5, 5, 26))
     assert np.array_equal(got, want)
+
+
+def _fused_vs_oracle(inp, n_text, grid, q_block=128):
+    """The fused call (transform in the quantise prologue) against the oracle's transform of
+    copies of Q and K followed by its quantisation: codes, scales and K mean bit-identical, and
+    the device Q, K, V left as they were."""
+    n, h, d = inp.q.shape
+    gq, gk, cos, sin = _tables(n, d, n_text, grid)
+    dev = torch.device("cuda:0")
+    storage = inp.storage.to(dev)
+
+    def dview(t):
+        off = t.storage_offset() - inp.storage.storage_offset()
+        return storage.as_strided(t.shape, t.stride(), storage.storage_offset() + off)
+
+    before = storage.clone()
+    gz = sage.sage_smooth_quant_qk_rmsnorm_rope(dview(inp.q), dview(inp.k), gq.to(dev), gk.to(dev), cos.to(dev),
+                                               sin.to(dev), EPS, q_block=q_block)
+    torch.cuda.synchronize()
+    assert torch.equal(storage.view(torch.int16), before.view(torch.int16))    # Q and K only read
+    q, k = inp.q.clone(), inp.k.clone()
+    oracle.rmsnorm_rope(q, gq.numpy(), cos.numpy(), sin.numpy(), EPS)
+    oracle.rmsnorm_rope(k, gk.numpy(), cos.numpy(), sin.numpy(), EPS)
+    oz = oracle.Quantized(q, k, inp.v, q_block=q_block)
+    assert np.array_equal(gz.k_mean.cpu().numpy().view(np.uint32), oz.k_mean.view(np.uint32))
+    assert np.array_equal(gz.q_scales.cpu().numpy().view(np.uint32), oz.q_scales.view(np.uint32))
+    assert np.array_equal(gz.k_scales.cpu().numpy().view(np.uint32), oz.k_scales.view(np.uint32))
+    assert np.array_equal(gz.q_codes.cpu().float().numpy(), oz.q_codes.astype(np.float32))
+    assert np.array_equal(gz.k_codes.cpu().float().numpy(), oz.k_codes.astype(np.float32))
+    return gz, oz
+
+
+@pytest.mark.parametrize("name,q_block", [("tiny", 128), ("strided64", 128), ("video", 128), ("tails", 32)])
+def test_fused_transform_quant_bit_exact(name, q_block):
+    _fused_vs_oracle(synth.make_inputs(name), 514, synth.VIDEO_GRID, q_block)
+
+
+@pytest.mark.parametrize("n,h,d", [(300, 3, 128), (129, 5, 64), (1, 1, 128)])
+def test_fused_transform_quant_ragged(n, h, d):
+    """Odd head counts (a warp's lanes past the last head run on zeros in the K-mean pass), a
+    partial last block and a single token."""
+    inp = synth.make_inputs(synth.custom(n, h, d, "qkv", seed=n + 2 * h, n_outlier=1))
+    _fused_vs_oracle(inp, min(n, 20), (4, 4, 8))
+
+
+def test_fused_transform_quant_hnd_and_attention():
+    """HND-contiguous views, then the attention on the fused call's codes against the oracle."""
+    inp = synth.to_hnd(synth.make_inputs(synth.custom(700, 3, 128, "qkv", seed=8, n_outlier=1)))
+    gz, oz = _fused_vs_oracle(inp, 50, (5, 5, 26))
+    dv = inp.v.to("cuda")
+    sage.sage_quant_v(dv, gz)
+    sm = 1.0 / math.sqrt(128)
+    out = sage.sage_attn_fwd_quantized(gz, sm)
+    torch.cuda.synchronize()
+    ref = oracle.attn_sq(oz, sm, list(range(700)), tile=128)
+    got = out.float().cpu().numpy().astype(np.float64)
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert rel <= 5e-3 and float(np.abs(got - ref).max()) <= 3e-2, rel

@@ -77,6 +77,7 @@ def lib():
             "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "sage_debug_wait_timeout": ([P, I, P], ctypes.c_int),
             "sage_qk_rmsnorm_rope": ([VP, VP, P, P, P, P, F, P], ctypes.c_int),
+            "sage_smooth_quant_qk_rmsnorm_rope": ([VP, VP, P, P, P, P, F, QP, P, S, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -267,3 +268,28 @@ def sage_qk_rmsnorm_rope(q: torch.Tensor, k: torch.Tensor, gamma_q: torch.Tensor
     _check(lib().sage_qk_rmsnorm_rope(ctypes.byref(vq), ctypes.byref(vk), gamma_q.data_ptr(), gamma_k.data_ptr(),
                                       rope_cos.data_ptr(), rope_sin.data_ptr(), float(eps), _stream(stream)),
            "sage_qk_rmsnorm_rope")
+
+
+def _check_transform_tables(n: int, d: int, gamma_q, gamma_k, rope_cos, rope_sin) -> None:
+    for t, shape in ((gamma_q, (d,)), (gamma_k, (d,)), (rope_cos, (n, d // 2)), (rope_sin, (n, d // 2))):
+        if t.dtype != torch.float32 or not t.is_cuda or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"expected a contiguous fp32 CUDA tensor of shape {shape}")
+
+
+def sage_smooth_quant_qk_rmsnorm_rope(q: torch.Tensor, k: torch.Tensor, gamma_q: torch.Tensor, gamma_k: torch.Tensor,
+                                      rope_cos: torch.Tensor, rope_sin: torch.Tensor, eps: float = 1e-6,
+                                      qz: Optional[Quantized] = None, scratch: Optional[torch.Tensor] = None,
+                                      stream=None, q_block: int = 128, v_format: str = "e4m3",
+                                      smooth_v: bool = False) -> Quantized:
+    """sage_qk_rmsnorm_rope then sage_smooth_quant_qk in one pass, without modifying q and k:
+    the transform runs in the quantise kernels' prologue."""
+    n, h, d = q.shape
+    _check_transform_tables(n, d, gamma_q, gamma_k, rope_cos, rope_sin)
+    qz = qz or Quantized(n, h, d, q.device, q_block, v_format, smooth_v)
+    scratch = scratch if scratch is not None else quant_scratch(n, h, d, q.device)
+    vq, vk, c = make_view(q), make_view(k), qz.c()
+    _check(lib().sage_smooth_quant_qk_rmsnorm_rope(ctypes.byref(vq), ctypes.byref(vk), gamma_q.data_ptr(),
+                                                   gamma_k.data_ptr(), rope_cos.data_ptr(), rope_sin.data_ptr(),
+                                                   float(eps), ctypes.byref(c), scratch.data_ptr(), scratch.numel(),
+                                                   _stream(stream)), "sage_smooth_quant_qk_rmsnorm_rope")
+    return qz

@@ -30,6 +30,7 @@
 
 #include <algorithm>
 
+#include "qk_row.cuh"
 #include "sage_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -44,60 +45,6 @@ __device__ __forceinline__ uint4 ld_rows(const uint16_t* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
-
-// ---- the row arithmetic, shared by both kernels ----------------------------------------
-__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float f[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(w[j] << 16);
-    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-  }
-}
-
-// sum_c x_c^2 of the row: the thread's 8 channels in channel order, then the butterfly over
-// the row's VPR consecutive lanes.  Every lane of the warp must call it.
-template <int VPR>
-__device__ __forceinline__ float row_sumsq(const float f[8]) {
-  float acc = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, __fmul_rn(f[j], f[j]));
-#pragma unroll
-  for (int s = VPR / 2; s > 0; s >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, s));
-  return acc;
-}
-
-// The thread's 8 channels after the norm (1 / sqrt(sum / D + eps), weight g) and the rotation
-// of its 4 channel pairs by (cs, sn), as 4 bf16x2 words.
-template <int D>
-__device__ __forceinline__ uint4 norm_rotate8(const float f[8], float sumsq, float eps, const float g[8],
-                                              const float4& cs, const float4& sn) {
-  const float ms = __fmul_rn(sumsq, 1.0f / D);
-  const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-  const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float y0 = __fmul_rn(__fmul_rn(f[2 * j], rs), g[2 * j]);
-    const float y1 = __fmul_rn(__fmul_rn(f[2 * j + 1], rs), g[2 * j + 1]);
-    const float z0 = __fsub_rn(__fmul_rn(y0, cc[j]), __fmul_rn(y1, ss[j]));
-    const float z1 = __fadd_rn(__fmul_rn(y0, ss[j]), __fmul_rn(y1, cc[j]));
-    o[j] = bf16x2_rne(z0, z1);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ void load_gamma8(const float* gamma, int c8, float g[8]) {
-  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8));
-  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gamma + c8 * 8 + 4));
-  g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-  g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
 }
 
 // blockIdx.z: 0 = Q, 1 = K.  Rows (t, h) are numbered t * H + h, heads fastest; batch b holds

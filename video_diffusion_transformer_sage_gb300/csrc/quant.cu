@@ -22,6 +22,7 @@
 
 #include <type_traits>
 
+#include "qk_row.cuh"
 #include "sage_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -136,6 +137,64 @@ __global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__
   }
 }
 
+// ---------------------------------------------------------------------------- transform
+// The qk_transform of the NP rows a thread holds (rows row_first + p * RPP, 8 channels each):
+// every lane of the block takes part (the row sum is a butterfly over the row's lanes); rows
+// past n stay zero (their table index is clamped into range and the result dropped).
+template <int D, int NP, int RPP>
+__device__ __forceinline__ void transform_rows(uint4 (&v)[NP], const float* gamma, int row_first, int n, int c8,
+                                               const RowTransform& tr) {
+  float g[8];
+  load_gamma8(gamma, c8, g);
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int row = row_first + p * RPP;
+    const uint4 y = transform_row8<D>(v[p], min(row, n - 1), c8, g, tr.rope_cos, tr.rope_sin, tr.eps);
+    v[p] = row < n ? y : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Column sums of the transformed K, per 128-token chunk, in the order of colreduce_kernel's
+// sum mode (ascending tokens, fp32): the partials of the mean of the transformed K.  One thread
+// per (chunk, 8 channels of one head); a head's D/8 threads are consecutive lanes.  Threads
+// past the last head run the loop on zeros (the row sums need every lane) and store nothing.
+template <int D>
+__global__ void __launch_bounds__(128) colsum_transform_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
+                                                               int n, int h, const RowTransform tr,
+                                                               float* __restrict__ partials) {
+  constexpr int VPR = D / 8;
+  const int g = blockIdx.y * blockDim.x + threadIdx.x;
+  const bool active = g < h * VPR;
+  const int hh = active ? g / VPR : 0, c8 = g % VPR;
+  const int t0 = blockIdx.x * 128;
+  const int t1 = min(t0 + 128, n);
+  const uint16_t* base = x + hh * sh + c8 * 8;
+  float gam[8];
+  load_gamma8(tr.gamma_k, c8, gam);
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int t = t0; t < t1; t += 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = (active && t + u < t1) ? ld_stream(base + static_cast<int64_t>(t + u) * st) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (t + u < t1) {   // uniform over the block
+        float f[8];
+        unpack8(transform_row8<D>(v[u], t + u, c8, gam, tr.rope_cos, tr.rope_sin, tr.eps), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = acc[j] + f[j];
+      }
+    }
+  }
+  if (!active) return;
+  float4* dst = reinterpret_cast<float4*>(partials + static_cast<int64_t>(blockIdx.x) * h * D + hh * D + c8 * 8);
+  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
 // ---------------------------------------------------------------------------- kernel Q
 template <int kThreads>
 __device__ __forceinline__ float block_max(float v, float* red) {
@@ -192,14 +251,19 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
 // only_k: every CTA does K (Q is quantised per smaller block by quant_q_grouped_kernel).
 // Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
 // all its loads before any arithmetic; the maxima share one block reduction.
-template <int D>
-// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.
-__global__ void __launch_bounds__(256, 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
+// kTransform: each loaded row first gets the qk_transform (RMSNorm + rotary embedding), so the
+// codes are those of the transformed Q and K, which are never written back.
+template <int D, bool kTransform>
+// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.  With
+// the transform, 3 CTAs per SM (80 registers, 88 bytes of spills to L1) measured fastest: 1.085 ms
+// for the fused call on the video workload, against 1.111 at 2 CTAs (127 registers, no spills)
+// and 1.097 at 4.
+__global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
                                                        const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
                                                        const float* __restrict__ k_mean, int n, int npad, int only_k,
                                                        uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
                                                        uint16_t* __restrict__ k_codes,
-                                                       float* __restrict__ k_scales) {
+                                                       float* __restrict__ k_scales, const RowTransform tr) {
   constexpr int VPR = D / 8;            // vectors per row
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
@@ -217,6 +281,7 @@ __global__ void __launch_bounds__(256, 4) quant_qk_kernel(const uint16_t* __rest
     const int row = row0 + p * RPP + rin;
     v[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
   }
+  if (kTransform) transform_rows<D, NP, RPP>(v, is_k ? tr.gamma_k : tr.gamma_q, row0 + rin, n, c8, tr);
   float mu[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mu[j] = is_k ? k_mean[hh * D + c8 * 8 + j] : 0.0f;
@@ -307,11 +372,11 @@ __global__ void __launch_bounds__(256, 4) quant_qk_kernel(const uint16_t* __rest
 // hold it (on bf16 bit patterns, as above), then over each group of q_block rows: shuffles
 // within a warp (thread t < 128 holds row t), shared memory across warps for 64-row groups.
 // Pad rows count as 0, so a group wholly in the padding gets scale 0 and codes 0.
-template <int D>
+template <int D, bool kTransform>
 __global__ void __launch_bounds__(256) quant_q_grouped_kernel(const uint16_t* __restrict__ q, int64_t qst,
                                                               int64_t qsh, int n, int npad, int q_block,
                                                               uint16_t* __restrict__ q_codes,
-                                                              float* __restrict__ q_scales) {
+                                                              float* __restrict__ q_scales, const RowTransform tr) {
   constexpr int VPR = D / 8;            // vectors per row
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
@@ -327,6 +392,7 @@ __global__ void __launch_bounds__(256) quant_q_grouped_kernel(const uint16_t* __
     const int row = row0 + p * RPP + rin;
     v[p] = row < n ? ld_stream(q + static_cast<int64_t>(row) * qst + hh * qsh + c8 * 8) : make_uint4(0, 0, 0, 0);
   }
+  if (kTransform) transform_rows<D, NP, RPP>(v, tr.gamma_q, row0 + rin, n, c8, tr);
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     uint32_t bits = __vmaxu2(__vmaxu2(v[p].x & 0x7FFF7FFFu, v[p].y & 0x7FFF7FFFu),
@@ -561,27 +627,45 @@ cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
-                            int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
-                            cudaStream_t s) {
+namespace {
+
+template <int D, bool kTransform>
+cudaError_t launch_quant_qk_t(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h,
+                              int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
+                              const RowTransform& tr, cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
   const int only_k = q_block != 128;
-  dim3 grid(h, npad / 128, only_k ? 1 : 2);
+  quant_qk_kernel<D, kTransform><<<dim3(h, npad / 128, only_k ? 1 : 2), 256, 0, s>>>(
+      q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k, q_codes, q_scales, k_codes, k_scales, tr);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !only_k) return e;
+  quant_q_grouped_kernel<D, kTransform><<<dim3(h, npad / 128), 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block,
+                                                                            q_codes, q_scales, tr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
+                            int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
+                            const RowTransform* tr, cudaStream_t s) {
+  const RowTransform none{};
   if (d == 128)
-    quant_qk_kernel<128><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k,
-                                              q_codes, q_scales, k_codes, k_scales);
+    return tr ? launch_quant_qk_t<128, true>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, *tr, s)
+              : launch_quant_qk_t<128, false>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, none,
+                                              s);
+  return tr ? launch_quant_qk_t<64, true>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, *tr, s)
+            : launch_quant_qk_t<64, false>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, none, s);
+}
+
+cudaError_t launch_colsum_transform(const StridedView& k, int n, int h, int d, const RowTransform& tr,
+                                    float* partials, cudaStream_t s) {
+  const int nchunk = (n + 127) / 128;
+  const dim3 grid(nchunk, (h * (d / 8) + 127) / 128);
+  if (d == 128)
+    colsum_transform_kernel<128><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, h, tr, partials);
   else
-    quant_qk_kernel<64><<<grid, 256, 0, s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k,
-                                             q_codes, q_scales, k_codes, k_scales);
-  if (only_k) {
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dim3 gq(h, npad / 128);
-    if (d == 128)
-      quant_q_grouped_kernel<128><<<gq, 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes, q_scales);
-    else
-      quant_q_grouped_kernel<64><<<gq, 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes, q_scales);
-  }
+    colsum_transform_kernel<64><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, h, tr, partials);
   return cudaGetLastError();
 }
 

@@ -155,7 +155,34 @@ sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const s
   if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), 0.0f, qz->k_mean, s);
   if (e == cudaSuccess)
     e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), q_block_of(qz), qz->q_codes,
-                              qz->q_scales, qz->k_codes, qz->k_scales, s);
+                              qz->q_scales, qz->k_codes, qz->k_scales, nullptr, s);
+  return cuda_status(e);
+}
+
+sage_status sage_smooth_quant_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const float* gamma_q,
+                                              const float* gamma_k, const float* rope_cos, const float* rope_sin,
+                                              float eps, const sage_quantized* qz, void* ws, size_t ws_bytes,
+                                              void* stream) {
+  sage_status st;
+  if ((st = check_view(q)) != SAGE_OK || (st = check_view(k)) != SAGE_OK) return st;
+  if (!same_shape(q, k)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_qz(qz, true, false)) != SAGE_OK) return st;
+  if (!gamma_q || !gamma_k || !rope_cos || !rope_sin) return SAGE_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !(eps < INFINITY)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(gamma_q) || !aligned16(gamma_k) || !aligned16(rope_cos) || !aligned16(rope_sin))
+    return SAGE_ERR_ALIGNMENT;
+  const int64_t n = q->n_tokens, h = q->n_heads, d = q->head_dim;
+  if (!ws || !aligned16(ws)) return ws ? SAGE_ERR_ALIGNMENT : SAGE_ERR_WORKSPACE;
+  if (ws_bytes < scratch_bytes(n, h, d)) return SAGE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* part = static_cast<float*>(ws);
+  const int nchunk = static_cast<int>((n + 127) / 128);
+  const sage::RowTransform tr{gamma_q, gamma_k, rope_cos, rope_sin, eps};
+  cudaError_t e = sage::launch_colsum_transform(sv(k), int(n), int(h), int(d), tr, part, s);
+  if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), 0.0f, qz->k_mean, s);
+  if (e == cudaSuccess)
+    e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), q_block_of(qz), qz->q_codes,
+                              qz->q_scales, qz->k_codes, qz->k_scales, &tr, s);
   return cuda_status(e);
 }
 
