@@ -180,6 +180,12 @@ __global__ void __launch_bounds__(128) colsum_transform_kernel(const uint16_t* _
     for (int u = 0; u < 8; ++u)
       v[u] = (active && t + u < t1) ? ld_stream(base + static_cast<int64_t>(t + u) * st) : make_uint4(0, 0, 0, 0);
 #pragma unroll
+    for (int u = 0; u < 8; ++u) {   // the 8 tokens' cos / sin rows into L1 ahead of the transforms
+      const int64_t off = static_cast<int64_t>(min(t + u, n - 1)) * (D / 2) + c8 * 4;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_cos + off));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_sin + off));
+    }
+#pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (t + u < t1) {   // uniform over the block
         float f[8];
@@ -255,9 +261,9 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
 // codes are those of the transformed Q and K, which are never written back.
 template <int D, bool kTransform>
 // Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.  With
-// the transform, 3 CTAs per SM (80 registers, 88 bytes of spills to L1) measured fastest: 1.085 ms
-// for the fused call on the video workload, against 1.111 at 2 CTAs (127 registers, no spills)
-// and 1.097 at 4.
+// the transform, 3 CTAs per SM (80 registers, spills to L1) measured fastest: 1.085 ms for the
+// fused call on the video workload, against 1.111 at 2 CTAs (127 registers, no spills) and
+// 1.097 at 4 (before the table prefetch below).
 __global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
                                                        const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
                                                        const float* __restrict__ k_mean, int n, int npad, int only_k,
@@ -281,7 +287,17 @@ __global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const
     const int row = row0 + p * RPP + rin;
     v[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
   }
-  if (kTransform) transform_rows<D, NP, RPP>(v, is_k ? tr.gamma_k : tr.gamma_q, row0 + rin, n, c8, tr);
+  if (kTransform) {
+    // The cos / sin rows of the thread's 8 rows into L1 ahead of the transform, which would
+    // otherwise wait on them one row at a time (1.075 -> 1.014 ms for the fused call).
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const int64_t off = static_cast<int64_t>(min(row0 + p * RPP + rin, n - 1)) * (D / 2) + c8 * 4;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_cos + off));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_sin + off));
+    }
+    transform_rows<D, NP, RPP>(v, is_k ? tr.gamma_k : tr.gamma_q, row0 + rin, n, c8, tr);
+  }
   float mu[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mu[j] = is_k ? k_mean[hh * D + c8 * 8 + j] : 0.0f;
