@@ -4,6 +4,7 @@ launching anything (these calls never reach the GPU)."""
 import ctypes
 
 import pytest
+import torch
 
 import video_diffusion_transformer_sage_gb300 as sage
 from video_diffusion_transformer_sage_gb300 import _lib
@@ -127,3 +128,19 @@ def test_argument_validation_never_launches(L):
     assert L.sage_check_device_status(0, None, None) == 1
     assert L.sage_debug_wait_timeout(0, 1000, None) == 1
     assert L.sage_debug_wait_timeout(4096, 0, None) == 1
+
+
+def test_binding_validates_options_before_allocating():
+    """The Python binding rejects unknown options itself (no device memory is touched)."""
+    with pytest.raises(ValueError):
+        sage.Quantized(256, 2, 128, device="cpu", v_format="fp4")
+    with pytest.raises(ValueError):
+        sage.Quantized(256, 2, 128, device="cpu", q_block=96)
+    qz = sage.Quantized(256, 2, 128, device="cpu", v_format="int8", smooth_v=True)
+    assert qz.v_codes.dtype == torch.float16 and tuple(qz.v_codes.shape) == (2, 128, 256)
+    assert qz.v_mean is not None and tuple(qz.v_mean.shape) == (2, 128)
+    c = qz.c()
+    assert c.v_format == 1 and c.v_mean == qz.v_mean.data_ptr() and c.q_block == 128
+    c0 = sage.Quantized(256, 2, 128, device="cpu").c()
+    assert c0.v_format == 0 and c0.v_mean is None
+    assert ctypes.sizeof(_lib.SageQuantizedC) == 8 * 10          # the header's struct: 10 eight-byte fields
