@@ -374,3 +374,21 @@ def test_v_smoothing_lowers_error_on_offset_v():
     e_plain = np.linalg.norm(plain[sel].double().cpu().numpy() - ex) / centred
     e_smooth = np.linalg.norm(smooth[sel].double().cpu().numpy() - ex) / centred
     assert e_smooth < 0.5 * e_plain, (e_smooth, e_plain)
+
+
+@pytest.mark.parametrize("v_format,smooth", [("int8", True), ("e4m3", True)])
+def test_v_options_with_row_q_scales(v_format, smooth):
+    """The V options combined with Q scales per 32 rows (the per-row Q lookup instantiations)."""
+    case = gpu_case("tails_voff")
+    n, h, d = case["q"].shape
+    sm = 1.0 / math.sqrt(d)
+    qz = sage.sage_smooth_quant_qk(case["q"], case["k"], q_block=32, v_format=v_format, smooth_v=smooth)
+    sage.sage_quant_v(case["v"], qz)
+    status = sage.status_block()
+    out = sage.sage_attn_fwd_quantized(qz, sm, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    inp = case["inp"]
+    oz = oracle.Quantized(inp.q, inp.k, inp.v, q_block=32, v_format=v_format, smooth_v=smooth)
+    sel = synth.sample_rows(n, 512, 29)
+    ok, info = _close_to_oracle(out[sel].float().cpu().numpy().astype(np.float64), oracle.attn_sq(oz, sm, sel, tile=128))
+    assert ok, info
