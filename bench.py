@@ -106,14 +106,22 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
+def attn_kernel_code_sha256(path: str = ATTN_SRC) -> str:
+    """sha256 of the kernel code of attn_fwd.cu: the text from `namespace sage {` to the
+    host-side marker (device code; the includes and the host launch code are left out)."""
+    text = open(path, encoding="utf-8").read()
+    i0 = text.index("namespace sage {")
+    i1 = text.index("// --------------------------------------------------------------------------- host side")
+    return hashlib.sha256(text[i0:i1].encode()).hexdigest()
+
+
 def _traffic_per_launch():
     """dram bytes per launch of the attention kernel from the committed ncu capture, or None
-    when the kernel source changed since the capture."""
+    when the kernel code changed since the capture."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        src = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()
-        if t.get("attn_fwd_cu_sha256") != src:
+        if t.get("attn_kernel_code_sha256") != attn_kernel_code_sha256():
             return None
         return t["bytes_per_launch_full_size"]
     except Exception:

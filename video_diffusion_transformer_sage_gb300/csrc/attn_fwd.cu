@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -626,12 +627,18 @@ template <int D, bool kRowQ, bool kPv16, bool kMean>
 cudaError_t launch_variant(dim3 grid, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const AttnParams& p, cudaStream_t s) {
   constexpr int kSmem = Cfg<D, kPv16>::kSmemBytes;
-  static bool attr_set = false;   // per instantiation
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kRowQ, kPv16, kMean>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  // The shared-memory limit is a per-device attribute of the function: set it once on each
+  // device (bit d of the mask), and on every call for device numbers past 63.
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kRowQ, kPv16, kMean>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(bit, std::memory_order_acq_rel);
   }
   attn_fwd_kernel<D, kRowQ, kPv16, kMean><<<grid, 384, kSmem, s>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
