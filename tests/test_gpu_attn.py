@@ -392,3 +392,25 @@ def test_v_options_with_row_q_scales(v_format, smooth):
     sel = synth.sample_rows(n, 512, 29)
     ok, info = _close_to_oracle(out[sel].float().cpu().numpy().astype(np.float64), oracle.attn_sq(oz, sm, sel, tile=128))
     assert ok, info
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("v_format,smooth", [("e4m3", False), ("int8", False), ("e4m3", True), ("int8", True)])
+def test_single_token_all_options(d, v_format, smooth):
+    """N = 1: each row attends to itself alone, so O = V.  Smoothed, V - mean = 0 (scale 0,
+    codes 0) and the epilogue's mean is V exactly: the bf16 output equals V bit for bit."""
+    inp = synth.make_inputs(synth.custom(1, 2, d, "qkv", seed=31, n_outlier=0))
+    st = inp.storage.cuda()
+    hd = 2 * d
+    q, k, v = (st[:, i * hd:(i + 1) * hd].view(1, 2, d) for i in range(3))
+    qz = sage.sage_smooth_quant_qk(q, k, v_format=v_format, smooth_v=smooth)
+    sage.sage_quant_v(v, qz)
+    status = sage.status_block()
+    out = sage.sage_attn_fwd_quantized(qz, 0.1, status=status)
+    assert sage.sage_check_device_status(status) == (0, 0)
+    if smooth:
+        assert torch.equal(out.cpu().view(torch.int16), inp.v.contiguous().view(torch.int16))
+    oz = oracle.Quantized(inp.q, inp.k, inp.v, v_format=v_format, smooth_v=smooth)
+    ref = oracle.attn_sq(oz, 0.1, [0], tile=128)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref).max() <= 2.0 ** -8 * np.abs(ref).max()
