@@ -24,7 +24,8 @@ _lock = threading.Lock()
 
 MUTATIONS = {"none": 0, "no_smooth": 1, "rescale_sign": 2, "scale_255": 3, "key_index": 4,
              "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8,
-             "q_block_index": 9, "rope_sign": 10, "rms_sum": 11, "v_mean_sign": 12, "p_i8_255": 13}
+             "q_block_index": 9, "rope_sign": 10, "rms_sum": 11, "v_mean_sign": 12, "p_i8_255": 13,
+             "v_i8_448": 14}
 
 Q_BLOCKS = (1, 2, 4, 8, 16, 32, 64, 128)
 V_FORMATS = {"e4m3": 0, "int8": 1}

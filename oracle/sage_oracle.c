@@ -44,7 +44,7 @@
 enum { MUT_NONE = 0, MUT_NO_SMOOTH = 1, MUT_RESCALE_SIGN = 2, MUT_SCALE_255 = 3,
        MUT_KEY_INDEX = 4, MUT_V_SCALE_CHANNEL = 5, MUT_DROP_LAST_KEY = 6,
        MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8, MUT_Q_BLOCK_INDEX = 9, MUT_ROPE_SIGN = 10,
-       MUT_RMS_SUM = 11, MUT_V_MEAN_SIGN = 12, MUT_P_I8_255 = 13 };
+       MUT_RMS_SUM = 11, MUT_V_MEAN_SIGN = 12, MUT_P_I8_255 = 13, MUT_V_I8_448 = 14 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
 
@@ -243,7 +243,7 @@ void oracle_quant_v_fmt(const uint16_t* v, int64_t n, int64_t h, int64_t d, int6
         float a = fabsf(bf16_to_f32(v[t * st + hh * sh + c]) - m);
         if (a > amax) amax = a;
       }
-      float scale = fmt ? amax / 127.0f : amax / 448.0f;
+      float scale = fmt ? amax / (g_mutation == MUT_V_I8_448 ? 448.0f : 127.0f) : amax / 448.0f;
       scales[hh * d + c] = scale;
       if (scale == 0.0f) continue;
       for (int64_t t = 0; t < n; ++t) {
