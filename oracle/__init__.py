@@ -25,7 +25,8 @@ _lock = threading.Lock()
 MUTATIONS = {"none": 0, "no_smooth": 1, "rescale_sign": 2, "scale_255": 3, "key_index": 4,
              "v_scale_channel": 5, "drop_last_key": 6, "e4m3_trunc": 7, "mean_n_pad": 8,
              "q_block_index": 9, "rope_sign": 10, "rms_sum": 11, "v_mean_sign": 12, "p_i8_255": 13,
-             "v_i8_448": 14}
+             "v_i8_448": 14, "f32_half_scale": 15, "f32_kscale_tile": 16, "f32_l_codes": 17,
+             "f32_exp_base": 18}
 
 Q_BLOCKS = (1, 2, 4, 8, 16, 32, 64, 128)
 V_FORMATS = {"e4m3": 0, "int8": 1}
@@ -62,6 +63,8 @@ def lib():
             L.oracle_quant_v.argtypes = [P, I, I, I, I, I, P, P]
             L.oracle_quant_v_fmt.argtypes = [P, I, I, I, I, I, P, I, P, P]
             L.oracle_attn_sq_v.argtypes = [P, P, I, P, P, P, P, P, I, I, I, I, ctypes.c_double, P, I, I, I, P]
+            L.oracle_attn_sq_trace.argtypes = [P, P, I, P, P, P, P, P, I, I, I, ctypes.c_double, I, P, I, I, I,
+                                               P, P, P, P]
             L.oracle_qk_int32.argtypes = [P, P, I, I, I, I, I, I, I, I, P]
             L.oracle_attn_sq.argtypes = [P, P, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
             L.oracle_attn_sq_blk.argtypes = [P, P, I, P, P, P, P, I, I, I, ctypes.c_double, P, I, I, I, P]
@@ -206,6 +209,25 @@ def attn_sq(qz: Quantized, sm_scale: float, rows, tile: int = 128, score_f32=Non
                            qz.n, qz.h, qz.d, float(sm_scale), _ptr(rows), len(rows), int(tile),
                            int(bool(score_f32)), _ptr(out))
     return out
+
+
+def attn_sq_trace(qz: Quantized, sm_scale: float, head: int, rows, tile: int = 128, score_f32: bool = True):
+    """attn_sq for query `rows` of one head, with each key's trace: returns (out [R, D], pp [R, N],
+    p8 [R, N], lw [R, N]).  pp[r, j] is the 448 p (127 p for INT8 P) whose code P takes, p8 the value
+    of that code, lw the running max key j's p is relative to, as a base-2 exponent: key j enters
+    the final sums with weight 2^(lw[r, j] - lw[r, N-1])."""
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    r, n, d = len(rows), qz.n, qz.d
+    out = np.zeros((r, d), np.float64)
+    pp, p8, lw = (np.zeros((r, n), np.float64) for _ in range(3))
+    v_mean = getattr(qz, "v_mean", None)
+    mu = None if v_mean is None else np.ascontiguousarray(v_mean, dtype=np.float32)
+    lib().oracle_attn_sq_trace(_ptr(qz.q_codes), _ptr(qz.q_scales), int(getattr(qz, "q_block", 128)),
+                               _ptr(qz.k_codes), _ptr(qz.k_scales), _ptr(qz.v_codes), _ptr(qz.v_scales),
+                               None if mu is None else _ptr(mu), V_FORMATS[getattr(qz, "v_format", "e4m3")],
+                               n, d, float(sm_scale), int(head), _ptr(rows), r, int(tile), int(bool(score_f32)),
+                               _ptr(out), _ptr(pp), _ptr(p8), _ptr(lw))
+    return out, pp, p8, lw
 
 
 def attn_exact(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_scale: float, rows) -> np.ndarray:

@@ -44,7 +44,8 @@
 enum { MUT_NONE = 0, MUT_NO_SMOOTH = 1, MUT_RESCALE_SIGN = 2, MUT_SCALE_255 = 3,
        MUT_KEY_INDEX = 4, MUT_V_SCALE_CHANNEL = 5, MUT_DROP_LAST_KEY = 6,
        MUT_E4M3_TRUNC = 7, MUT_MEAN_N_PAD = 8, MUT_Q_BLOCK_INDEX = 9, MUT_ROPE_SIGN = 10,
-       MUT_RMS_SUM = 11, MUT_V_MEAN_SIGN = 12, MUT_P_I8_255 = 13, MUT_V_I8_448 = 14 };
+       MUT_RMS_SUM = 11, MUT_V_MEAN_SIGN = 12, MUT_P_I8_255 = 13, MUT_V_I8_448 = 14,
+       MUT_F32_HALF_SCALE = 15, MUT_F32_KSCALE_TILE = 16, MUT_F32_L_CODES = 17, MUT_F32_EXP_BASE = 18 };
 static int g_mutation = 0;
 void oracle_set_mutation(int m) { g_mutation = m; }
 
@@ -315,102 +316,135 @@ static double p_code(double pp, int64_t vfmt) {
   return rint(g_mutation == MUT_P_I8_255 ? pp * (255.0 / 127.0) : pp);
 }
 
-void oracle_attn_sq_v(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
-                      const uint8_t* vc, const float* vs, const float* vmu, int64_t vfmt, int64_t n,
-                      int64_t h, int64_t d, double sm_scale, const int64_t* rows, int64_t nrows,
-                      int64_t tile, int64_t score_f32, double* out) {
+/* One (query row i, head hh) of the same-quantisation attention described above, written to
+ * o[0..d).  When tr_pp is not NULL, each key j < n also leaves a trace: tr_pp[j] = the 448 p
+ * (127 p) whose code P takes, tr_p8[j] = the value of that code, tr_lw[j] = the running max that
+ * key's p is relative to, as a base-2 exponent (so the weight key j carries in the final sums is
+ * 2^(tr_lw[j] - tr_lw[n-1])).  Keys the row does not visit keep pp = p8 = 0. */
+static void attn_row(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
+                     const uint8_t* vc, const float* vs, const float* vmu, int64_t vfmt, int64_t n,
+                     int64_t d, double sm_scale, int64_t i, int64_t hh, int64_t tile, int64_t score_f32,
+                     double* o, double* tr_pp, double* tr_p8, double* tr_lw) {
   int64_t np = pad128(n), nbq = np / qb, nbk = np / 64;
   int64_t nkeys = (g_mutation == MUT_DROP_LAST_KEY) ? n - 1 : n;
   const float kLog2E = 1.4426950408889634f;
   /* log2 of P's static scale: log2(448) for E4M3 P, log2(127) for INT8 P */
   const float kLog2P = vfmt ? 6.988684686772166f : 8.807354922057604f;
   const double pscale = vfmt ? 127.0 : 448.0;
-#pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t rh = 0; rh < nrows * h; ++rh) {
-    int64_t r = rh / h, hh = rh % h, i = rows[r];
-    double* o = (double*)calloc((size_t)d, sizeof(double));
-    double* s = (double*)malloc(sizeof(double) * (size_t)n);
-    int64_t* S = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
-    const int8_t* a = qc + (hh * np + i) * d;
-    /* the Q block of row i (the planted mistake reads the 128-row block's index instead) */
-    const int64_t qbi = (g_mutation == MUT_Q_BLOCK_INDEX) ? i / 128 : i / qb;
-    double sq = (double)qs[hh * nbq + qbi];
-    for (int64_t j = 0; j < nkeys; ++j) {
-      int64_t jj = (g_mutation == MUT_KEY_INDEX) ? (j ^ 1) % n : j;
-      const int8_t* b = kc + (hh * np + jj) * d;
-      int64_t acc = 0;
-      for (int64_t c = 0; c < d; ++c) acc += (int64_t)a[c] * (int64_t)b[c];
-      S[j] = acc;
-      s[j] = (double)acc * sq * (double)ks[hh * nbk + j / 64] * sm_scale;
-    }
-    double m = -INFINITY, l = 0.0;
-    float mf = -INFINITY;
-    int64_t tw = tile > 0 ? tile : nkeys;
-    if (tile <= 0)
-      for (int64_t j = 0; j < nkeys; ++j) if (s[j] > m) m = s[j];
-    const float cq = qs[hh * nbq + qbi] * ((float)sm_scale * kLog2E);
-    for (int64_t j0 = 0; j0 < nkeys; j0 += tw) {
-      int64_t j1 = j0 + tw < nkeys ? j0 + tw : nkeys;
-      if (tile > 0 && score_f32) {
-        float mt = -INFINITY;
-        for (int64_t h0 = j0; h0 < j1; h0 += 64) {       /* 64-key halves, one K scale each */
-          int64_t h1 = h0 + 64 < j1 ? h0 + 64 : j1;
-          float mx = -INFINITY;
-          for (int64_t j = h0; j < h1; ++j) if ((float)S[j] > mx) mx = (float)S[j];
-          float cb = cq * ks[hh * nbk + h0 / 64];
-          float v = cb * mx;
-          if (v > mt) mt = v;
-        }
-        if (mt > mf) {
-          if (mf != -INFINITY) {
-            float dm = (g_mutation == MUT_RESCALE_SIGN) ? mt - mf : mf - mt;
-            double alpha = exp2((double)dm);
-            for (int64_t c = 0; c < d; ++c) o[c] *= alpha;
-            l *= alpha;
-          }
-          mf = mt;
-        }
-        const float bias = kLog2P - mf;
-        for (int64_t j = j0; j < j1; ++j) {
-          float cb = cq * ks[hh * nbk + j / 64];
-          float x = fmaf((float)S[j], cb, bias);
-          float pp = (float)exp2((double)x);             /* 448 p or 127 p, rounded to fp32 */
-          l += (double)pp;
-          double p8 = p_code((double)pp, vfmt);
-          if (p8 == 0.0) continue;
-          for (int64_t c = 0; c < d; ++c) o[c] += p8 * v_value(vc[(hh * d + c) * np + j], vfmt);
-        }
-        continue;
+  const double log2e = 1.4426950408889634;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  int64_t* S = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+  const int8_t* a = qc + (hh * np + i) * d;
+  /* the Q block of row i (the planted mistake reads the 128-row block's index instead) */
+  const int64_t qbi = (g_mutation == MUT_Q_BLOCK_INDEX) ? i / 128 : i / qb;
+  double sq = (double)qs[hh * nbq + qbi];
+  for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+  if (tr_pp)
+    for (int64_t j = 0; j < n; ++j) tr_pp[j] = tr_p8[j] = tr_lw[j] = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    int64_t jj = (g_mutation == MUT_KEY_INDEX) ? (j ^ 1) % n : j;
+    const int8_t* b = kc + (hh * np + jj) * d;
+    int64_t acc = 0;
+    for (int64_t c = 0; c < d; ++c) acc += (int64_t)a[c] * (int64_t)b[c];
+    S[j] = acc;
+    s[j] = (double)acc * sq * (double)ks[hh * nbk + j / 64] * sm_scale;
+  }
+  double m = -INFINITY, l = 0.0;
+  float mf = -INFINITY;
+  int64_t tw = tile > 0 ? tile : nkeys;
+  if (tile <= 0)
+    for (int64_t j = 0; j < nkeys; ++j) if (s[j] > m) m = s[j];
+  const float cq = qs[hh * nbq + qbi] * ((float)sm_scale * kLog2E);
+  for (int64_t j0 = 0; j0 < nkeys; j0 += tw) {
+    int64_t j1 = j0 + tw < nkeys ? j0 + tw : nkeys;
+    if (tile > 0 && score_f32) {
+      float mt = -INFINITY;
+      for (int64_t h0 = j0; h0 < j1; h0 += 64) {       /* 64-key halves, one K scale each */
+        int64_t h1 = h0 + 64 < j1 ? h0 + 64 : j1;
+        float mx = -INFINITY;
+        for (int64_t j = h0; j < h1; ++j) if ((float)S[j] > mx) mx = (float)S[j];
+        int64_t kb = h0 / 64;
+        if (g_mutation == MUT_F32_HALF_SCALE && (kb ^ 1) < nbk) kb ^= 1;
+        float cb = cq * ks[hh * nbk + kb];
+        float v = cb * mx;
+        if (v > mt) mt = v;
       }
-      if (tile > 0) {
-        double mt = -INFINITY;
-        for (int64_t j = j0; j < j1; ++j) if (s[j] > mt) mt = s[j];
-        if (mt > m) {
-          if (m != -INFINITY) {
-            double alpha = (g_mutation == MUT_RESCALE_SIGN) ? exp(mt - m) : exp(m - mt);
-            for (int64_t c = 0; c < d; ++c) o[c] *= alpha;
-            l *= alpha;
-          }
-          m = mt;
+      if (mt > mf) {
+        if (mf != -INFINITY) {
+          float dm = (g_mutation == MUT_RESCALE_SIGN) ? mt - mf : mf - mt;
+          double alpha = exp2((double)dm);
+          for (int64_t c = 0; c < d; ++c) o[c] *= alpha;
+          l *= alpha;
         }
+        mf = mt;
       }
+      const float bias = kLog2P - mf;
       for (int64_t j = j0; j < j1; ++j) {
-        double p = exp(s[j] - m);
-        l += pscale * p;
-        double p8 = p_code(pscale * p, vfmt);
+        int64_t kb = (g_mutation == MUT_F32_KSCALE_TILE) ? j0 / 64 : j / 64;
+        float cb = cq * ks[hh * nbk + kb];
+        float x = fmaf((float)S[j], cb, bias);
+        /* 448 p or 127 p, rounded to fp32 (the planted mistake takes e^x for 2^x) */
+        float pp = (g_mutation == MUT_F32_EXP_BASE) ? (float)exp((double)x) : (float)exp2((double)x);
+        double p8 = p_code((double)pp, vfmt);
+        l += (g_mutation == MUT_F32_L_CODES) ? p8 : (double)pp;
+        if (tr_pp) { tr_pp[j] = (double)pp; tr_p8[j] = p8; tr_lw[j] = (double)mf; }
         if (p8 == 0.0) continue;
         for (int64_t c = 0; c < d; ++c) o[c] += p8 * v_value(vc[(hh * d + c) * np + j], vfmt);
       }
+      continue;
     }
-    for (int64_t c = 0; c < d; ++c) {
-      double mean = 0.0;
-      if (vmu) mean = (g_mutation == MUT_V_MEAN_SIGN) ? -(double)vmu[hh * d + c] : (double)vmu[hh * d + c];
-      out[(r * h + hh) * d + c] = o[c] * (double)vs[hh * d + c] / l + mean;
+    if (tile > 0) {
+      double mt = -INFINITY;
+      for (int64_t j = j0; j < j1; ++j) if (s[j] > mt) mt = s[j];
+      if (mt > m) {
+        if (m != -INFINITY) {
+          double alpha = (g_mutation == MUT_RESCALE_SIGN) ? exp(mt - m) : exp(m - mt);
+          for (int64_t c = 0; c < d; ++c) o[c] *= alpha;
+          l *= alpha;
+        }
+        m = mt;
+      }
     }
-    free(o);
-    free(s);
-    free(S);
+    for (int64_t j = j0; j < j1; ++j) {
+      double p = exp(s[j] - m);
+      l += pscale * p;
+      double p8 = p_code(pscale * p, vfmt);
+      if (tr_pp) { tr_pp[j] = pscale * p; tr_p8[j] = p8; tr_lw[j] = m * log2e; }
+      if (p8 == 0.0) continue;
+      for (int64_t c = 0; c < d; ++c) o[c] += p8 * v_value(vc[(hh * d + c) * np + j], vfmt);
+    }
   }
+  for (int64_t c = 0; c < d; ++c) {
+    double mean = 0.0;
+    if (vmu) mean = (g_mutation == MUT_V_MEAN_SIGN) ? -(double)vmu[hh * d + c] : (double)vmu[hh * d + c];
+    o[c] = o[c] * (double)vs[hh * d + c] / l + mean;
+  }
+  free(s);
+  free(S);
+}
+
+void oracle_attn_sq_v(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
+                      const uint8_t* vc, const float* vs, const float* vmu, int64_t vfmt, int64_t n,
+                      int64_t h, int64_t d, double sm_scale, const int64_t* rows, int64_t nrows,
+                      int64_t tile, int64_t score_f32, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t rh = 0; rh < nrows * h; ++rh) {
+    int64_t r = rh / h, hh = rh % h;
+    attn_row(qc, qs, qb, kc, ks, vc, vs, vmu, vfmt, n, d, sm_scale, rows[r], hh, tile, score_f32,
+             out + (r * h + hh) * d, NULL, NULL, NULL);
+  }
+}
+
+/* The same computation for query `rows` of one head, with each key's trace (see attn_row):
+ * out [nrows][d], pp / p8 / lw [nrows][n]. */
+void oracle_attn_sq_trace(const int8_t* qc, const float* qs, int64_t qb, const int8_t* kc, const float* ks,
+                          const uint8_t* vc, const float* vs, const float* vmu, int64_t vfmt, int64_t n,
+                          int64_t d, double sm_scale, int64_t head, const int64_t* rows, int64_t nrows,
+                          int64_t tile, int64_t score_f32, double* out, double* pp, double* p8, double* lw) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < nrows; ++r)
+    attn_row(qc, qs, qb, kc, ks, vc, vs, vmu, vfmt, n, d, sm_scale, rows[r], head, tile, score_f32,
+             out + r * d, pp + r * n, p8 + r * n, lw + r * n);
 }
 
 /* E4M3 V as in oracle_quant_v (Q and K scales per qb-row / 64-row block as above). */
