@@ -152,12 +152,16 @@ sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const s
  *     is allocated: no cudaMalloc, no cudaFree, no allocating library call.
  *   - Limit: ceil(n_tokens / 128) * n_heads * head_dim <= 4,194,304 (the pages' call uses
  *     2,121,728).  Larger problems return SAGE_ERR_WORKSPACE and nothing is launched.
- *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture begins.
+ *   - Each call looks up the array's device address with the caller's device current (a
+ *     host-side query that does not synchronise), so the address stays right after a device
+ *     reset.  The first call in a process may load the library's device code: make the first
+ *     call on each device before any stream capture begins.
  *   - Every call on a device uses the same array, so calls that can overlap on the GPU (other
  *     streams, other host threads) race: serialise them.  No element needs to start at zero:
  *     each call writes every scratch element it reads.
- * Errors and argument checks as for sage_smooth_quant_qk. */
+ * Errors: the argument checks of sage_smooth_quant_qk come first and give the same statuses
+ * (e.g. SAGE_ERR_UNSUPPORTED for n_tokens > 2^22); then the limit above (SAGE_ERR_WORKSPACE);
+ * SAGE_ERR_CUDA if the address lookup or a launch fails. */
 sage_status sage_smooth_quant_qk_noalloc(const sage_view* q, const sage_view* k, const sage_quantized* qz,
                                          void* stream);
 

@@ -54,7 +54,17 @@ def test_noalloc_matches_allocating_entry_point(name):
 def test_noalloc_rejects_oversize_before_launch():
     build.build()
     L = _lib.lib()
-    # ceil(75620/128) * 56 * 128 = 4,236,288 floats > 4,194,304: refused, nothing launched
-    v = _lib.SageView(16, 75620, 56, 128, 3 * 56 * 128, 128)
     qz = _lib.SageQuantizedC(*([4096] * 7))
-    assert L.sage_smooth_quant_qk_noalloc(ctypes.byref(v), ctypes.byref(v), ctypes.byref(qz), None) == 4
+
+    def call(n, h, d):
+        v = _lib.SageView(16, n, h, d, 3 * h * d, d)
+        return L.sage_smooth_quant_qk_noalloc(ctypes.byref(v), ctypes.byref(v), ctypes.byref(qz), None)
+
+    # ceil(75620/128) * 56 * 128 = 4,236,288 floats > 4,194,304: refused, nothing launched
+    assert call(75620, 56, 128) == 4                       # SAGE_ERR_WORKSPACE
+    # beyond what sage_smooth_quant_qk accepts at all: its own status comes first
+    assert call((1 << 22) + 1, 1, 64) == 3                 # SAGE_ERR_UNSUPPORTED, not WORKSPACE
+    assert call(128, 1, 96) == 3                           # unsupported head dim
+    misaligned = _lib.SageQuantizedC(*([4096 + 4] + [4096] * 6))
+    v = _lib.SageView(16, 1024, 2, 128, 3 * 256, 128)
+    assert L.sage_smooth_quant_qk_noalloc(ctypes.byref(v), ctypes.byref(v), ctypes.byref(misaligned), None) == 2

@@ -13,8 +13,6 @@
 // size bounds the problem: ceil(N / 128) * H * D <= kNoAllocScratchFloats.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "sage_internal.h"
 
 namespace {
@@ -26,23 +24,6 @@ constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;
 // same call, so nothing needs clearing between calls.
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-float* g_scratch_ptr[kMaxDevices] = {};
-cudaError_t g_setup_err[kMaxDevices] = {};
-
-// The host-side name g_noalloc_scratch is not a device address; the kernels must be given the
-// address cudaGetSymbolAddress returns, looked up once per device with that device current.
-float* device_scratch(int dev, cudaError_t* err) {
-  std::call_once(g_once[dev], [dev] {
-    void* p = nullptr;
-    g_setup_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    g_scratch_ptr[dev] = g_setup_err[dev] == cudaSuccess ? static_cast<float*>(p) : nullptr;
-  });
-  *err = g_setup_err[dev];
-  return g_scratch_ptr[dev];
-}
-
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -51,24 +32,25 @@ extern "C" {
 
 sage_status sage_smooth_quant_qk_noalloc(const sage_view* q, const sage_view* k, const sage_quantized* qz,
                                          void* stream) {
-  if (!q || !k || !qz || !q->data || !k->data) return SAGE_ERR_INVALID_ARG;
+  // The argument checks of sage_smooth_quant_qk first, so a bad view or shape gets the same
+  // status from both entry points; then the limit of the fixed array, before touching the device.
+  sage_status st = sage::check_smooth_quant_qk_args(q, k, qz);
+  if (st != SAGE_OK) return st;
   const int64_t n = q->n_tokens, h = q->n_heads, d = q->head_dim;
-  if (n <= 0 || h <= 0 || d <= 0) return SAGE_ERR_INVALID_ARG;
-  if (k->n_tokens != n || k->n_heads != h || k->head_dim != d) return SAGE_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return SAGE_ERR_UNSUPPORTED;
-  // Beyond the fixed array: refuse before touching the device.
   if (static_cast<size_t>((n + 127) / 128) * static_cast<size_t>(h) * static_cast<size_t>(d) >
       kNoAllocScratchFloats)
     return SAGE_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SAGE_ERR_CUDA;
-  cudaError_t e = cudaSuccess;
-  float* scratch = device_scratch(dev, &e);
-  if (e != cudaSuccess || !scratch) return SAGE_ERR_CUDA;
-  if (!aligned16(scratch)) return SAGE_ERR_ALIGNMENT;
-  // The argument checks and the three launches of sage_smooth_quant_qk, with the scratch
-  // pointer above in place of a caller workspace.
-  return sage_smooth_quant_qk(q, k, qz, scratch, kNoAllocScratchFloats * sizeof(float), stream);
+  // The host-side name g_noalloc_scratch is not a device address: the kernels get the address
+  // cudaGetSymbolAddress returns with the caller's device current.  It is looked up on every
+  // call (a host-side query that does not synchronise), so a pointer from an earlier context --
+  // before a cudaDeviceReset, say -- is never reused, and a failed lookup is not remembered.
+  // The first call in a process may load the library's device code: make it before any stream
+  // capture on that device.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SAGE_ERR_CUDA;
+  if (!aligned16(p)) return SAGE_ERR_ALIGNMENT;
+  // The three launches of sage_smooth_quant_qk, with the array in place of a caller workspace.
+  return sage_smooth_quant_qk(q, k, qz, p, kNoAllocScratchFloats * sizeof(float), stream);
 }
 
 }  // extern "C"

@@ -112,6 +112,15 @@ Carve carve(void* base, int64_t n, int64_t h, int64_t d) {
 
 }  // namespace
 
+namespace sage {
+sage_status check_smooth_quant_qk_args(const sage_view* q, const sage_view* k, const sage_quantized* qz) {
+  sage_status st;
+  if ((st = check_view(q)) != SAGE_OK || (st = check_view(k)) != SAGE_OK) return st;
+  if (!same_shape(q, k)) return SAGE_ERR_INVALID_ARG;
+  return check_qz(qz, true, false);
+}
+}  // namespace sage
+
 extern "C" {
 
 const char* sage_status_string(sage_status status) {
@@ -142,9 +151,7 @@ size_t sage_status_block_bytes(void) { return kStatusBytes; }
 sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const sage_quantized* qz, void* ws,
                                  size_t ws_bytes, void* stream) {
   sage_status st;
-  if ((st = check_view(q)) != SAGE_OK || (st = check_view(k)) != SAGE_OK) return st;
-  if (!same_shape(q, k)) return SAGE_ERR_INVALID_ARG;
-  if ((st = check_qz(qz, true, false)) != SAGE_OK) return st;
+  if ((st = sage::check_smooth_quant_qk_args(q, k, qz)) != SAGE_OK) return st;
   const int64_t n = q->n_tokens, h = q->n_heads, d = q->head_dim;
   if (!ws || !aligned16(ws)) return ws ? SAGE_ERR_ALIGNMENT : SAGE_ERR_WORKSPACE;
   if (ws_bytes < scratch_bytes(n, h, d)) return SAGE_ERR_WORKSPACE;

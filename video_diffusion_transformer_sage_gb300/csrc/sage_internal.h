@@ -29,6 +29,10 @@ struct StridedView {
 
 inline int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
 
+// sage_api.cu: the argument checks of sage_smooth_quant_qk (views, shapes, output buffers),
+// everything but the workspace.
+sage_status check_smooth_quant_qk_args(const sage_view* q, const sage_view* k, const sage_quantized* qz);
+
 // quant.cu
 // Per-128-token column partials: sums, or maxima of |x| (of |fl32(x - mean)| when mean is set).
 cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, const float* mean,
