@@ -409,6 +409,11 @@ def run_gpu(args):
                                "step_ms": round(v_quant + v_attn, 3)}
             del vz
 
+    # ---- the measured tensor-core ceiling of the attention kernel's instructions (outside the
+    # timed region): one CTA per SM issuing each MMA shape back to back on resident operands
+    # (sage_measure_mma_rate), 1 warm-up launch, then 3 timed launches per mode with CUDA events.
+    mma_ceiling = None if args.no_mma_ceiling else mma_rates(sage, dev, stream, status)
+
     bf16_burst, bf16_sus, hbm, peak_src = _peaks()
     if qk_transform is not None:
         qk_transform["hbm_frac"] = round(qk_transform["gbs"] / hbm, 4)
@@ -459,7 +464,11 @@ def run_gpu(args):
                                    f"composite of the {peak_src} {'burst' if full_clock else 'sustained'} bf16 "
                                    f"{p16} TFLOP/s (QK^T, fp16 operands) and 2x that for E4M3 (PV)"),
                      "frac_of_e4m3_peak": round(achieved / p8, 4),
-                     "frac_of_bf16_peak": round(achieved / p16, 4)},
+                     "frac_of_bf16_peak": round(achieved / p16, 4),
+                     "frac_of_mma_ceiling": (round(achieved / mma_ceiling["tflops"][
+                         "qk_pv_tile_mix" if args.v_format == "e4m3" else "qk_f16_128x128x16"], 4)
+                                             if mma_ceiling else None)},
+        "mma_ceiling": mma_ceiling,
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
                        "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
                        "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},
@@ -484,6 +493,36 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+MMA_MODES = {0: "qk_f16_128x128x16", 1: "pv_e4m3_tmemA_128x128x32", 2: "qk_pv_tile_mix",
+             3: "e4m3_ss_128x256x32", 4: "f16_ss_128x256x16"}
+# rounds per launch: about 20 ms each at the nominal per-SM rates (8192 fp16 / 16384 E4M3 FLOP per clock)
+MMA_ITERS = {0: 640000, 1: 640000, 2: 54000, 3: 320000, 4: 320000}
+
+
+def mma_rates(sage, dev, stream, status):
+    """TFLOP/s of each sage_measure_mma_rate mode with one CTA per SM."""
+    import torch
+    from video_diffusion_transformer_sage_gb300 import _lib
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for mode, name in MMA_MODES.items():
+        sage.sage_measure_mma_rate(mode, MMA_ITERS[mode] // 10, sms, status, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+        torch.cuda.synchronize()
+        for a_, b_ in ev:
+            a_.record(stream)
+            sage.sage_measure_mma_rate(mode, MMA_ITERS[mode], sms, status, stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        ms = min(a_.elapsed_time(b_) for a_, b_ in ev)
+        out[name] = round(_lib.MMA_RATE_FLOPS[mode] * MMA_ITERS[mode] * sms / (ms * 1e-3) / 1e12, 1)
+    code, where = sage.sage_check_device_status(status, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at {where} (MMA rate)")
+    return {"tflops": out, "ctas": sms, "how": "one CTA per SM issuing each tcgen05.mma shape back to back on "
+            "resident zero operands (sage_measure_mma_rate); best of 3 launches of ~20 ms"}
 
 
 def _pct(xs, q):
@@ -582,6 +621,8 @@ def main():
                     help="skip the timing of the INT8 P.V variant and of V smoothing")
     ap.add_argument("--no-qk-transform", action="store_true",
                     help="skip the timing of the in-place RMSNorm + rotary stage")
+    ap.add_argument("--no-mma-ceiling", action="store_true",
+                    help="skip the measurement of the tensor-core rate of the kernel's MMA shapes")
     ap.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS with qkv layout")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -258,6 +258,20 @@ sage_status sage_debug_qk_int32(int64_t n_tokens, int64_t n_heads, int64_t head_
  * hangs.  Read the result with sage_check_device_status. */
 sage_status sage_debug_wait_timeout(void* status_block, int64_t limit_ns, void* stream);
 
+/* Measurement hook: the tensor-core rate of the MMA instructions the fused attention issues,
+ * i.e. the ceiling its roofline is read against.  `ctas` CTAs (one per SM: 128 threads, 512 TMEM
+ * columns, ~49 KB shared memory) each issue `iters` rounds of `mode` back to back on zero operands
+ * and wait for the last; the caller times the call (e.g. CUDA events on `stream`).  FLOPs per CTA
+ * and round, 2 M N K per MMA:
+ *   mode 0  kind::f16 128x128x16, both operands in shared memory (the QK^T step)     524,288
+ *   mode 1  kind::f8f6f4 E4M3 128x128x32, A in tensor memory (the P.V step)         1,048,576
+ *   mode 2  8 of mode 0 then 4 of mode 1: one key tile of one 128-row Q tile      8,388,608
+ *   mode 3  kind::f8f6f4 E4M3 128x256x32, both in shared memory (E4M3 dense peak)  2,097,152
+ *   mode 4  kind::f16 128x256x16, both in shared memory (16-bit dense peak)        1,048,576
+ * iters 1 .. 1e8, ctas 1 .. 65535.  A wait that exceeds 2 s is recorded in status_block as for
+ * the other kernels (read it with sage_check_device_status).  Not part of the attention path. */
+sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, void* status_block, void* stream);
+
 /* Waits for `stream`, reads the status block (device pointer) and returns SAGE_OK,
  * SAGE_ERR_DEVICE_TIMEOUT (a bounded wait expired; the block is then cleared) or
  * SAGE_ERR_CUDA.  If where != NULL (host), *where receives the code of the wait that

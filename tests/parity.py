@@ -7,11 +7,15 @@ Three references, all computed by the oracle on the same quantised operands:
   ref64  the same schedule with its scores in fp64
   glob   the one-pass fp64 definition: P coded against each row's global max
 Bars:
-  - against ref32 and ref64: relative L2 <= 5e-3 and max-abs <= 3e-2 (the same-quantisation bars);
+  - against ref32: relative L2 <= 5e-3 and max-abs <= 3e-2 (the same-quantisation bars);
+  - against ref64: relative L2 <= 5e-3; max-abs <= 3e-2 + the oracle's own max-abs distance
+    between ref32 and ref64.  The two schedules code P identically except where a key's 448 p
+    lies within fp32 rounding of a code boundary (pinned key by key on the CPU), and one such
+    flip on a dominant key moves an output element by up to one E4M3 step of its weight;
   - against glob: the schedule's own distance from the definition (ref64 against glob, which the
-    CPU pins bound) plus the same two bars.  Coding P against a running max instead of the global
-    max rounds each p at another scale; that difference belongs to the online method, and the GPU
-    may add at most the same-quantisation error on top of it.
+    CPU pins bound) plus the same bars, the max-abs one widened as above.  Coding P against a
+    running max instead of the global max rounds each p at another scale; that difference
+    belongs to the online method, and the GPU may add at most the same-quantisation error.
 With `widen`, an element's max-abs allowance grows by 2^-8 of its magnitude (the bf16 rounding of
 outputs far above 1, e.g. V with large channel offsets).
 """
@@ -39,14 +43,15 @@ def check(got, oz, sm, rows, widen=False):
     glob = oracle.attn_sq(oz, sm, rows, tile=0)
     sched_rel = rel_l2(ref64, glob)
     sched_abs = float(np.abs(ref64 - glob).max())
+    prec_abs = float(np.abs(ref32 - ref64).max())
     info = dict(rel32=rel_l2(got, ref32), abs32=float(np.abs(got - ref32).max()),
                 rel64=rel_l2(got, ref64), abs64=float(np.abs(got - ref64).max()),
                 rel_glob=rel_l2(got, glob), abs_glob=float(np.abs(got - glob).max()),
-                sched_rel=sched_rel, sched_abs=sched_abs)
+                sched_rel=sched_rel, sched_abs=sched_abs, prec_rel=rel_l2(ref32, ref64), prec_abs=prec_abs)
     ok = (info["rel32"] <= SQ_REL and _abs_excess(got, ref32, SQ_ABS, widen) <= 0
-          and info["rel64"] <= SQ_REL and _abs_excess(got, ref64, SQ_ABS, widen) <= 0
+          and info["rel64"] <= SQ_REL and _abs_excess(got, ref64, SQ_ABS + prec_abs, widen) <= 0
           and info["rel_glob"] <= sched_rel + SQ_REL
-          and _abs_excess(got, glob, sched_abs + SQ_ABS, widen) <= 0)
+          and _abs_excess(got, glob, sched_abs + prec_abs + SQ_ABS, widen) <= 0)
     return ok, info
 
 

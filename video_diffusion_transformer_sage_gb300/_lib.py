@@ -76,6 +76,7 @@ def lib():
             "sage_debug_qk_int32": ([I, I, I, QP, I, I, I, I, I, P, P, P], ctypes.c_int),
             "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "sage_debug_wait_timeout": ([P, I, P], ctypes.c_int),
+            "sage_measure_mma_rate": ([I, I, I, P, P], ctypes.c_int),
             "sage_qk_rmsnorm_rope": ([VP, VP, P, P, P, P, F, P], ctypes.c_int),
             "sage_smooth_quant_qk_rmsnorm_rope": ([VP, VP, P, P, P, P, F, QP, P, S, P], ctypes.c_int),
         }
@@ -247,6 +248,16 @@ def sage_debug_qk_int32(qz: Quantized, head: int, i0: int, j0: int, row_tiles: i
 
 def sage_debug_wait_timeout(status: torch.Tensor, limit_ns: int, stream=None) -> None:
     _check(lib().sage_debug_wait_timeout(status.data_ptr(), int(limit_ns), _stream(stream)), "sage_debug_wait_timeout")
+
+
+# FLOPs per CTA and round of each sage_measure_mma_rate mode (2 M N K per MMA).
+MMA_RATE_FLOPS = {0: 2 * 128 * 128 * 16, 1: 2 * 128 * 128 * 32, 2: 8 * 2 * 128 * 128 * 16 + 4 * 2 * 128 * 128 * 32,
+                  3: 2 * 128 * 256 * 32, 4: 2 * 128 * 256 * 16}
+
+
+def sage_measure_mma_rate(mode: int, iters: int, ctas: int, status: torch.Tensor, stream=None) -> None:
+    _check(lib().sage_measure_mma_rate(int(mode), int(iters), int(ctas), status.data_ptr(), _stream(stream)),
+           "sage_measure_mma_rate")
 
 
 def sage_check_device_status(status: torch.Tensor, stream=None):

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsage_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["sage_api.cu", "quant.cu", "attn_fwd.cu", "attn_dense.cu", "noalloc.cu", "qk_transform.cu"]
+SOURCES = ["sage_api.cu", "quant.cu", "attn_fwd.cu", "attn_dense.cu", "noalloc.cu", "qk_transform.cu", "mma_rate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr"]

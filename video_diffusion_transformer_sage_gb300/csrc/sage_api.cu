@@ -293,6 +293,13 @@ sage_status sage_debug_qk_int32(int64_t n, int64_t h, int64_t d, const sage_quan
                                            static_cast<cudaStream_t>(stream)));
 }
 
+sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, void* status_block, void* stream) {
+  if (mode < 0 || mode > 4 || iters < 1 || iters > 100000000 || ctas < 1 || ctas > 65535 || !status_block)
+    return SAGE_ERR_INVALID_ARG;
+  return cuda_status(sage::launch_mma_rate(int(mode), int(iters), int(ctas), static_cast<int32_t*>(status_block),
+                                           2000000000ull, static_cast<cudaStream_t>(stream)));
+}
+
 sage_status sage_debug_wait_timeout(void* status_block, int64_t limit_ns, void* stream) {
   if (!status_block || limit_ns <= 0 || limit_ns > 10000000000LL) return SAGE_ERR_INVALID_ARG;
   return cuda_status(sage::launch_debug_wait_timeout(static_cast<int32_t*>(status_block),

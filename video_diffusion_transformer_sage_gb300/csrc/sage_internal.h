@@ -74,6 +74,9 @@ cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int h
 
 cudaError_t launch_debug_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t s);
 
+// mma_rate.cu: `ctas` CTAs each issue `iters` rounds of the tensor-core MMAs of `mode` (0-4).
+cudaError_t launch_mma_rate(int mode, int iters, int ctas, int32_t* status, uint64_t limit_ns, cudaStream_t s);
+
 // attn_dense.cu
 cudaError_t launch_attn_dense(const StridedView& q, const StridedView& k, const StridedView& v, int n, int h,
                               int d, float sm_scale, void* out, int64_t ost, int64_t osh, cudaStream_t s);
