@@ -243,6 +243,7 @@ def run_gpu(args):
     e2e_steps = 0 if (args.no_e2e or not default_path) else max(3, min(args.steps, 10))
     e2e_ms = e2e_serial_ms = float("nan")
     e2e_runs = []
+    e2e_timeline = None
     host_out = [torch.empty((n, h, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     if e2e_steps:
         ws = sage.workspace(n, h, d, dev)
@@ -251,20 +252,32 @@ def run_gpu(args):
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         comp = torch.cuda.current_stream(dev)
 
-        def run(steps, pipelined):
+        def run(steps, pipelined, timeline=None):
             # The H2D of step i+1 is enqueued before the D2H of step i: a D2H waits for its
             # step's compute, and if both copy streams share one copy engine, a prefetch
             # queued behind it would wait for that compute too (measured: 29-30 ms per step
-            # instead of 23.8 on some runs).
-            ev_in = [torch.cuda.Event() for _ in range(steps)]
-            ev_done = [torch.cuda.Event() for _ in range(steps)]
-            ev_out = [torch.cuda.Event() for _ in range(steps)]
+            # instead of 23.8 on some runs).  With `timeline` (a list), every copy and every call
+            # is bracketed by timing events and its [start, end] in ms from the run's start is
+            # appended, per step, as (h2d, compute, d2h).
+            T = timeline is not None
+
+            def ev():
+                return torch.cuda.Event(enable_timing=T)
+
+            ev_in = [ev() for _ in range(steps)]
+            ev_done = [ev() for _ in range(steps)]
+            ev_out = [ev() for _ in range(steps)]
+            st_in = [ev() for _ in range(steps)]
+            st_comp = [ev() for _ in range(steps)]
+            st_out = [ev() for _ in range(steps)]
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             sin = s_in if pipelined else comp
             sout = s_out if pipelined else comp
             torch.cuda.synchronize()
             a.record(comp)
             sin.wait_event(a)
+            if T:
+                st_in[0].record(sin)
             with torch.cuda.stream(sin):
                 bufs[0].copy_(host, non_blocking=True)
             ev_in[0].record(sin)
@@ -273,23 +286,51 @@ def run_gpu(args):
                 comp.wait_event(ev_in[i])
                 if i >= 2:
                     comp.wait_event(ev_out[i - 2])      # D2H of step i-2 released output k_
+                if T:
+                    st_comp[i].record(comp)
                 qv, kv, vv = views(bufs[k_])
                 sage.sage_attn_fwd(qv, kv, vv, sm_scale, outs[k_], ws, comp)
                 ev_done[i].record(comp)
                 if i + 1 < steps:
                     if i >= 1:
                         sin.wait_event(ev_done[i - 1])  # compute of step i-1 released buffer (i+1)%2
+                    if T:
+                        st_in[i + 1].record(sin)
                     with torch.cuda.stream(sin):
                         bufs[(i + 1) % 2].copy_(host, non_blocking=True)
                     ev_in[i + 1].record(sin)
                 sout.wait_event(ev_done[i])
+                if T:
+                    st_out[i].record(sout)
                 with torch.cuda.stream(sout):
                     host_out[k_].copy_(outs[k_], non_blocking=True)
                 ev_out[i].record(sout)
             comp.wait_event(ev_out[steps - 1])
             b.record(comp)
             torch.cuda.synchronize()
+            if T:
+                for i in range(steps):
+                    timeline.append(tuple((a.elapsed_time(x), a.elapsed_time(y)) for x, y in
+                                          ((st_in[i], ev_in[i]), (st_comp[i], ev_done[i]), (st_out[i], ev_out[i]))))
             return a.elapsed_time(b) / steps
+
+        def overlap_summary(tl):
+            """Mean copy and call durations, the share of each copy's time that a call overlaps, and
+            the mean idle gap of the compute stream between calls (ms)."""
+            def inter(x, y):
+                return max(0.0, min(x[1], y[1]) - max(x[0], y[0]))
+            comps = [t[1] for t in tl]
+            out = {}
+            for name, idx in (("h2d", 0), ("d2h", 2)):
+                ivs = [t[idx] for t in tl]
+                dur = [y - x for x, y in ivs]
+                ov = [sum(inter(iv, c) for c in comps) for iv in ivs]
+                out[f"{name}_ms"] = round(statistics.mean(dur), 3)
+                out[f"{name}_overlapped_by_compute"] = round(sum(ov) / max(sum(dur), 1e-9), 3)
+            out["compute_ms"] = round(statistics.mean(c[1] - c[0] for c in comps), 3)
+            gaps = [comps[i][0] - comps[i - 1][1] for i in range(1, len(comps))]
+            out["compute_idle_gap_ms"] = round(statistics.mean(gaps), 3) if gaps else 0.0
+            return out
 
         run(2, True)
         # The overlap of copies with compute varies from run to run on these boxes (23.8 or
@@ -297,6 +338,10 @@ def run_gpu(args):
         e2e_runs = [run(e2e_steps, True) for _ in range(3)]
         e2e_ms = reduce_max(statistics.median(e2e_runs), pg, dev)
         e2e_serial_ms = run(e2e_steps, False)
+        # The same loop once more with every copy and call bracketed by events: where the time goes.
+        tl = []
+        e2e_timeline_ms = run(e2e_steps, True, tl)
+        e2e_timeline = dict(overlap_summary(tl), ms_per_step=round(e2e_timeline_ms, 3))
 
     # ---- per-call distribution of the public call, in the pages' protocol: after the warm-up
     # above, 5 rounds x 10 calls of sage_attn_fwd (steps a1-a8 from the strided views), each
@@ -479,7 +524,8 @@ def run_gpu(args):
                        "streams, double-buffered (step i overlaps H2D of i+1 and D2H of i-1; the H2D of i+1 "
                        "is enqueued before the D2H of i)",
                 "serial_ms_per_step": round(e2e_serial_ms, 3),
-                "pipelined_runs_ms": [round(x, 3) for x in e2e_runs] if e2e_steps else []},
+                "pipelined_runs_ms": [round(x, 3) for x in e2e_runs] if e2e_steps else [],
+                "timeline": e2e_timeline},
         "call_timing": call_timing,
         "qk_transform": qk_transform,
         "variants": variants,
@@ -498,7 +544,7 @@ def run_gpu(args):
 MMA_MODES = {0: "qk_f16_128x128x16", 1: "pv_e4m3_tmemA_128x128x32", 2: "qk_pv_tile_mix",
              3: "e4m3_ss_128x256x32", 4: "f16_ss_128x256x16"}
 # rounds per launch: about 20 ms each at the nominal per-SM rates (8192 fp16 / 16384 E4M3 FLOP per clock)
-MMA_ITERS = {0: 640000, 1: 640000, 2: 54000, 3: 320000, 4: 320000}
+MMA_ITERS = {0: 80000, 1: 80000, 2: 54000, 3: 40000, 4: 40000}
 
 
 def mma_rates(sage, dev, stream, status):

@@ -263,11 +263,11 @@ sage_status sage_debug_wait_timeout(void* status_block, int64_t limit_ns, void* 
  * columns, ~49 KB shared memory) each issue `iters` rounds of `mode` back to back on zero operands
  * and wait for the last; the caller times the call (e.g. CUDA events on `stream`).  FLOPs per CTA
  * and round, 2 M N K per MMA:
- *   mode 0  kind::f16 128x128x16, both operands in shared memory (the QK^T step)     524,288
- *   mode 1  kind::f8f6f4 E4M3 128x128x32, A in tensor memory (the P.V step)         1,048,576
- *   mode 2  8 of mode 0 then 4 of mode 1: one key tile of one 128-row Q tile      8,388,608
- *   mode 3  kind::f8f6f4 E4M3 128x256x32, both in shared memory (E4M3 dense peak)  2,097,152
- *   mode 4  kind::f16 128x256x16, both in shared memory (16-bit dense peak)        1,048,576
+ *   mode 0  8 x kind::f16 128x128x16, both operands in shared memory (QK^T steps)  4,194,304
+ *   mode 1  8 x kind::f8f6f4 E4M3 128x128x32, A in tensor memory (P.V steps)       8,388,608
+ *   mode 2  8 QK^T steps then 4 P.V steps: one key tile of one 128-row Q tile      8,388,608
+ *   mode 3  8 x kind::f8f6f4 E4M3 128x256x32, both in shared memory (E4M3 peak)  16,777,216
+ *   mode 4  8 x kind::f16 128x256x16, both in shared memory (16-bit peak)          8,388,608
  * iters 1 .. 1e8, ctas 1 .. 65535.  A wait that exceeds 2 s is recorded in status_block as for
  * the other kernels (read it with sage_check_device_status).  Not part of the attention path. */
 sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, void* status_block, void* stream);
@@ -275,7 +275,9 @@ sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, voi
 /* Waits for `stream`, reads the status block (device pointer) and returns SAGE_OK,
  * SAGE_ERR_DEVICE_TIMEOUT (a bounded wait expired; the block is then cleared) or
  * SAGE_ERR_CUDA.  If where != NULL (host), *where receives the code of the wait that
- * expired (0 if none).  This is the one call that synchronises. */
+ * expired: 1 Q tile, 2 K/V tile loaded, 3 K/V slot free, 4 S ready, 5 P ready, 6 P.V done,
+ * 7/8 the S-tile hook's load / MMA, 10 the timeout hook; 0 if none.  This is the one call that
+ * synchronises. */
 sage_status sage_check_device_status(void* status_block, void* stream, int32_t* where);
 
 #ifdef __cplusplus

@@ -361,8 +361,9 @@ def test_fp32_scores_agree_with_fp64_key_by_key(oracle_lib, name, nrows, v_forma
 
 
 def test_fp32_scores_agree_with_fp64_video_sample(oracle_lib):
-    """The same key-by-key agreement on the full video shape (N=37810, H=56, D=128): 4 sampled
-    query rows (including the last) against every key of every head."""
+    """The same key-by-key agreement on the full video shape (N=37810, H=56, D=128): 8 query rows
+    (both ends, the segment borders 99/100/513/514 and the last tile's first two) against every
+    key of every head."""
     inp = synth.make_inputs("video")
     qz = oracle.Quantized(inp.q, inp.k, inp.v)
     n, h, d = inp.q.shape

@@ -5,13 +5,14 @@
 // columns it reads as an operand, then one thread issues `iters` rounds of MMAs back to back
 // (tcgen05.mma issue blocks while the pipe is busy, so the loop runs at the pipe's rate), and
 // the CTA waits for the last one.  Modes (per round):
-//   0  QK^T step: kind::f16, A and B from shared memory, 128 x 128 x 16            (1 MMA)
+//   0  QK^T step: kind::f16, A and B from shared memory, 128 x 128 x 16, into two
+//      accumulators in turn (as the two Q tiles' S_0 and S_1)                      (8 MMAs)
 //   1  P.V step:  kind::f8f6f4 E4M3, A from tensor memory, B from shared memory,
-//                 128 x 128 x 32                                                    (1 MMA)
+//                 128 x 128 x 32, into two accumulators in turn (O_0, O_1)          (8 MMAs)
 //   2  one key tile of one 128-row Q tile as the fused kernel issues it: 8 of mode 0 into an
 //      S accumulator, then 4 of mode 1 reading P from the other S accumulator     (12 MMAs)
-//   3  kind::f8f6f4 E4M3, both operands from shared memory, 128 x 256 x 32         (1 MMA)
-//   4  kind::f16, both operands from shared memory, 128 x 256 x 16                 (1 MMA)
+//   3  kind::f8f6f4 E4M3, both operands from shared memory, 128 x 256 x 32         (8 MMAs)
+//   4  kind::f16, both operands from shared memory, 128 x 256 x 16                 (8 MMAs)
 // The operands are zeros: the rate of these instructions does not depend on the values.
 #include <cuda_runtime.h>
 
@@ -63,16 +64,27 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, i
     const uint32_t sa = smem_u32(smem), sb = smem_u32(smem + kATileBytes);
     const uint64_t da = sdesc_k_sw128(sa), db = sdesc_k_sw128(sb);
     constexpr uint32_t id128 = idesc_f32acc(128, 128), id256 = idesc_f32acc(128, 256);
-    for (int it = 0; it < iters; ++it) {
-      const uint32_t acc = it > 0 ? 1u : 0u;
-      switch (mode) {
-        case 0:
-          mma_f16_ss(tmem, da, db, id128, acc);
-          break;
-        case 1:
-          mma_f8_ts(tmem + 256, tmem, db, id128, acc);
-          break;
-        case 2: {
+    // One loop per mode, 8 MMAs (mode 2: 12) unrolled per round, so the issuing thread's loop
+    // overhead stays far below the MMAs' execution time.
+    switch (mode) {
+      case 0:   // two accumulators in turn, as the kernel's two Q tiles use S_0 and S_1
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            mma_f16_ss(tmem + (u & 1) * 128, sdesc_k_sw128(sa + (u >> 1) * 32), sdesc_k_sw128(sb + (u >> 1) * 32),
+                       id128, (it > 0 || u > 1) ? 1u : 0u);
+        }
+        break;
+      case 1:   // two accumulators in turn (O_0, O_1), P read from S_0 and S_1
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            mma_f8_ts(tmem + 256 + (u & 1) * 128, tmem + (u & 1) * 128 + (u >> 1) * 8,
+                      sdesc_k_sw128(sb + (u >> 1) * 32), id128, (it > 0 || u > 1) ? 1u : 0u);
+        }
+        break;
+      case 2:
+        for (int it = 0; it < iters; ++it) {
           const uint32_t s_acc = tmem + (it & 1) * 128, s_p = tmem + ((it + 1) & 1) * 128;
           const uint32_t o_acc = tmem + 256 + (it & 1) * 128;
 #pragma unroll
@@ -81,16 +93,21 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, i
                        kk > 0 ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ts(o_acc, s_p + kk * 8, sdesc_k_sw128(sb + kk * 32), id128, acc | (kk > 0 ? 1u : 0u));
-          break;
+            mma_f8_ts(o_acc, s_p + kk * 8, sdesc_k_sw128(sb + kk * 32), id128, (it > 1 || kk > 0) ? 1u : 0u);
         }
-        case 3:
-          mma_f8_ss(tmem, da, db, id256, acc);
-          break;
-        default:
-          mma_f16_ss(tmem, da, db, id256, acc);
-          break;
-      }
+        break;
+      case 3:
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mma_f8_ss(tmem + (u & 1) * 256, da, db, id256, (it > 0 || u > 1) ? 1u : 0u);
+        }
+        break;
+      default:
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mma_f16_ss(tmem + (u & 1) * 256, da, db, id256, (it > 0 || u > 1) ? 1u : 0u);
+        }
+        break;
     }
     tc_commit(&bar_done);
     if (!mbar_wait(&bar_done, 0, limit) && atomicCAS(status, 0, 1) == 0) status[1] = kWhereDebugMma;
