@@ -19,7 +19,9 @@
 //   warps 8-11  softmax + epilogue of tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+D), O_1 [256+D, 256+2D).
 // P_t (E4M3, 4 keys per 32-bit column) overwrites columns [0,32) of S_t and is the A
-// operand of the P.V MMA straight from TMEM.
+// operand of the P.V MMA straight from TMEM.  At D = 64 the columns from 384 on are free and
+// P_t has its own there (P_0 at 384, P_1 after it): S_t of the next key tile is then issued as
+// soon as the softmax has read S_t, and P.V no longer sits between a softmax and the next S.
 //
 // The INT8 P.V variant (kPv16; the sampling-component page's sol_int8_qk_pv_* /
 // v_int8_quantize) keeps the same schedule with V as INT8 codes and P = rint(127 p), both held
@@ -84,9 +86,15 @@ struct Cfg {
   static constexpr int kStageBytes = kKTileBytes + kVTileBytes;
   static constexpr int kStages = D == 128 ? (kPv16 ? 2 : 3) : 4;
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // At D = 64 the O accumulators end at column 384 and [384, 512) is free: P_t gets its own
+  // columns there (32 for E4M3, 64 for fp16 codes) instead of overwriting S_t, so the next S_t
+  // may be computed as soon as the softmax has read S_t into registers.
+  static constexpr bool kSepP = D == 64;
+  static constexpr int kColP0 = 384, kColP1 = 384 + (kPv16 ? 64 : 32);
   static constexpr int kTmemCols = 512;
   static constexpr int kBarOffset = 2 * kQTileBytes + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], s_free[2], mma_final
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;   // + slack for 1024-B alignment
 };
 
@@ -174,22 +182,33 @@ __device__ __forceinline__ void p_codes_f16(const float pp[4], uint64_t magic2, 
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(w23) : "r"(h23), "r"(0x64006400u));
 }
 
-// One 128-key tile of the online softmax for the calling thread's row (= TMEM lane):
+// One 128-key tile j of the online softmax for the calling thread's row (= TMEM lane):
 //   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
 //   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
 //   p = exp2(S c - m_new) into the first 32 columns of S (kPv16: P = rint(127 p) as fp16 into
 //   the first 64); l = alpha l + sum p; and, if any row of the warp saw its max rise,
 //   multiplies that row's O by alpha = exp2(m_old - m_new).
+// With separate P columns (Cfg::kSepP, D = 64): S_t is released to the MMA issuer (s_free) as
+//   soon as it is in registers; P goes to its own columns tP, written, like O's rescale, only
+//   once P.V of tile j - 1 has finished with them (pv_done, phase (j - 1) & 1).  Returns false
+//   if that wait expired.
 // kTail: keys >= kvalid are excluded from the max and get p = 0.
 template <int D, bool kTail, bool kPv16>
-__device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0, float c1, int kvalid, bool first,
-                                             float& m, float& l) {
+__device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint32_t tP, float c0, float c1, int kvalid,
+                                             bool first, float& m, float& l, uint64_t* s_free, uint64_t* pv_done,
+                                             int j, uint64_t limit) {
+  constexpr bool kSep = Cfg<D, kPv16>::kSepP;
   uint32_t sr[128];
   SAGE_TMEM_LD32(tS + 0, (sr + 0));
   SAGE_TMEM_LD32(tS + 32, (sr + 32));
   SAGE_TMEM_LD32(tS + 64, (sr + 64));
   SAGE_TMEM_LD32(tS + 96, (sr + 96));
   tmem_wait_ld();
+  if (kSep) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(s_free);
+  }
   float mx0, mx1;
   if (!kTail) {
     mx0 = block_max64(sr);
@@ -215,6 +234,8 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
   // Partial sums of p': one per (32-key chunk, key pair parity), so no add waits on more than
   // eight earlier ones.
   uint64_t l2[4][2];
+  // With separate P columns the P words wait in registers until P.V of tile j - 1 is done.
+  uint32_t pkeep[kSep ? (kPv16 ? 64 : 32) : 1];
 #pragma unroll
   for (int cch = 0; cch < 4; ++cch) {
     const float cb = cch < 2 ? c0 : c1;
@@ -243,19 +264,32 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
       else
         pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
     }
-    // All of S is in registers (tmem_wait_ld above), so P may overwrite its columns.
-    if (kPv16)
+    if (kSep) {
+#pragma unroll
+      for (int i = 0; i < (kPv16 ? 16 : 8); ++i) pkeep[cch * (kPv16 ? 16 : 8) + i] = pw[i];
+    } else if (kPv16) {
+      // All of S is in registers (tmem_wait_ld above), so P may overwrite its columns.
       SAGE_TMEM_ST16(tS + cch * 16, pw);
-    else
+    } else {
       SAGE_TMEM_ST8(tS + cch * 8, pw);
+    }
   }
   const uint64_t la = f2_add(f2_add(l2[0][0], l2[0][1]), f2_add(l2[1][0], l2[1][1]));
   const uint64_t lb = f2_add(f2_add(l2[2][0], l2[2][1]), f2_add(l2[3][0], l2[3][1]));
   float llo, lhi;
   f2_unpack(f2_add(la, lb), llo, lhi);
   l = l * alpha + (llo + lhi);
+  if (kSep) {
+    if (!first) {
+      if (!warp_wait(pv_done, (j - 1) & 1, limit)) return false;
+      tc_fence_after();
+    }
+    SAGE_TMEM_ST32(tP, pkeep);
+    if (kPv16) SAGE_TMEM_ST32(tP + 32, (pkeep + 32));
+  }
   // O is rescaled after P is formed, when S no longer occupies registers.  P.V of this tile
-  // is issued only after p_full, so O still holds the previous tiles' sum here.
+  // is issued only after p_full, so O still holds the previous tiles' sum here (with separate P
+  // columns, P.V of tile j - 1 has completed: the wait above).
   if (__any_sync(0xffffffffu, rise)) {
     // The whole O row in one TMEM round trip: S no longer occupies registers here.
     const uint64_t a2 = f2_pack(alpha, alpha);
@@ -274,6 +308,7 @@ __device__ __forceinline__ void softmax_step(uint32_t tS, uint32_t tO, float c0,
     for (int c = 0; c < D; c += 32) SAGE_TMEM_ST32(tO + c, (o + c));
   }
   tmem_wait_st();
+  return true;
 }
 
 // kRowQ: Q scales per 2^q_shift < 128 rows, so each softmax thread reads its own row's scale;
@@ -299,7 +334,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = kv_empty + C::kStages;
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
-  uint64_t* mma_final = pv_done + 2;
+  uint64_t* s_free = pv_done + 2;
+  uint64_t* mma_final = s_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -319,6 +355,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, 128);
       mbar_init(pv_done + t, 1);
+      mbar_init(s_free + t, 4);
     }
     mbar_init(mma_final, 1);
     fence_mbar_init();
@@ -373,6 +410,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t skv = smem_u32(sKV);
         const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
         const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
+        const uint32_t colP[2] = {tmem + (C::kSepP ? C::kColP0 : C::kColS0), tmem + (C::kSepP ? C::kColP1 : C::kColS1)};
         bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
         if (!ok) record_error(p.status, kWhereQFull, &s_abort);
         if (ok) {
@@ -382,7 +420,43 @@ __global__ void __launch_bounds__(384, 1)
           issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
           tc_commit(s_full + 1);
         }
-        for (int j = 0; ok && j < ntiles; ++j) {
+        // Separate P columns: S_t of tile j + 1 is issued as soon as the softmax has read S_t of tile
+        // j (s_free), P.V of tile j once P_t is written (p_full).  A softmax writes P_t of tile j + 1
+        // only after P.V of tile j is done, so it never runs two tiles ahead of these waits.
+        for (int j = 0; C::kSepP && ok && j < ntiles; ++j) {
+          const int s = j % C::kStages;
+          if (j + 1 < ntiles) {
+            if (!mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+              record_error(p.status, kWhereKvFull, &s_abort);
+              break;
+            }
+            const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+            int t = 0;
+            for (; t < 2; ++t) {
+              if (!mbar_wait(s_free + t, j & 1, limit)) {
+                record_error(p.status, kWhereSFull, &s_abort);
+                break;
+              }
+              tc_fence_after();
+              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              tc_commit(s_full + t);
+            }
+            if (t < 2) break;
+          }
+          int t = 0;
+          for (; t < 2; ++t) {
+            if (!mbar_wait(p_full + t, j & 1, limit)) {
+              record_error(p.status, kWherePFull, &s_abort);
+              break;
+            }
+            tc_fence_after();
+            issue_pv<D, kPv16>(colO[t], colP[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            tc_commit(pv_done + t);
+          }
+          if (t < 2) break;
+          tc_commit(kv_empty + s);
+        }
+        for (int j = 0; !C::kSepP && ok && j < ntiles; ++j) {
           const int s = j % C::kStages;
           const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
           for (int t = 0; t < 2 && ok; ++t) {
@@ -428,6 +502,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t tO = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
+    const uint32_t tP = C::kSepP ? tmem + lane_base + (t == 0 ? C::kColP0 : C::kColP1) : tS;
     const int nbk = p.npad / 64;
     float qscale;
     if (kRowQ) {
@@ -456,10 +531,16 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float c0 = cq * ks0, c1 = cq * ks1;
       const int kvalid = min(kBN, p.n - j * kBN);
-      if (kvalid == kBN)
-        softmax_step<D, false, kPv16>(tS, tO, c0, c1, kBN, j == 0, m, l);
-      else
-        softmax_step<D, true, kPv16>(tS, tO, c0, c1, kvalid, j == 0, m, l);
+      const bool stepped =
+          kvalid == kBN
+              ? softmax_step<D, false, kPv16>(tS, tO, tP, c0, c1, kBN, j == 0, m, l, s_free + t, pv_done + t, j, limit)
+              : softmax_step<D, true, kPv16>(tS, tO, tP, c0, c1, kvalid, j == 0, m, l, s_free + t, pv_done + t, j,
+                                             limit);
+      if (!stepped) {
+        if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
+        ok = false;
+        break;
+      }
       tc_fence_before();
       mbar_arrive(p_full + t);
     }
