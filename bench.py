@@ -454,6 +454,24 @@ def run_gpu(args):
                                "step_ms": round(v_quant + v_attn, 3)}
             del vz
 
+    # ---- the dense quality anchor (sage_attn_dense_bf16: unquantised, fp32 arithmetic on CUDA
+    # cores), timed once after one warm-up call, beside the pages' dense figure -- context only.
+    dense = None
+    if args.dense_anchor:
+        dense_out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
+        sage.sage_attn_dense_bf16(q, k, v, sm_scale, dense_out, stream)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a_.record(stream)
+        sage.sage_attn_dense_bf16(q, k, v, sm_scale, dense_out, stream)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        d_ms = a_.elapsed_time(b_)
+        dense = {"call": "sage_attn_dense_bf16", "ms": round(d_ms, 3),
+                 "tflops": round(w.flops / (d_ms * 1e-3) / 1e12, 2),
+                 "note": "CUDA-core fp32 correctness path; the pages' dense attention took 947.9 ms at N=37810"}
+        del dense_out
+
     # ---- the measured tensor-core ceiling of the attention kernel's instructions (outside the
     # timed region): one CTA per SM issuing each MMA shape back to back on resident operands
     # (sage_measure_mma_rate), 1 warm-up launch, then 3 timed launches per mode with CUDA events.
@@ -517,6 +535,7 @@ def run_gpu(args):
                          "qk_pv_tile_mix" if args.v_format == "e4m3" else "qk_f16_128x128x16"], 4)
                                              if mma_ceiling else None)},
         "mma_ceiling": mma_ceiling,
+        "dense_anchor": dense,
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
                        "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
                        "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},
@@ -670,6 +689,8 @@ def main():
                     help="skip the timing of the INT8 P.V variant and of V smoothing")
     ap.add_argument("--no-qk-transform", action="store_true",
                     help="skip the timing of the in-place RMSNorm + rotary stage")
+    ap.add_argument("--dense-anchor", action="store_true",
+                    help="also time one call of the unquantised dense path (slow: CUDA cores)")
     ap.add_argument("--no-mma-ceiling", action="store_true",
                     help="skip the measurement of the tensor-core rate of the kernel's MMA shapes")
     ap.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS with qkv layout")

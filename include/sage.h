@@ -280,6 +280,10 @@ sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, voi
  * synchronises. */
 sage_status sage_check_device_status(void* status_block, void* stream, int32_t* where);
 
+/* The same call as sage_check_device_status, under the name "get device status": reads (and on a
+ * recorded timeout clears) the device status word of status_block after `stream` drains. */
+sage_status sage_get_device_status(void* status_block, void* stream, int32_t* where);
+
 #ifdef __cplusplus
 }
 #endif

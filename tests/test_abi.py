@@ -13,7 +13,7 @@ EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_by
             "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
             "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
             "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout", "sage_qk_rmsnorm_rope",
-            "sage_smooth_quant_qk_rmsnorm_rope", "sage_measure_mma_rate"}
+            "sage_smooth_quant_qk_rmsnorm_rope", "sage_measure_mma_rate", "sage_get_device_status"}
 
 
 @pytest.fixture(scope="module")

@@ -9,6 +9,7 @@ exact fp64 attention -- or, where the method itself is farther than that from ex
 these synthetic inputs (E4M3 V on N(0,1) values alone costs ~2.6 %), within the oracle's own gap
 + 5e-3.
 """
+import ctypes
 import hashlib
 import math
 
@@ -159,6 +160,11 @@ def test_bounded_wait_expires_into_status():
     sage.sage_debug_wait_timeout(status, 50_000_000)          # 50 ms
     assert sage.sage_check_device_status(status) == (6, 10)
     assert sage.sage_check_device_status(status) == (0, 0)    # cleared by the read
+    # the same read under its other name
+    sage.sage_debug_wait_timeout(status, 50_000_000)
+    where = ctypes.c_int32(0)
+    code = sage.lib().sage_get_device_status(status.data_ptr(), None, ctypes.byref(where))
+    assert (code, where.value) == (6, 10)
     case = gpu_case("tiny")
     out = sage.sage_attn_fwd(case["q"], case["k"], case["v"])
     torch.cuda.synchronize()

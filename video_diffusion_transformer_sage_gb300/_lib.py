@@ -75,6 +75,7 @@ def lib():
             "sage_attn_dense_bf16": ([VP, VP, VP, F, P, I, I, P], ctypes.c_int),
             "sage_debug_qk_int32": ([I, I, I, QP, I, I, I, I, I, P, P, P], ctypes.c_int),
             "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            "sage_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "sage_debug_wait_timeout": ([P, I, P], ctypes.c_int),
             "sage_measure_mma_rate": ([I, I, I, P, P], ctypes.c_int),
             "sage_qk_rmsnorm_rope": ([VP, VP, P, P, P, P, F, P], ctypes.c_int),

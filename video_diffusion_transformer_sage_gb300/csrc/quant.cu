@@ -252,52 +252,17 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
   return h;
 }
 
-// One CTA per (head h, 128-row block b, operand): z = 0 quantises the Q block with one
-// scale; z = 1 quantises the same rows of K - mean as two 64-row blocks, one scale each.
-// only_k: every CTA does K (Q is quantised per smaller block by quant_q_grouped_kernel).
-// Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
-// all its loads before any arithmetic; the maxima share one block reduction.
-// kTransform: each loaded row first gets the qk_transform (RMSNorm + rotary embedding), so the
-// codes are those of the transformed Q and K, which are never written back.
-template <int D, bool kTransform>
-// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.  With
-// the transform, 3 CTAs per SM (80 registers, spills to L1) measured fastest: 1.085 ms for the
-// fused call on the video workload, against 1.111 at 2 CTAs (127 registers, no spills) and
-// 1.097 at 4 (before the table prefetch below).
-__global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
-                                                       const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
-                                                       const float* __restrict__ k_mean, int n, int npad, int only_k,
-                                                       uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
-                                                       uint16_t* __restrict__ k_codes,
-                                                       float* __restrict__ k_scales, const RowTransform tr) {
-  constexpr int VPR = D / 8;            // vectors per row
-  constexpr int RPP = 256 / VPR;        // rows per pass
-  constexpr int NP = 128 / RPP;         // passes per 128-row block
-  __shared__ float red[2][8];
-  const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
-  const bool is_k = only_k || blockIdx.z != 0;
-  const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
+// Codes and scales of one (head hh, 128-row block b) whose rows the block holds in v (the thread's
+// NP rows row0 + p * RPP + rin, 8 channels c8 each; already transformed when the qk_transform
+// applies): Q's |x| maximum over the block, or K's |k - mean| maximum per 64-row half; the block
+// reduction through red; the codes; the scales.  Pad rows (>= n) are excluded from the maxima and
+// written as code 0.  Every thread of the block must call it.
+template <int D, int NP, int RPP>
+__device__ __forceinline__ void quant_block(uint4 (&v)[NP], bool is_k, const float* __restrict__ k_mean, int hh, int b,
+                                            int n, int npad, int c8, int rin, float (&red)[2][8],
+                                            uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
+                                            uint16_t* __restrict__ k_codes, float* __restrict__ k_scales) {
   const int row0 = b * 128;
-  const uint16_t* src = is_k ? k : q;
-  const int64_t st = is_k ? kst : qst, sh = is_k ? ksh : qsh;
-
-  uint4 v[NP];
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const int row = row0 + p * RPP + rin;
-    v[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
-  }
-  if (kTransform) {
-    // The cos / sin rows of the thread's 8 rows into L1 ahead of the transform, which would
-    // otherwise wait on them one row at a time (1.075 -> 1.014 ms for the fused call).
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      const int64_t off = static_cast<int64_t>(min(row0 + p * RPP + rin, n - 1)) * (D / 2) + c8 * 4;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_cos + off));
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_sin + off));
-    }
-    transform_rows<D, NP, RPP>(v, is_k ? tr.gamma_k : tr.gamma_q, row0 + rin, n, c8, tr);
-  }
   float mu[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mu[j] = is_k ? k_mean[hh * D + c8 * 8 + j] : 0.0f;
@@ -381,6 +346,139 @@ __global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const
       q_scales[hh * (npad / 128) + b] = s0;
     }
   }
+}
+
+// One CTA per (head h, 128-row block b, operand): z = 0 quantises the Q block with one
+// scale; z = 1 quantises the same rows of K - mean as two 64-row blocks, one scale each.
+// only_k: every CTA does K (Q is quantised per smaller block by quant_q_grouped_kernel).
+// Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
+// all its loads before any arithmetic; the maxima share one block reduction.
+// kTransform: each loaded row first gets the qk_transform (RMSNorm + rotary embedding), so the
+// codes are those of the transformed Q and K, which are never written back.
+template <int D, bool kTransform>
+// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.  With
+// the transform, 3 CTAs per SM (80 registers, spills to L1) measured fastest: 1.085 ms for the
+// fused call on the video workload, against 1.111 at 2 CTAs (127 registers, no spills) and
+// 1.097 at 4 (before the table prefetch below).
+__global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
+                                                       const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
+                                                       const float* __restrict__ k_mean, int n, int npad, int only_k,
+                                                       uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
+                                                       uint16_t* __restrict__ k_codes,
+                                                       float* __restrict__ k_scales, const RowTransform tr) {
+  constexpr int VPR = D / 8;            // vectors per row
+  constexpr int RPP = 256 / VPR;        // rows per pass
+  constexpr int NP = 128 / RPP;         // passes per 128-row block
+  __shared__ float red[2][8];
+  const int hh = blockIdx.x, b = blockIdx.y;   // heads fastest: co-resident CTAs read adjacent columns
+  const bool is_k = only_k || blockIdx.z != 0;
+  const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
+  const int row0 = b * 128;
+  const uint16_t* src = is_k ? k : q;
+  const int64_t st = is_k ? kst : qst, sh = is_k ? ksh : qsh;
+
+  uint4 v[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int row = row0 + p * RPP + rin;
+    v[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
+  }
+  if (kTransform) {
+    // The cos / sin rows of the thread's 8 rows into L1 ahead of the transform, which would
+    // otherwise wait on them one row at a time (1.075 -> 1.014 ms for the fused call).
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const int64_t off = static_cast<int64_t>(min(row0 + p * RPP + rin, n - 1)) * (D / 2) + c8 * 4;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_cos + off));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_sin + off));
+    }
+    transform_rows<D, NP, RPP>(v, is_k ? tr.gamma_k : tr.gamma_q, row0 + rin, n, c8, tr);
+  }
+  quant_block<D, NP, RPP>(v, is_k, k_mean, hh, b, n, npad, c8, rin, red, q_codes, q_scales, k_codes, k_scales);
+}
+
+// The rows [row0, row0 + 128) of the rotary table (cos and sin of D/2 angles per token, the same
+// for every head) into shared memory: tab[r * D/8 + i] holds cos of pairs 4i .. 4i + 3 of token
+// row0 + r, tab[128 * D/8 + ...] the sines.  Rows past n are clamped into range (their results
+// are dropped).  Every thread of the block must call it; a __syncthreads must follow.
+template <int D>
+__device__ __forceinline__ void stage_rope_table(float4* tab, int row0, int n, const RowTransform& tr) {
+  constexpr int VPR = D / 8;
+  for (int i = threadIdx.x; i < 128 * VPR; i += blockDim.x) {
+    const int64_t off = static_cast<int64_t>(min(row0 + i / VPR, n - 1)) * (D / 2) + (i % VPR) * 4;
+    tab[i] = __ldg(reinterpret_cast<const float4*>(tr.rope_cos + off));
+    tab[128 * VPR + i] = __ldg(reinterpret_cast<const float4*>(tr.rope_sin + off));
+  }
+}
+
+// Heads [h0, h0 + G) of one 128-row block b of Q (is_k false) or K - mean (is_k true), with the
+// qk_transform applied to each row as it is loaded from the staged table, done in turn: the next
+// head's rows are loaded while the current one is transformed and quantised (quant_block).
+template <int D, int G>
+__device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src, int64_t st, int64_t sh, bool is_k,
+                                                const float* __restrict__ k_mean, int h0, int h, int b, int n,
+                                                int npad, const float4* tab, const RowTransform& tr,
+                                                float (&red)[2][2][8], uint16_t* __restrict__ q_codes,
+                                                float* __restrict__ q_scales, uint16_t* __restrict__ k_codes,
+                                                float* __restrict__ k_scales) {
+  constexpr int VPR = D / 8;            // vectors per row (and float4s of cos or sin per token)
+  constexpr int RPP = 256 / VPR;        // rows per pass
+  constexpr int NP = 128 / RPP;         // passes per 128-row block
+  const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
+  const int row0 = b * 128;
+  float g[8];
+  load_gamma8(is_k ? tr.gamma_k : tr.gamma_q, c8, g);
+  uint4 nxt[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int row = row0 + p * RPP + rin;
+    nxt[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + h0 * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
+  }
+  for (int gi = 0; gi < G && h0 + gi < h; ++gi) {   // uniform over the block
+    const int hh = h0 + gi;
+    uint4 v[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) v[p] = nxt[p];
+    if (gi + 1 < G && hh + 1 < h) {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const int row = row0 + p * RPP + rin;
+        nxt[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + (hh + 1) * sh + c8 * 8)
+                         : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const int r = p * RPP + rin;
+      float f[8];
+      unpack_bf16x8(v[p], f);
+      const float ss = row_sumsq<VPR>(f);
+      const uint4 y = norm_rotate8<D>(f, ss, tr.eps, g, tab[r * VPR + c8], tab[128 * VPR + r * VPR + c8]);
+      v[p] = row0 + r < n ? y : make_uint4(0, 0, 0, 0);
+    }
+    quant_block<D, NP, RPP>(v, is_k, k_mean, hh, b, n, npad, c8, rin, red[gi & 1], q_codes, q_scales, k_codes,
+                            k_scales);
+  }
+}
+
+// The quantisation with the qk_transform applied to each row as it is loaded, for G heads of one
+// 128-row block per CTA (z = 0 Q, z = 1 K; only_k: K only).  The block's rows of the rotary
+// table are staged in shared memory once and serve all G heads, instead of being read again from
+// L2 by one CTA per head.  Dynamic shared memory: 2 x 128 x D/2 floats.
+template <int D, int G>
+__global__ void __launch_bounds__(256, 2) quant_qk_tab_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
+                                                             const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
+                                                             const float* __restrict__ k_mean, int n, int h, int npad,
+                                                             int only_k, uint16_t* __restrict__ q_codes,
+                                                             float* __restrict__ q_scales, uint16_t* __restrict__ k_codes,
+                                                             float* __restrict__ k_scales, const RowTransform tr) {
+  extern __shared__ float4 tab[];
+  __shared__ float red[2][2][8];        // by head parity: a head's reduction never meets the next one's
+  const bool is_k = only_k || blockIdx.z != 0;
+  stage_rope_table<D>(tab, blockIdx.y * 128, n, tr);
+  __syncthreads();
+  tab_quant_heads<D, G>(is_k ? k : q, is_k ? kst : qst, is_k ? ksh : qsh, is_k, k_mean, blockIdx.x * G, h,
+                        blockIdx.y, n, npad, tab, tr, red, q_codes, q_scales, k_codes, k_scales);
 }
 
 // One CTA per (head h, 128-row block b) of Q when one scale covers q_block < 128 rows
@@ -645,14 +743,28 @@ cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, 
 
 namespace {
 
+constexpr int kTabHeads = 8;   // heads per CTA of quant_qk_tab_kernel
+
 template <int D, bool kTransform>
 cudaError_t launch_quant_qk_t(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h,
                               int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                               const RowTransform& tr, cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
   const int only_k = q_block != 128;
-  quant_qk_kernel<D, kTransform><<<dim3(h, npad / 128, only_k ? 1 : 2), 256, 0, s>>>(
-      q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k, q_codes, q_scales, k_codes, k_scales, tr);
+  if (kTransform) {
+    constexpr int kTab = 2 * 128 * (D / 2) * 4;
+    // The dynamic shared-memory limit is a per-device attribute of the function: set it on every
+    // call (a host-side call, no device synchronisation).
+    cudaError_t e = cudaFuncSetAttribute(quant_qk_tab_kernel<D, kTabHeads>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTab);
+    if (e != cudaSuccess) return e;
+    quant_qk_tab_kernel<D, kTabHeads><<<dim3((h + kTabHeads - 1) / kTabHeads, npad / 128, only_k ? 1 : 2), 256, kTab,
+                                        s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, h, npad, only_k,
+                                             q_codes, q_scales, k_codes, k_scales, tr);
+  } else {
+    quant_qk_kernel<D, kTransform><<<dim3(h, npad / 128, only_k ? 1 : 2), 256, 0, s>>>(
+        q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k, q_codes, q_scales, k_codes, k_scales, tr);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !only_k) return e;
   quant_q_grouped_kernel<D, kTransform><<<dim3(h, npad / 128), 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block,

@@ -321,4 +321,8 @@ sage_status sage_check_device_status(void* status_block, void* stream, int32_t* 
   return SAGE_OK;
 }
 
+sage_status sage_get_device_status(void* status_block, void* stream, int32_t* where) {
+  return sage_check_device_status(status_block, stream, where);
+}
+
 }  // extern "C"

@@ -52,8 +52,8 @@ struct RowTransform {
 // Per-128-token column sums of the transformed K rows (the partials of the K mean).
 cudaError_t launch_colsum_transform(const StridedView& k, int n, int h, int d, const RowTransform& tr,
                                     float* partials, cudaStream_t s);
-// q_block: rows per Q scale, a power of two <= 128.  tr: NULL, or the transform to apply to
-// every Q and K row first.
+// q_block: rows per Q scale, a power of two <= 128.  tr: NULL, or the transform to
+// apply to every Q and K row first.
 cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
                             int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
                             const RowTransform* tr, cudaStream_t s);
