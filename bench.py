@@ -334,14 +334,16 @@ def run_gpu(args):
 
         run(2, True)
         # The overlap of copies with compute varies from run to run on these boxes (23.8 or
-        # 27.6-30 ms per step for the same code): three runs, the median reported, all listed.
-        e2e_runs = [run(e2e_steps, True) for _ in range(3)]
+        # 26.3-30 ms per step for the same code): three runs, the median reported, all listed,
+        # each with every copy and call bracketed by events so that a slow run shows where its
+        # time went.
+        e2e_runs, e2e_timeline = [], []
+        for _ in range(3):
+            tl = []
+            e2e_runs.append(run(e2e_steps, True, tl))
+            e2e_timeline.append(dict(overlap_summary(tl), ms_per_step=round(e2e_runs[-1], 3)))
         e2e_ms = reduce_max(statistics.median(e2e_runs), pg, dev)
         e2e_serial_ms = run(e2e_steps, False)
-        # The same loop once more with every copy and call bracketed by events: where the time goes.
-        tl = []
-        e2e_timeline_ms = run(e2e_steps, True, tl)
-        e2e_timeline = dict(overlap_summary(tl), ms_per_step=round(e2e_timeline_ms, 3))
 
     # ---- per-call distribution of the public call, in the pages' protocol: after the warm-up
     # above, 5 rounds x 10 calls of sage_attn_fwd (steps a1-a8 from the strided views), each
