@@ -396,8 +396,9 @@ def run_gpu(args):
         # The same transform fused into the K mean and the Q / K quantisation
         # (sage_smooth_quant_qk_rmsnorm_rope: Q and K only read), against the unfused pair
         # (the in-place transform, then sage_smooth_quant_qk) on the same data; 3 warm-up calls,
-        # then 20 calls each, CUDA events per call.  Algorithmic bytes of the fused call: K read
-        # twice (mean, codes) and Q once (6 N H D), fp16 codes written (4 N H D), the table (4 N D).
+        # then 20 calls each, CUDA events per call.  Bytes of the fused call: K read once and its
+        # transformed rows written and read back (6 N H D), Q read once (2 N H D), fp16 codes
+        # written (4 N H D), the table (4 N D).
         fz = sage.Quantized(n, h, d, dev)
 
         def timed(fn, calls=20):
@@ -416,7 +417,7 @@ def run_gpu(args):
                                                                         stream))
         pair_ms = timed(lambda: (sage.sage_qk_rmsnorm_rope(tq, tk, gq, gk, cos, sin, 1e-6, stream),
                                  sage.sage_smooth_quant_qk(tq, tk, fz, scratch, stream)))
-        f_bytes = 10 * n * h * d + 4 * n * d
+        f_bytes = 12 * n * h * d + 4 * n * d
         qk_transform["fused_with_quantise"] = {
             "call": "sage_smooth_quant_qk_rmsnorm_rope", "ms": round(fused_ms, 4), "bytes": f_bytes,
             "gbs": round(f_bytes / (fused_ms * 1e-3) / 1e9, 1), "unfused_pair_ms": round(pair_ms, 4),

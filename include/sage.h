@@ -218,11 +218,13 @@ sage_status sage_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const f
 
 /* The qk_transform fused into the K smoothing and Q / K quantisation: the same outputs, bit for
  * bit, as sage_qk_rmsnorm_rope(q, k, ...) followed by sage_smooth_quant_qk(q, k, qz, ...), but
- * q and k are only READ.  The transform is applied to each row as the quantise kernels load
- * it (and as the K-mean pass sums it); the transformed Q and K are never written, which saves
- * their write and re-read (4 N H D bytes each) -- the fusion of the rms_rope stage into the
- * quantisation prologue.  Arguments: q, k, gamma_*, rope_*, eps as for sage_qk_rmsnorm_rope;
- * qz, ws, ws_bytes as for sage_smooth_quant_qk (any q_block).  Errors as for both. */
+ * q and k are only READ -- the fusion of the rms_rope stage into the quantisation prologue.
+ * K is transformed once, by the K-mean pass, which leaves the transformed rows in qz->q_codes
+ * for K's quantisation to read back; Q is transformed as its quantise kernel loads it, and
+ * its codes then replace that scratch content.  The transformed Q is never written, and Q and
+ * K are not written back in place.  Arguments: q, k, gamma_*, rope_*, eps as for
+ * sage_qk_rmsnorm_rope; qz, ws, ws_bytes as for sage_smooth_quant_qk (any q_block).  Errors
+ * as for both; after an error qz->q_codes may hold transformed K rows. */
 sage_status sage_smooth_quant_qk_rmsnorm_rope(const sage_view* q, const sage_view* k, const float* gamma_q,
                                               const float* gamma_k, const float* rope_cos, const float* rope_sin,
                                               float eps, const sage_quantized* qz, void* ws, size_t ws_bytes,

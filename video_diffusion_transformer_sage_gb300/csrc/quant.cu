@@ -155,13 +155,16 @@ __device__ __forceinline__ void transform_rows(uint4 (&v)[NP], const float* gamm
 }
 
 // Column sums of the transformed K, per 128-token chunk, in the order of colreduce_kernel's
-// sum mode (ascending tokens, fp32): the partials of the mean of the transformed K.  One thread
-// per (chunk, 8 channels of one head); a head's D/8 threads are consecutive lanes.  Threads
-// past the last head run the loop on zeros (the row sums need every lane) and store nothing.
+// sum mode (ascending tokens, fp32): the partials of the mean of the transformed K.  The
+// transformed rows themselves (bf16) go to kt, head-major [H][npad][D], so that K is
+// transformed once and its quantisation reads them back.  One thread per (chunk, 8 channels of
+// one head); a head's D/8 threads are consecutive lanes.  Threads past the last head run the
+// loop on zeros (the row sums need every lane) and store nothing.
 template <int D>
 __global__ void __launch_bounds__(128) colsum_transform_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
-                                                               int n, int h, const RowTransform tr,
-                                                               float* __restrict__ partials) {
+                                                               int n, int npad, int h, const RowTransform tr,
+                                                               float* __restrict__ partials,
+                                                               uint16_t* __restrict__ kt) {
   constexpr int VPR = D / 8;
   const int g = blockIdx.y * blockDim.x + threadIdx.x;
   const bool active = g < h * VPR;
@@ -188,8 +191,10 @@ __global__ void __launch_bounds__(128) colsum_transform_kernel(const uint16_t* _
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (t + u < t1) {   // uniform over the block
+        const uint4 y = transform_row8<D>(v[u], t + u, c8, gam, tr.rope_cos, tr.rope_sin, tr.eps);
+        if (active) *reinterpret_cast<uint4*>(kt + (static_cast<int64_t>(hh) * npad + t + u) * D + c8 * 8) = y;
         float f[8];
-        unpack8(transform_row8<D>(v[u], t + u, c8, gam, tr.rope_cos, tr.rope_sin, tr.eps), f);
+        unpack8(y, f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = acc[j] + f[j];
       }
@@ -350,22 +355,17 @@ __device__ __forceinline__ void quant_block(uint4 (&v)[NP], bool is_k, const flo
 
 // One CTA per (head h, 128-row block b, operand): z = 0 quantises the Q block with one
 // scale; z = 1 quantises the same rows of K - mean as two 64-row blocks, one scale each.
-// only_k: every CTA does K (Q is quantised per smaller block by quant_q_grouped_kernel).
-// Pad rows (>= n) are excluded from the maxima and written as code 0.  Each thread issues
-// all its loads before any arithmetic; the maxima share one block reduction.
-// kTransform: each loaded row first gets the qk_transform (RMSNorm + rotary embedding), so the
-// codes are those of the transformed Q and K, which are never written back.
-template <int D, bool kTransform>
-// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.  With
-// the transform, 3 CTAs per SM (80 registers, spills to L1) measured fastest: 1.085 ms for the
-// fused call on the video workload, against 1.111 at 2 CTAs (127 registers, no spills) and
-// 1.097 at 4 (before the table prefetch below).
-__global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
-                                                       const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
-                                                       const float* __restrict__ k_mean, int n, int npad, int only_k,
-                                                       uint16_t* __restrict__ q_codes, float* __restrict__ q_scales,
-                                                       uint16_t* __restrict__ k_codes,
-                                                       float* __restrict__ k_scales, const RowTransform tr) {
+// only_k: every CTA does K (Q is quantised by another kernel).  Pad rows (>= n) are excluded
+// from the maxima and written as code 0.  Each thread issues all its loads before any
+// arithmetic; the maxima share one block reduction.
+// Capped at 64 registers (4 CTAs per SM): at 70 the lost fourth CTA cost 9 % of its time.
+template <int D>
+__global__ void __launch_bounds__(256, 4) quant_qk_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
+                                                          const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
+                                                          const float* __restrict__ k_mean, int n, int npad,
+                                                          int only_k, uint16_t* __restrict__ q_codes,
+                                                          float* __restrict__ q_scales, uint16_t* __restrict__ k_codes,
+                                                          float* __restrict__ k_scales) {
   constexpr int VPR = D / 8;            // vectors per row
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
@@ -382,17 +382,6 @@ __global__ void __launch_bounds__(256, kTransform ? 3 : 4) quant_qk_kernel(const
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
     v[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + hh * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
-  }
-  if (kTransform) {
-    // The cos / sin rows of the thread's 8 rows into L1 ahead of the transform, which would
-    // otherwise wait on them one row at a time (1.075 -> 1.014 ms for the fused call).
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      const int64_t off = static_cast<int64_t>(min(row0 + p * RPP + rin, n - 1)) * (D / 2) + c8 * 4;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_cos + off));
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_sin + off));
-    }
-    transform_rows<D, NP, RPP>(v, is_k ? tr.gamma_k : tr.gamma_q, row0 + rin, n, c8, tr);
   }
   quant_block<D, NP, RPP>(v, is_k, k_mean, hh, b, n, npad, c8, rin, red, q_codes, q_scales, k_codes, k_scales);
 }
@@ -411,23 +400,21 @@ __device__ __forceinline__ void stage_rope_table(float4* tab, int row0, int n, c
   }
 }
 
-// Heads [h0, h0 + G) of one 128-row block b of Q (is_k false) or K - mean (is_k true), with the
-// qk_transform applied to each row as it is loaded from the staged table, done in turn: the next
-// head's rows are loaded while the current one is transformed and quantised (quant_block).
+// Heads [h0, h0 + G) of one 128-row block b of Q, with the qk_transform applied to each row as
+// it is loaded, the rotary factors taken from the staged table; done in turn: the next head's
+// rows are loaded while the current one is transformed and quantised (quant_block).
 template <int D, int G>
-__device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src, int64_t st, int64_t sh, bool is_k,
-                                                const float* __restrict__ k_mean, int h0, int h, int b, int n,
-                                                int npad, const float4* tab, const RowTransform& tr,
-                                                float (&red)[2][2][8], uint16_t* __restrict__ q_codes,
-                                                float* __restrict__ q_scales, uint16_t* __restrict__ k_codes,
-                                                float* __restrict__ k_scales) {
+__device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src, int64_t st, int64_t sh, int h0,
+                                                int h, int b, int n, int npad, const float4* tab,
+                                                const RowTransform& tr, float (&red)[2][2][8],
+                                                uint16_t* __restrict__ q_codes, float* __restrict__ q_scales) {
   constexpr int VPR = D / 8;            // vectors per row (and float4s of cos or sin per token)
   constexpr int RPP = 256 / VPR;        // rows per pass
   constexpr int NP = 128 / RPP;         // passes per 128-row block
   const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
   const int row0 = b * 128;
   float g[8];
-  load_gamma8(is_k ? tr.gamma_k : tr.gamma_q, c8, g);
+  load_gamma8(tr.gamma_q, c8, g);
   uint4 nxt[NP];
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
@@ -456,29 +443,24 @@ __device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src
       const uint4 y = norm_rotate8<D>(f, ss, tr.eps, g, tab[r * VPR + c8], tab[128 * VPR + r * VPR + c8]);
       v[p] = row0 + r < n ? y : make_uint4(0, 0, 0, 0);
     }
-    quant_block<D, NP, RPP>(v, is_k, k_mean, hh, b, n, npad, c8, rin, red[gi & 1], q_codes, q_scales, k_codes,
-                            k_scales);
+    quant_block<D, NP, RPP>(v, false, nullptr, hh, b, n, npad, c8, rin, red[gi & 1], q_codes, q_scales, nullptr,
+                            nullptr);
   }
 }
 
-// The quantisation with the qk_transform applied to each row as it is loaded, for G heads of one
-// 128-row block per CTA (z = 0 Q, z = 1 K; only_k: K only).  The block's rows of the rotary
-// table are staged in shared memory once and serve all G heads, instead of being read again from
-// L2 by one CTA per head.  Dynamic shared memory: 2 x 128 x D/2 floats.
+// The quantisation of Q (one scale per 128 rows) with the qk_transform applied to each row as it
+// is loaded, for G heads of one 128-row block per CTA.  The block's rows of the rotary table are
+// staged in shared memory once and serve all G heads, instead of being read again from L2 by
+// one CTA per head.  Dynamic shared memory: 2 x 128 x D/2 floats.
 template <int D, int G>
-__global__ void __launch_bounds__(256, 2) quant_qk_tab_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
-                                                             const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
-                                                             const float* __restrict__ k_mean, int n, int h, int npad,
-                                                             int only_k, uint16_t* __restrict__ q_codes,
-                                                             float* __restrict__ q_scales, uint16_t* __restrict__ k_codes,
-                                                             float* __restrict__ k_scales, const RowTransform tr) {
+__global__ void __launch_bounds__(256, 2) quant_q_tab_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
+                                                            int n, int h, int npad, uint16_t* __restrict__ q_codes,
+                                                            float* __restrict__ q_scales, const RowTransform tr) {
   extern __shared__ float4 tab[];
   __shared__ float red[2][2][8];        // by head parity: a head's reduction never meets the next one's
-  const bool is_k = only_k || blockIdx.z != 0;
   stage_rope_table<D>(tab, blockIdx.y * 128, n, tr);
   __syncthreads();
-  tab_quant_heads<D, G>(is_k ? k : q, is_k ? kst : qst, is_k ? ksh : qsh, is_k, k_mean, blockIdx.x * G, h,
-                        blockIdx.y, n, npad, tab, tr, red, q_codes, q_scales, k_codes, k_scales);
+  tab_quant_heads<D, G>(q, qst, qsh, blockIdx.x * G, h, blockIdx.y, n, npad, tab, tr, red, q_codes, q_scales);
 }
 
 // One CTA per (head h, 128-row block b) of Q when one scale covers q_block < 128 rows
@@ -743,32 +725,51 @@ cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, 
 
 namespace {
 
-constexpr int kTabHeads = 8;   // heads per CTA of quant_qk_tab_kernel
+// Heads per CTA of quant_q_tab_kernel: the fused call on the video workload took 0.752 ms at
+// 8, 0.745 at 14 and 0.741 at 28.
+constexpr int kTabHeads = 28;
 
-template <int D, bool kTransform>
+template <int D>
 cudaError_t launch_quant_qk_t(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h,
                               int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
-                              const RowTransform& tr, cudaStream_t s) {
+                              cudaStream_t s) {
   const int npad = static_cast<int>(pad128(n));
   const int only_k = q_block != 128;
-  if (kTransform) {
+  quant_qk_kernel<D><<<dim3(h, npad / 128, only_k ? 1 : 2), 256, 0, s>>>(
+      q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k, q_codes, q_scales, k_codes, k_scales);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !only_k) return e;
+  quant_q_grouped_kernel<D, false><<<dim3(h, npad / 128), 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes,
+                                                                       q_scales, RowTransform{});
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_quant_k_t(const StridedView& k, const float* k_mean, int n, int h, uint16_t* k_codes,
+                             float* k_scales, cudaStream_t s) {
+  const int npad = static_cast<int>(pad128(n));
+  quant_qk_kernel<D><<<dim3(h, npad / 128, 1), 256, 0, s>>>(k.data, k.st, k.sh, k.data, k.st, k.sh, k_mean, n, npad,
+                                                            1, nullptr, nullptr, k_codes, k_scales);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_quant_q_transform_t(const StridedView& q, int n, int h, int q_block, uint16_t* q_codes,
+                                       float* q_scales, const RowTransform& tr, cudaStream_t s) {
+  const int npad = static_cast<int>(pad128(n));
+  if (q_block == 128) {
     constexpr int kTab = 2 * 128 * (D / 2) * 4;
     // The dynamic shared-memory limit is a per-device attribute of the function: set it on every
     // call (a host-side call, no device synchronisation).
-    cudaError_t e = cudaFuncSetAttribute(quant_qk_tab_kernel<D, kTabHeads>,
+    cudaError_t e = cudaFuncSetAttribute(quant_q_tab_kernel<D, kTabHeads>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kTab);
     if (e != cudaSuccess) return e;
-    quant_qk_tab_kernel<D, kTabHeads><<<dim3((h + kTabHeads - 1) / kTabHeads, npad / 128, only_k ? 1 : 2), 256, kTab,
-                                        s>>>(q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, h, npad, only_k,
-                                             q_codes, q_scales, k_codes, k_scales, tr);
+    quant_q_tab_kernel<D, kTabHeads><<<dim3((h + kTabHeads - 1) / kTabHeads, npad / 128), 256, kTab, s>>>(
+        q.data, q.st, q.sh, n, h, npad, q_codes, q_scales, tr);
   } else {
-    quant_qk_kernel<D, kTransform><<<dim3(h, npad / 128, only_k ? 1 : 2), 256, 0, s>>>(
-        q.data, q.st, q.sh, k.data, k.st, k.sh, k_mean, n, npad, only_k, q_codes, q_scales, k_codes, k_scales, tr);
+    quant_q_grouped_kernel<D, true><<<dim3(h, npad / 128), 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes,
+                                                                        q_scales, tr);
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !only_k) return e;
-  quant_q_grouped_kernel<D, kTransform><<<dim3(h, npad / 128), 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block,
-                                                                            q_codes, q_scales, tr);
   return cudaGetLastError();
 }
 
@@ -776,24 +777,33 @@ cudaError_t launch_quant_qk_t(const StridedView& q, const StridedView& k, const 
 
 cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
                             int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
-                            const RowTransform* tr, cudaStream_t s) {
-  const RowTransform none{};
+                            cudaStream_t s) {
   if (d == 128)
-    return tr ? launch_quant_qk_t<128, true>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, *tr, s)
-              : launch_quant_qk_t<128, false>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, none,
-                                              s);
-  return tr ? launch_quant_qk_t<64, true>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, *tr, s)
-            : launch_quant_qk_t<64, false>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, none, s);
+    return launch_quant_qk_t<128>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, s);
+  return launch_quant_qk_t<64>(q, k, k_mean, n, h, q_block, q_codes, q_scales, k_codes, k_scales, s);
+}
+
+cudaError_t launch_quant_k(const StridedView& k, const float* k_mean, int n, int h, int d, uint16_t* k_codes,
+                           float* k_scales, cudaStream_t s) {
+  if (d == 128) return launch_quant_k_t<128>(k, k_mean, n, h, k_codes, k_scales, s);
+  return launch_quant_k_t<64>(k, k_mean, n, h, k_codes, k_scales, s);
+}
+
+cudaError_t launch_quant_q_transform(const StridedView& q, int n, int h, int d, int q_block, uint16_t* q_codes,
+                                     float* q_scales, const RowTransform& tr, cudaStream_t s) {
+  if (d == 128) return launch_quant_q_transform_t<128>(q, n, h, q_block, q_codes, q_scales, tr, s);
+  return launch_quant_q_transform_t<64>(q, n, h, q_block, q_codes, q_scales, tr, s);
 }
 
 cudaError_t launch_colsum_transform(const StridedView& k, int n, int h, int d, const RowTransform& tr,
-                                    float* partials, cudaStream_t s) {
+                                    float* partials, uint16_t* kt, cudaStream_t s) {
   const int nchunk = (n + 127) / 128;
+  const int npad = static_cast<int>(pad128(n));
   const dim3 grid(nchunk, (h * (d / 8) + 127) / 128);
   if (d == 128)
-    colsum_transform_kernel<128><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, h, tr, partials);
+    colsum_transform_kernel<128><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, npad, h, tr, partials, kt);
   else
-    colsum_transform_kernel<64><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, h, tr, partials);
+    colsum_transform_kernel<64><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, npad, h, tr, partials, kt);
   return cudaGetLastError();
 }
 

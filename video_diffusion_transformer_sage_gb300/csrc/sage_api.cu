@@ -162,7 +162,7 @@ sage_status sage_smooth_quant_qk(const sage_view* q, const sage_view* k, const s
   if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), 0.0f, qz->k_mean, s);
   if (e == cudaSuccess)
     e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), q_block_of(qz), qz->q_codes,
-                              qz->q_scales, qz->k_codes, qz->k_scales, nullptr, s);
+                              qz->q_scales, qz->k_codes, qz->k_scales, s);
   return cuda_status(e);
 }
 
@@ -185,11 +185,17 @@ sage_status sage_smooth_quant_qk_rmsnorm_rope(const sage_view* q, const sage_vie
   float* part = static_cast<float*>(ws);
   const int nchunk = static_cast<int>((n + 127) / 128);
   const sage::RowTransform tr{gamma_q, gamma_k, rope_cos, rope_sin, eps};
-  cudaError_t e = sage::launch_colsum_transform(sv(k), int(n), int(h), int(d), tr, part, s);
+  // K is transformed once: the K-mean pass leaves the transformed rows in the Q code buffer
+  // (same [H][pad128(N)][D] 16-bit shape), K is quantised from there, and only then are the Q
+  // codes written, from Q transformed as it is loaded.
+  const sage::StridedView kt{qz->q_codes, d, pad128(n) * d};
+  cudaError_t e = sage::launch_colsum_transform(sv(k), int(n), int(h), int(d), tr, part, qz->q_codes, s);
   if (e == cudaSuccess) e = sage::launch_colfinal(part, nchunk, int(h * d), int(n), 0.0f, qz->k_mean, s);
   if (e == cudaSuccess)
-    e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), q_block_of(qz), qz->q_codes,
-                              qz->q_scales, qz->k_codes, qz->k_scales, &tr, s);
+    e = sage::launch_quant_k(kt, qz->k_mean, int(n), int(h), int(d), qz->k_codes, qz->k_scales, s);
+  if (e == cudaSuccess)
+    e = sage::launch_quant_q_transform(sv(q), int(n), int(h), int(d), q_block_of(qz), qz->q_codes, qz->q_scales, tr,
+                                       s);
   return cuda_status(e);
 }
 

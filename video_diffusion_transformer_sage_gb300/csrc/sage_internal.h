@@ -41,7 +41,7 @@ cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool abs
 cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, float amax_div, float* out,
                             cudaStream_t s);
 // The qk_transform of a row (RMSNorm with weight gamma, rotary embedding by the [N][D/2] cos /
-// sin table), applied by the quantise kernels to each row as they load it.
+// sin table), applied by the fused quantise path to each row as it loads it.
 struct RowTransform {
   const float* gamma_q;
   const float* gamma_k;
@@ -49,14 +49,20 @@ struct RowTransform {
   const float* rope_sin;
   float eps;
 };
-// Per-128-token column sums of the transformed K rows (the partials of the K mean).
+// Per-128-token column sums of the transformed K rows (the partials of the K mean); the
+// transformed rows themselves (bf16) go to kt, head-major [H][pad128(n)][D].
 cudaError_t launch_colsum_transform(const StridedView& k, int n, int h, int d, const RowTransform& tr,
-                                    float* partials, cudaStream_t s);
-// q_block: rows per Q scale, a power of two <= 128.  tr: NULL, or the transform to
-// apply to every Q and K row first.
+                                    float* partials, uint16_t* kt, cudaStream_t s);
+// Codes and scales of Q and of K - k_mean.  q_block: rows per Q scale, a power of two <= 128.
 cudaError_t launch_quant_qk(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h, int d,
                             int q_block, uint16_t* q_codes, float* q_scales, uint16_t* k_codes, float* k_scales,
-                            const RowTransform* tr, cudaStream_t s);
+                            cudaStream_t s);
+// Codes and scales of K - k_mean alone.
+cudaError_t launch_quant_k(const StridedView& k, const float* k_mean, int n, int h, int d, uint16_t* k_codes,
+                           float* k_scales, cudaStream_t s);
+// Codes and scales of Q with the qk_transform applied to each row as it is loaded.
+cudaError_t launch_quant_q_transform(const StridedView& q, int n, int h, int d, int q_block, uint16_t* q_codes,
+                                     float* q_scales, const RowTransform& tr, cudaStream_t s);
 // v_format 0: E4M3 bytes; 1: INT8 codes held as fp16.  v_mean: NULL or the mean to subtract.
 cudaError_t launch_quant_v(const StridedView& v, const float* v_scales, const float* v_mean, int v_format, int n,
                            int h, int d, void* v_codes, cudaStream_t s);
