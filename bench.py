@@ -503,8 +503,11 @@ def run_gpu(args):
     achieved = flops / (attn_avg * 1e-3) / 1e12
     # INT8 P.V runs both contractions on 16-bit operands: the bf16 peak is its roofline.
     attn_peak = p16 if args.v_format == "int8" else composite
-    kname = "attn_fwd_kernel<128, false, %s, %s>" % ("true" if args.v_format == "int8" else "false",
-                                                     "true" if args.smooth_v else "false")
+    kname = "attn_fwd_kernel<%d, false, %s, %s>" % (d, "true" if args.v_format == "int8" else "false",
+                                                    "true" if args.smooth_v else "false")
+    # The measured ceiling of the kernel's own MMA mix: one key tile of one Q tile at its D.
+    mix_mode = ("qk_pv_tile_mix" if d == 128 else "qk_pv_tile_mix_d64") if args.v_format == "e4m3" \
+        else "qk_f16_128x128x16"
     traffic = _traffic_per_launch()
     quant_avg = statistics.mean(quant_ms)
     quant_bytes = 13 * n * h * d
@@ -534,9 +537,9 @@ def run_gpu(args):
                                    f"{p16} TFLOP/s (QK^T, fp16 operands) and 2x that for E4M3 (PV)"),
                      "frac_of_e4m3_peak": round(achieved / p8, 4),
                      "frac_of_bf16_peak": round(achieved / p16, 4),
-                     "frac_of_mma_ceiling": (round(achieved / mma_ceiling["tflops"][
-                         "qk_pv_tile_mix" if args.v_format == "e4m3" else "qk_f16_128x128x16"], 4)
-                                             if mma_ceiling else None)},
+                     "frac_of_mma_ceiling": (round(achieved / mma_ceiling["tflops"][mix_mode], 4)
+                                             if mma_ceiling else None),
+                     "mma_ceiling_mode": mix_mode},
         "mma_ceiling": mma_ceiling,
         "dense_anchor": dense,
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
@@ -567,9 +570,10 @@ def run_gpu(args):
 
 
 MMA_MODES = {0: "qk_f16_128x128x16", 1: "pv_e4m3_tmemA_128x128x32", 2: "qk_pv_tile_mix",
-             3: "e4m3_ss_128x256x32", 4: "f16_ss_128x256x16"}
-# rounds per launch: about 20 ms each at the nominal per-SM rates (8192 fp16 / 16384 E4M3 FLOP per clock)
-MMA_ITERS = {0: 80000, 1: 80000, 2: 54000, 3: 40000, 4: 40000}
+             3: "e4m3_ss_128x256x32", 4: "f16_ss_128x256x16", 5: "pv_e4m3_tmemA_128x64x32",
+             6: "qk_pv_tile_mix_d64"}
+# rounds per launch: about 10-20 ms each at the nominal per-SM rates (8192 fp16 / 16384 E4M3 FLOP per clock)
+MMA_ITERS = {0: 80000, 1: 80000, 2: 54000, 3: 40000, 4: 40000, 5: 80000, 6: 80000}
 
 
 def mma_rates(sage, dev, stream, status):

@@ -270,6 +270,8 @@ sage_status sage_debug_wait_timeout(void* status_block, int64_t limit_ns, void* 
  *   mode 2  8 QK^T steps then 4 P.V steps: one key tile of one 128-row Q tile      8,388,608
  *   mode 3  8 x kind::f8f6f4 E4M3 128x256x32, both in shared memory (E4M3 peak)  16,777,216
  *   mode 4  8 x kind::f16 128x256x16, both in shared memory (16-bit peak)          8,388,608
+ *   mode 5  8 x kind::f8f6f4 E4M3 128x64x32, A in tensor memory (P.V at D = 64)    4,194,304
+ *   mode 6  4 QK^T steps then 4 P.V steps at D = 64: one key tile of one Q tile    4,194,304
  * iters 1 .. 1e8, ctas 1 .. 65535.  A wait that exceeds 2 s is recorded in status_block as for
  * the other kernels (read it with sage_check_device_status).  Not part of the attention path. */
 sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, void* status_block, void* stream);

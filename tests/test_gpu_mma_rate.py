@@ -9,12 +9,13 @@ from video_diffusion_transformer_sage_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 
-# Nominal dense FLOP per clock per SM: 8192 for 16-bit operands, 16384 for E4M3; mode 2 is the
-# attention's per-tile mix, half of each.
-NOMINAL_PER_CLK = {0: 8192, 1: 16384, 2: 1.0 / (0.5 / 8192 + 0.5 / 16384), 3: 16384, 4: 8192}
+# Nominal dense FLOP per clock per SM: 8192 for 16-bit operands, 16384 for E4M3; modes 2 and 6
+# are the attention's per-tile mixes (D = 128, D = 64), half of their FLOPs of each kind.
+MIX = 1.0 / (0.5 / 8192 + 0.5 / 16384)
+NOMINAL_PER_CLK = {0: 8192, 1: 16384, 2: MIX, 3: 16384, 4: 8192, 5: 16384, 6: MIX}
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5, 6])
 def test_mma_rate_modes(mode):
     props = torch.cuda.get_device_properties(0)
     sms = props.multi_processor_count
@@ -36,7 +37,7 @@ def test_mma_rate_modes(mode):
 def test_mma_rate_rejects_bad_arguments():
     status = sage.status_block()
     L = _lib.lib()
-    assert L.sage_measure_mma_rate(5, 10, 1, status.data_ptr(), None) == 1
+    assert L.sage_measure_mma_rate(7, 10, 1, status.data_ptr(), None) == 1
     assert L.sage_measure_mma_rate(0, 0, 1, status.data_ptr(), None) == 1
     assert L.sage_measure_mma_rate(0, 10, 0, status.data_ptr(), None) == 1
     assert L.sage_measure_mma_rate(0, 10, 1, None, None) == 1

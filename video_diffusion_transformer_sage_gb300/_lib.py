@@ -253,7 +253,8 @@ def sage_debug_wait_timeout(status: torch.Tensor, limit_ns: int, stream=None) ->
 
 # FLOPs per CTA and round of each sage_measure_mma_rate mode (2 M N K per MMA).
 MMA_RATE_FLOPS = {0: 8 * 2 * 128 * 128 * 16, 1: 8 * 2 * 128 * 128 * 32, 2: 8 * 2 * 128 * 128 * 16 + 4 * 2 * 128 * 128 * 32,
-                  3: 8 * 2 * 128 * 256 * 32, 4: 8 * 2 * 128 * 256 * 16}
+                  3: 8 * 2 * 128 * 256 * 32, 4: 8 * 2 * 128 * 256 * 16, 5: 8 * 2 * 128 * 64 * 32,
+                  6: 4 * 2 * 128 * 128 * 16 + 4 * 2 * 128 * 64 * 32}
 
 
 def sage_measure_mma_rate(mode: int, iters: int, ctas: int, status: torch.Tensor, stream=None) -> None:

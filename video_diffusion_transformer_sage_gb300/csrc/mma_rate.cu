@@ -13,6 +13,9 @@
 //      S accumulator, then 4 of mode 1 reading P from the other S accumulator     (12 MMAs)
 //   3  kind::f8f6f4 E4M3, both operands from shared memory, 128 x 256 x 32         (8 MMAs)
 //   4  kind::f16, both operands from shared memory, 128 x 256 x 16                 (8 MMAs)
+//   5  P.V step at D = 64: as mode 1 with 128 x 64 x 32                            (8 MMAs)
+//   6  one key tile of one 128-row Q tile at D = 64: 4 of mode 0 into an S accumulator,
+//      then 4 of mode 5 reading P from the other S accumulator                     (8 MMAs)
 // The operands are zeros: the rate of these instructions does not depend on the values.
 #include <cuda_runtime.h>
 
@@ -64,6 +67,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, i
     const uint32_t sa = smem_u32(smem), sb = smem_u32(smem + kATileBytes);
     const uint64_t da = sdesc_k_sw128(sa), db = sdesc_k_sw128(sb);
     constexpr uint32_t id128 = idesc_f32acc(128, 128), id256 = idesc_f32acc(128, 256);
+    constexpr uint32_t id64 = idesc_f32acc(128, 64);
     // One loop per mode, 8 MMAs (mode 2: 12) unrolled per round, so the issuing thread's loop
     // overhead stays far below the MMAs' execution time.
     switch (mode) {
@@ -94,6 +98,26 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int mode, int iters, i
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(o_acc, s_p + kk * 8, sdesc_k_sw128(sb + kk * 32), id128, (it > 1 || kk > 0) ? 1u : 0u);
+        }
+        break;
+      case 5:   // two accumulators in turn (O_0, O_1 at D = 64), P read from S_0 and S_1
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            mma_f8_ts(tmem + 256 + (u & 1) * 64, tmem + (u & 1) * 128 + (u >> 1) * 8,
+                      sdesc_k_sw128(sb + (u >> 1) * 32), id64, (it > 0 || u > 1) ? 1u : 0u);
+        }
+        break;
+      case 6:
+        for (int it = 0; it < iters; ++it) {
+          const uint32_t s_acc = tmem + (it & 1) * 128, s_p = tmem + ((it + 1) & 1) * 128;
+          const uint32_t o_acc = tmem + 256 + (it & 1) * 64;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss(s_acc, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), id128, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_ts(o_acc, s_p + kk * 8, sdesc_k_sw128(sb + kk * 32), id64, (it > 1 || kk > 0) ? 1u : 0u);
         }
         break;
       case 3:

@@ -300,7 +300,7 @@ sage_status sage_debug_qk_int32(int64_t n, int64_t h, int64_t d, const sage_quan
 }
 
 sage_status sage_measure_mma_rate(int64_t mode, int64_t iters, int64_t ctas, void* status_block, void* stream) {
-  if (mode < 0 || mode > 4 || iters < 1 || iters > 100000000 || ctas < 1 || ctas > 65535 || !status_block)
+  if (mode < 0 || mode > 6 || iters < 1 || iters > 100000000 || ctas < 1 || ctas > 65535 || !status_block)
     return SAGE_ERR_INVALID_ARG;
   return cuda_status(sage::launch_mma_rate(int(mode), int(iters), int(ctas), static_cast<int32_t*>(status_block),
                                            2000000000ull, static_cast<cudaStream_t>(stream)));
