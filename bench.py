@@ -545,13 +545,13 @@ def run_gpu(args):
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
                        "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
                        "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},
-        "e2e": {"value": round(job_throughput(flops, 1, world, e2e_ms), 2), "unit": UNIT,
+        "e2e": {"value": (round(job_throughput(flops, 1, world, e2e_ms), 2) if e2e_steps else None), "unit": UNIT,
                 "h2d_bytes_per_step": int(host.numel() * 2), "d2h_bytes_per_step": int(host_out[0].numel() * 2),
-                "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
+                "ms_per_step": round(e2e_ms, 3) if e2e_steps else None, "steps": e2e_steps,
                 "how": "pinned host QKV -> H2D, sage_attn_fwd, D2H -> pinned host each step; copies on their own "
                        "streams, double-buffered (step i overlaps H2D of i+1 and D2H of i-1; the H2D of i+1 "
                        "is enqueued before the D2H of i)",
-                "serial_ms_per_step": round(e2e_serial_ms, 3),
+                "serial_ms_per_step": round(e2e_serial_ms, 3) if e2e_steps else None,
                 "pipelined_runs_ms": [round(x, 3) for x in e2e_runs] if e2e_steps else [],
                 "timeline": e2e_timeline},
         "call_timing": call_timing,

@@ -20,6 +20,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "qk_row.cuh"
@@ -157,53 +159,51 @@ __device__ __forceinline__ void transform_rows(uint4 (&v)[NP], const float* gamm
 // Column sums of the transformed K, per 128-token chunk, in the order of colreduce_kernel's
 // sum mode (ascending tokens, fp32): the partials of the mean of the transformed K.  The
 // transformed rows themselves (bf16) go to kt, head-major [H][npad][D], so that K is
-// transformed once and its quantisation reads them back.  One thread per (chunk, 8 channels of
-// one head); a head's D/8 threads are consecutive lanes.  Threads past the last head run the
-// loop on zeros (the row sums need every lane) and store nothing.
+// transformed once and its quantisation reads them back.
+// One CTA per (128-token chunk, 128 columns = 128 / D heads).  Phase 1: the 256 threads
+// transform the chunk's rows in parallel, 8 row vectors each (a row's D/8 vectors are
+// consecutive lanes, for the row sum's butterfly), store them to kt and to a shared-memory
+// tile.  Phase 2: one thread per column adds the chunk's values from the tile in ascending token
+// order.  Columns of heads past h are neither stored nor summed.
 template <int D>
-__global__ void __launch_bounds__(128) colsum_transform_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
+__global__ void __launch_bounds__(256) colsum_transform_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
                                                                int n, int npad, int h, const RowTransform tr,
                                                                float* __restrict__ partials,
                                                                uint16_t* __restrict__ kt) {
-  constexpr int VPR = D / 8;
-  const int g = blockIdx.y * blockDim.x + threadIdx.x;
-  const bool active = g < h * VPR;
-  const int hh = active ? g / VPR : 0, c8 = g % VPR;
-  const int t0 = blockIdx.x * 128;
-  const int t1 = min(t0 + 128, n);
-  const uint16_t* base = x + hh * sh + c8 * 8;
+  constexpr int VPR = D / 8;            // 16-byte vectors per row
+  constexpr int HG = 128 / D;           // heads per CTA
+  __shared__ __align__(16) uint16_t tile[128][128];
+  const int t0 = blockIdx.x * 128, t1 = min(t0 + 128, n);
+  const int h0 = blockIdx.y * HG;
+  const int c16 = threadIdx.x & 15;     // 8-column vector within the CTA's 128 columns
+  const int head = h0 + c16 / VPR, c8 = c16 % VPR;
+  const bool hv = head < h;
   float gam[8];
   load_gamma8(tr.gamma_k, c8, gam);
-  float acc[8];
+  const uint16_t* base = x + static_cast<int64_t>(hv ? head : 0) * sh + c8 * 8;
+  uint4 v[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-  for (int t = t0; t < t1; t += 8) {
-    uint4 v[8];
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (threadIdx.x >> 4) + 16 * i;
+    v[i] = (hv && t < t1) ? ld_stream(base + static_cast<int64_t>(t) * st) : make_uint4(0, 0, 0, 0);
+  }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      v[u] = (active && t + u < t1) ? ld_stream(base + static_cast<int64_t>(t + u) * st) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {   // the 8 tokens' cos / sin rows into L1 ahead of the transforms
-      const int64_t off = static_cast<int64_t>(min(t + u, n - 1)) * (D / 2) + c8 * 4;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_cos + off));
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(tr.rope_sin + off));
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (t + u < t1) {   // uniform over the block
-        const uint4 y = transform_row8<D>(v[u], t + u, c8, gam, tr.rope_cos, tr.rope_sin, tr.eps);
-        if (active) *reinterpret_cast<uint4*>(kt + (static_cast<int64_t>(hh) * npad + t + u) * D + c8 * 8) = y;
-        float f[8];
-        unpack8(y, f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = acc[j] + f[j];
-      }
+  for (int i = 0; i < 8; ++i) {
+    const int r = (threadIdx.x >> 4) + 16 * i, t = t0 + r;
+    // Every lane transforms (the row sum is a butterfly); rows past n are dropped.
+    const uint4 y = transform_row8<D>(v[i], min(t, n - 1), c8, gam, tr.rope_cos, tr.rope_sin, tr.eps);
+    if (t < t1) {
+      if (hv) *reinterpret_cast<uint4*>(kt + (static_cast<int64_t>(head) * npad + t) * D + c8 * 8) = y;
+      *reinterpret_cast<uint4*>(&tile[r][c16 * 8]) = y;
     }
   }
-  if (!active) return;
-  float4* dst = reinterpret_cast<float4*>(partials + static_cast<int64_t>(blockIdx.x) * h * D + hh * D + c8 * 8);
-  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (threadIdx.x < 128 && h0 + static_cast<int>(threadIdx.x) / D < h) {
+    const int c = threadIdx.x;
+    float acc = 0.0f;
+    for (int r = 0; r < t1 - t0; ++r) acc = acc + __uint_as_float(static_cast<uint32_t>(tile[r][c]) << 16);
+    partials[static_cast<int64_t>(blockIdx.x) * h * D + h0 * D + c] = acc;
+  }
 }
 
 // ---------------------------------------------------------------------------- kernel Q
@@ -400,12 +400,12 @@ __device__ __forceinline__ void stage_rope_table(float4* tab, int row0, int n, c
   }
 }
 
-// Heads [h0, h0 + G) of one 128-row block b of Q, with the qk_transform applied to each row as
+// Heads [h0, h0 + g) of one 128-row block b of Q, with the qk_transform applied to each row as
 // it is loaded, the rotary factors taken from the staged table; done in turn: the next head's
 // rows are loaded while the current one is transformed and quantised (quant_block).
-template <int D, int G>
+template <int D>
 __device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src, int64_t st, int64_t sh, int h0,
-                                                int h, int b, int n, int npad, const float4* tab,
+                                                int g, int h, int b, int n, int npad, const float4* tab,
                                                 const RowTransform& tr, float (&red)[2][2][8],
                                                 uint16_t* __restrict__ q_codes, float* __restrict__ q_scales) {
   constexpr int VPR = D / 8;            // vectors per row (and float4s of cos or sin per token)
@@ -413,20 +413,20 @@ __device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src
   constexpr int NP = 128 / RPP;         // passes per 128-row block
   const int c8 = threadIdx.x % VPR, rin = threadIdx.x / VPR;
   const int row0 = b * 128;
-  float g[8];
-  load_gamma8(tr.gamma_q, c8, g);
+  float gam[8];
+  load_gamma8(tr.gamma_q, c8, gam);
   uint4 nxt[NP];
 #pragma unroll
   for (int p = 0; p < NP; ++p) {
     const int row = row0 + p * RPP + rin;
     nxt[p] = row < n ? ld_stream(src + static_cast<int64_t>(row) * st + h0 * sh + c8 * 8) : make_uint4(0, 0, 0, 0);
   }
-  for (int gi = 0; gi < G && h0 + gi < h; ++gi) {   // uniform over the block
+  for (int gi = 0; gi < g && h0 + gi < h; ++gi) {   // uniform over the block
     const int hh = h0 + gi;
     uint4 v[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) v[p] = nxt[p];
-    if (gi + 1 < G && hh + 1 < h) {
+    if (gi + 1 < g && hh + 1 < h) {
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         const int row = row0 + p * RPP + rin;
@@ -440,7 +440,7 @@ __device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src
       float f[8];
       unpack_bf16x8(v[p], f);
       const float ss = row_sumsq<VPR>(f);
-      const uint4 y = norm_rotate8<D>(f, ss, tr.eps, g, tab[r * VPR + c8], tab[128 * VPR + r * VPR + c8]);
+      const uint4 y = norm_rotate8<D>(f, ss, tr.eps, gam, tab[r * VPR + c8], tab[128 * VPR + r * VPR + c8]);
       v[p] = row0 + r < n ? y : make_uint4(0, 0, 0, 0);
     }
     quant_block<D, NP, RPP>(v, false, nullptr, hh, b, n, npad, c8, rin, red[gi & 1], q_codes, q_scales, nullptr,
@@ -449,18 +449,18 @@ __device__ __forceinline__ void tab_quant_heads(const uint16_t* __restrict__ src
 }
 
 // The quantisation of Q (one scale per 128 rows) with the qk_transform applied to each row as it
-// is loaded, for G heads of one 128-row block per CTA.  The block's rows of the rotary table are
+// is loaded, for g heads of one 128-row block per CTA.  The block's rows of the rotary table are
 // staged in shared memory once and serve all G heads, instead of being read again from L2 by
 // one CTA per head.  Dynamic shared memory: 2 x 128 x D/2 floats.
-template <int D, int G>
+template <int D>
 __global__ void __launch_bounds__(256, 2) quant_q_tab_kernel(const uint16_t* __restrict__ q, int64_t qst, int64_t qsh,
-                                                            int n, int h, int npad, uint16_t* __restrict__ q_codes,
+                                                            int n, int h, int g, int npad, uint16_t* __restrict__ q_codes,
                                                             float* __restrict__ q_scales, const RowTransform tr) {
   extern __shared__ float4 tab[];
   __shared__ float red[2][2][8];        // by head parity: a head's reduction never meets the next one's
   stage_rope_table<D>(tab, blockIdx.y * 128, n, tr);
   __syncthreads();
-  tab_quant_heads<D, G>(q, qst, qsh, blockIdx.x * G, h, blockIdx.y, n, npad, tab, tr, red, q_codes, q_scales);
+  tab_quant_heads<D>(q, qst, qsh, blockIdx.x * g, g, h, blockIdx.y, n, npad, tab, tr, red, q_codes, q_scales);
 }
 
 // One CTA per (head h, 128-row block b) of Q when one scale covers q_block < 128 rows
@@ -725,9 +725,34 @@ cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, 
 
 namespace {
 
-// Heads per CTA of quant_q_tab_kernel: the fused call on the video workload took 0.752 ms at
-// 8, 0.745 at 14 and 0.741 at 28.
-constexpr int kTabHeads = 28;
+// Heads per CTA of quant_q_tab_kernel.  Two CTAs fit on an SM (its shared-memory table), and a
+// CTA's time is about (heads + 1) head-steps (the +1: staging the table), so the call takes
+// about ceil(CTAs / (2 SMs)) x (g + 1) head-steps; g minimises that, the larger g on a tie.  At
+// the video shape (296 row blocks, 56 heads) it picks 56 (one wave); the fused call took 0.752
+// ms at 8 heads per CTA, 0.745 at 14, 0.741 at 28 and 0.740 at 56.  At N = 8192 (64 row blocks)
+// a fixed 28 left 128 CTAs for 152 SMs, and 12 made 320 CTAs, one wave and a 16-CTA tail.
+int tab_heads_per_cta(int h, int blocks) {
+  static std::atomic<int> sms_of[64];   // SM count per device, looked up once
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int sms = sms_of[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
+    sms_of[dev].store(sms, std::memory_order_relaxed);
+  }
+  const int64_t slots = 2 * static_cast<int64_t>(sms);
+  int best = h;
+  int64_t best_cost = -1;
+  for (int g = h; g >= 1; --g) {
+    const int64_t ctas = static_cast<int64_t>(blocks) * ((h + g - 1) / g);
+    const int64_t cost = (ctas + slots - 1) / slots * (g + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = g;
+    }
+  }
+  return best;
+}
 
 template <int D>
 cudaError_t launch_quant_qk_t(const StridedView& q, const StridedView& k, const float* k_mean, int n, int h,
@@ -761,11 +786,11 @@ cudaError_t launch_quant_q_transform_t(const StridedView& q, int n, int h, int q
     constexpr int kTab = 2 * 128 * (D / 2) * 4;
     // The dynamic shared-memory limit is a per-device attribute of the function: set it on every
     // call (a host-side call, no device synchronisation).
-    cudaError_t e = cudaFuncSetAttribute(quant_q_tab_kernel<D, kTabHeads>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTab);
+    cudaError_t e = cudaFuncSetAttribute(quant_q_tab_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTab);
     if (e != cudaSuccess) return e;
-    quant_q_tab_kernel<D, kTabHeads><<<dim3((h + kTabHeads - 1) / kTabHeads, npad / 128), 256, kTab, s>>>(
-        q.data, q.st, q.sh, n, h, npad, q_codes, q_scales, tr);
+    const int g = tab_heads_per_cta(h, npad / 128);
+    quant_q_tab_kernel<D><<<dim3((h + g - 1) / g, npad / 128), 256, kTab, s>>>(q.data, q.st, q.sh, n, h, g, npad,
+                                                                              q_codes, q_scales, tr);
   } else {
     quant_q_grouped_kernel<D, true><<<dim3(h, npad / 128), 256, 0, s>>>(q.data, q.st, q.sh, n, npad, q_block, q_codes,
                                                                         q_scales, tr);
@@ -799,11 +824,11 @@ cudaError_t launch_colsum_transform(const StridedView& k, int n, int h, int d, c
                                     float* partials, uint16_t* kt, cudaStream_t s) {
   const int nchunk = (n + 127) / 128;
   const int npad = static_cast<int>(pad128(n));
-  const dim3 grid(nchunk, (h * (d / 8) + 127) / 128);
+  const dim3 grid(nchunk, (h * d + 127) / 128);
   if (d == 128)
-    colsum_transform_kernel<128><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, npad, h, tr, partials, kt);
+    colsum_transform_kernel<128><<<grid, 256, 0, s>>>(k.data, k.st, k.sh, n, npad, h, tr, partials, kt);
   else
-    colsum_transform_kernel<64><<<grid, 128, 0, s>>>(k.data, k.st, k.sh, n, npad, h, tr, partials, kt);
+    colsum_transform_kernel<64><<<grid, 256, 0, s>>>(k.data, k.st, k.sh, n, npad, h, tr, partials, kt);
   return cudaGetLastError();
 }
 
