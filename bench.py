@@ -240,7 +240,7 @@ def run_gpu(args):
     # loop.  The serial variant (copy, compute, copy, in order) is reported beside it.
     # e2e and the per-call distribution time the public whole-path call (sage_attn_fwd), which
     # runs the default path: skipped when a V option is timed.
-    e2e_steps = 0 if (args.no_e2e or not default_path) else max(3, min(args.steps, 10))
+    e2e_steps = 0 if (args.no_e2e or not default_path) else max(3, args.steps)
     e2e_ms = e2e_serial_ms = float("nan")
     e2e_runs = []
     e2e_timeline = None
