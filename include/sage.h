@@ -230,9 +230,13 @@ sage_status sage_smooth_quant_qk_rmsnorm_rope(const sage_view* q, const sage_vie
                                               float eps, const sage_quantized* qz, void* ws, size_t ws_bytes,
                                               void* stream);
 
-/* The whole path: sage_smooth_quant_qk, sage_quant_v and sage_attn_fwd_quantized on
- * buffers carved from ws (>= sage_workspace_bytes, 256-byte aligned; the status block at
- * its start must be zeroed once by the caller before first use). */
+/* The whole path: the Sage2 call whose stages "gb10-sampling-component-profile-1344x768-124f-
+ * seed440420.json" times under attention_internal_p50_milliseconds.sage2 (K smoothing,
+ * qk_quantize, v_quantize, attention_forward; total_excluding_external_layout), as
+ * sage_smooth_quant_qk, sage_quant_v and sage_attn_fwd_quantized on buffers carved from ws
+ * (>= sage_workspace_bytes, 256-byte aligned, caller-owned; the status block at its start must
+ * be zeroed once by the caller before first use).  Arguments, layouts and errors as for those
+ * three calls; a device timeout is reported through the status block at the start of ws. */
 sage_status sage_attn_fwd(const sage_view* q, const sage_view* k, const sage_view* v, float sm_scale,
                           void* out, int64_t out_stride_token, int64_t out_stride_head, void* ws,
                           size_t ws_bytes, void* stream);
@@ -245,7 +249,8 @@ sage_status sage_attn_dense_bf16(const sage_view* q, const sage_view* k, const s
                                  float sm_scale, void* out, int64_t out_stride_token,
                                  int64_t out_stride_head, void* stream);
 
-/* Test hook: the integer S = Qc Kc^T of head `head`, query rows [i0, i0 + 128 * row_tiles)
+/* Test hook: the integer S = Qc Kc^T (the QK^T product inside attention_forward of the call
+ * above) of head `head`, query rows [i0, i0 + 128 * row_tiles)
  * and keys [j0, j0 + 128 * col_tiles), produced by the same tensor-core QK^T code path
  * as sage_attn_fwd_quantized and converted to int32.  i0, j0 multiples of 128 and inside
  * N_pad.  out: int32 [128 * row_tiles][128 * col_tiles] row-major. */
