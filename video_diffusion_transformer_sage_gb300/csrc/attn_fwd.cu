@@ -45,6 +45,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "sage_internal.h"
@@ -108,6 +109,7 @@ struct AttnParams {
   float sm_scale_log2;     // sm_scale * log2(e)
   uint16_t* out;           // bf16
   int64_t ost, osh;
+  int tma_out;             // 1: the epilogue stores through the output tensor map
   int32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -319,7 +321,8 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint32_t 
 template <int D, bool kRowQ, bool kPv16, bool kMean>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                    const AttnParams p) {
   using C = Cfg<D, kPv16>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_skip;
@@ -550,12 +553,17 @@ __global__ void __launch_bounds__(384, 1)
       const float* vs = p.v_scales + hh * D;
       const float* vm = p.v_mean + hh * D;
       uint16_t* orow = p.out + static_cast<int64_t>(row) * p.ost + static_cast<int64_t>(hh) * p.osh;
+      // With the output map, the rows go through Q tile t's shared memory (every Q.K^T that read it
+      // was issued before this tile's last P.V, so it has completed) in the map's 128-byte
+      // swizzled layout, and each warp stores its 32 rows with one bulk tensor copy per 64
+      // channels: whole lines, instead of 16 bytes per row and instruction.
+      uint8_t* stage = sQ + t * C::kQTileBytes;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
         SAGE_TMEM_LD32(tO + c, o);
         tmem_wait_ld();
-        if (row < p.n) {
+        if (p.tma_out || row < p.n) {
 #pragma unroll
           for (int v8 = 0; v8 < 4; ++v8) {
             uint32_t w[4];
@@ -571,9 +579,28 @@ __global__ void __launch_bounds__(384, 1)
               w[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
             }
-            *reinterpret_cast<uint4*>(orow + c + v8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (p.tma_out) {
+              const int col = c + v8 * 8, chunk = (col & 63) >> 3;
+              *reinterpret_cast<uint4*>(stage + (col >> 6) * C::kPanelBytes + r * 128 + ((chunk ^ (r & 7)) << 4)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              *reinterpret_cast<uint4*>(orow + c + v8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
         }
+      }
+      if (p.tma_out) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int row0 = q0 + t * kBM + wq * 32;
+        if (lane == 0 && row0 < p.n) {   // rows past n are not written (a box wholly past n is skipped)
+#pragma unroll
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_store_3d(&omap, stage + pn * C::kPanelBytes + wq * 32 * 128, pn * 64, hh, row0);
+          bulk_commit();
+          bulk_wait_read<0>();
+        }
+        __syncwarp();
       }
     } else if (ok) {
       if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
@@ -689,6 +716,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// The bf16 output as a [N][H][D] tensor with the caller's token and head strides (elements),
+// 128-byte swizzled boxes of 32 rows x 1 head x 64 channels.  False if the strides do not suit a
+// tensor map (the epilogue then stores row by row).
+bool make_out_map(CUtensorMap* m, void* out, int n, int h, int d, int64_t ost, int64_t osh) {
+  auto fn = encode_fn();
+  if (!fn || ost <= 0 || osh <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(osh) * 2, static_cast<cuuint64_t>(ost) * 2};
+  cuuint32_t box[3] = {64, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major [rows][inner] matrix, 128-byte swizzled boxes of box_rows x box_inner elements.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
               uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
@@ -706,7 +748,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void
 
 template <int D, bool kRowQ, bool kPv16, bool kMean>
 cudaError_t launch_variant(dim3 grid, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const AttnParams& p, cudaStream_t s) {
+                           const CUtensorMap& omap, const AttnParams& p, cudaStream_t s) {
   constexpr int kSmem = Cfg<D, kPv16>::kSmemBytes;
   // The shared-memory limit is a per-device attribute of the function: set it once on each
   // device (bit d of the mask), and on every call for device numbers past 63.
@@ -721,15 +763,15 @@ cudaError_t launch_variant(dim3 grid, const CUtensorMap& qmap, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_acq_rel);
   }
-  attn_fwd_kernel<D, kRowQ, kPv16, kMean><<<grid, 384, kSmem, s>>>(qmap, kmap, vmap, p);
+  attn_fwd_kernel<D, kRowQ, kPv16, kMean><<<grid, 384, kSmem, s>>>(qmap, kmap, vmap, omap, p);
   return cudaGetLastError();
 }
 
 template <int D, bool kRowQ, bool kPv16>
 cudaError_t launch_mean(dim3 grid, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        const AttnParams& p, cudaStream_t s) {
-  return p.v_mean ? launch_variant<D, kRowQ, kPv16, true>(grid, qmap, kmap, vmap, p, s)
-                  : launch_variant<D, kRowQ, kPv16, false>(grid, qmap, kmap, vmap, p, s);
+                        const CUtensorMap& omap, const AttnParams& p, cudaStream_t s) {
+  return p.v_mean ? launch_variant<D, kRowQ, kPv16, true>(grid, qmap, kmap, vmap, omap, p, s)
+                  : launch_variant<D, kRowQ, kPv16, false>(grid, qmap, kmap, vmap, omap, p, s);
 }
 
 template <int D>
@@ -759,15 +801,20 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_bloc
   p.out = static_cast<uint16_t*>(out);
   p.ost = ost;
   p.osh = osh;
+  CUtensorMap omap;
+  memset(&omap, 0, sizeof(omap));
+  // At D = 64 the staged store measured slower (strided64 1.623 ms against 1.612 storing row by
+  // row); at D = 128 faster (video 21.96 against 21.99 ms).
+  p.tma_out = (D == 128 && make_out_map(&omap, out, n, h, D, ost, osh)) ? 1 : 0;
   p.status = status;
   p.wait_limit_ns = kWaitLimitNs;
   const dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
   const bool row_q = q_block != 128;
   if (pv16)
-    return row_q ? launch_mean<D, true, true>(grid, qmap, kmap, vmap, p, s)
-                 : launch_mean<D, false, true>(grid, qmap, kmap, vmap, p, s);
-  return row_q ? launch_mean<D, true, false>(grid, qmap, kmap, vmap, p, s)
-               : launch_mean<D, false, false>(grid, qmap, kmap, vmap, p, s);
+    return row_q ? launch_mean<D, true, true>(grid, qmap, kmap, vmap, omap, p, s)
+                 : launch_mean<D, false, true>(grid, qmap, kmap, vmap, omap, p, s);
+  return row_q ? launch_mean<D, true, false>(grid, qmap, kmap, vmap, omap, p, s)
+               : launch_mean<D, false, false>(grid, qmap, kmap, vmap, omap, p, s);
 }
 
 template <int D>

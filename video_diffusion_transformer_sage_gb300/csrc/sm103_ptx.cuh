@@ -86,6 +86,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// 3-D tiled store of one box from shared memory (laid out as the map's swizzle says), tracked
+// by bulk groups (bulk_commit / bulk_wait_read).  x is the innermost coordinate (elements, its
+// byte offset a multiple of 16); no coordinate may be negative.  Elements outside the tensor
+// are not written.
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Untiled bulk copies (TMA).  Addresses 16-byte aligned, size a multiple of 16 bytes.
 // Global -> shared, completion signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
