@@ -122,6 +122,31 @@ def test_quantized_entry_point_and_strided_output():
     assert torch.isnan(big[:, : h * d]).all()          # nothing written outside the view
 
 
+def test_output_layouts_d128():
+    """At D = 128 the epilogue stores O through a tensor map built from the output strides:
+    token-major inside a wider buffer, head-major [H][N][D], and a padded token stride all give
+    the contiguous output bit for bit, and nothing outside the view is written (N = 4100 leaves a
+    ragged last 32-row box)."""
+    case = gpu_case("tails")
+    n, h, d = case["q"].shape
+    qz = _gpu_qz(case)
+    ref = torch.empty((n, h, d), dtype=torch.bfloat16, device="cuda")
+    sage.sage_attn_fwd_quantized(qz, out=ref)
+    wide = torch.full((n, 2 * h * d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    hnd = torch.full((h, n + 3, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    padded = torch.full((n, h * d + 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    views = [wide[:, h * d:].view(n, h, d), hnd[:, :n].permute(1, 0, 2),
+             padded[:, :h * d].unflatten(1, (h, d))]
+    for v in views:
+        sage.sage_attn_fwd_quantized(qz, out=v)
+    torch.cuda.synchronize()
+    for v in views:
+        assert torch.equal(v, ref)
+    assert torch.isnan(wide[:, :h * d]).all()
+    assert torch.isnan(hnd[:, n:]).all()
+    assert torch.isnan(padded[:, h * d:]).all()
+
+
 def test_deterministic_and_layout_invariant():
     case = gpu_case("tails")
     hnd = gpu_case("tails_hndcopy")
