@@ -252,10 +252,13 @@ __device__ __forceinline__ uint32_t i8codes_f16x2(float x0, float x1, float s, u
     q0 = __fdiv_rn(x0, s);
     q1 = __fdiv_rn(x1, s);
   }
-  q0 = fminf(fmaxf(rintf(q0), -127.0f), 127.0f);
-  q1 = fminf(fmaxf(rintf(q1), -127.0f), 127.0f);
+  // rint, then the clamp to [-127, 127] on the fp16 pair: integers up to 2048 convert exactly,
+  // anything larger (or infinite) becomes at least 2048 in magnitude and clamps to +-127 as it
+  // would in fp32, and a NaN gives -127 in both (max returns the non-NaN operand, as fmaxf).
   uint32_t h;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(q1), "f"(q0));   // integers |q| <= 127: exact
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(rintf(q1)), "f"(rintf(q0)));
+  asm("max.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0xD7F0D7F0u));   // -127, -127
+  asm("min.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0x57F057F0u));   // 127, 127
   return h;
 }
 
