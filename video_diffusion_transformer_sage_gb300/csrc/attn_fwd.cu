@@ -558,12 +558,15 @@ __global__ void __launch_bounds__(384, 1)
       // swizzled layout, and each warp stores its 32 rows with one bulk tensor copy per 64
       // channels: whole lines, instead of 16 bytes per row and instruction.
       uint8_t* stage = sQ + t * C::kQTileBytes;
+      // The staged store exists only at D = 128 (at D = 64 it measured slower); the D = 64
+      // instantiations keep the row stores alone.
+      const bool tma_out = D == 128 && p.tma_out;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
         SAGE_TMEM_LD32(tO + c, o);
         tmem_wait_ld();
-        if (p.tma_out || row < p.n) {
+        if (tma_out || row < p.n) {
 #pragma unroll
           for (int v8 = 0; v8 < 4; ++v8) {
             uint32_t w[4];
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(384, 1)
               w[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
             }
-            if (p.tma_out) {
+            if (tma_out) {
               const int col = c + v8 * 8, chunk = (col & 63) >> 3;
               *reinterpret_cast<uint4*>(stage + (col >> 6) * C::kPanelBytes + r * 128 + ((chunk ^ (r & 7)) << 4)) =
                   make_uint4(w[0], w[1], w[2], w[3]);
@@ -589,7 +592,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (p.tma_out) {
+      if (tma_out) {
         fence_proxy_async_smem();
         __syncwarp();
         const int row0 = q0 + t * kBM + wq * 32;
