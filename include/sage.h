@@ -99,7 +99,9 @@ typedef struct sage_view {
  *            taken out of V before its scales and codes are formed, and the attention adds it
  *            back to every output row (softmax rows sum to 1).  It lowers the quantisation
  *            error of V with a large per-channel offset.  sage_attn_fwd leaves it NULL.
- * All of these pointers must be 16-byte aligned. */
+ * All of these pointers must be 16-byte aligned, and the buffers must not overlap one another
+ * (the calls write several of them at once); equal q_codes and k_codes pointers are refused
+ * with SAGE_ERR_INVALID_ARG. */
 typedef struct sage_quantized {
   uint16_t* q_codes;
   float* q_scales;

@@ -56,7 +56,8 @@ def _view(ptr=16, n=256, h=2, d=128, st=256, sh=128):
 
 
 def _qz(ptr=4096):
-    return _lib.SageQuantizedC(*([ptr] * 7))
+    # seven distinct fake buffers, 16-byte aligned when ptr is
+    return _lib.SageQuantizedC(*[ptr + 4096 * i for i in range(7)])
 
 
 def test_argument_validation_never_launches(L):
@@ -81,8 +82,13 @@ def test_argument_validation_never_launches(L):
     # workspace too small / missing
     assert call(by(q), by(k), by(qz), 4096, 16, None) == 4
     assert call(by(q), by(k), by(qz), 0, 1 << 30, None) == 4
-    # quantised buffers misaligned
+    # quantised buffers misaligned; one buffer for the Q and the K codes
     assert call(by(q), by(k), by(_qz(ptr=4100)), 4096, 1 << 30, None) == 2
+    same = _qz()
+    same.k_codes = same.q_codes
+    assert call(by(q), by(k), by(same), 4096, 1 << 30, None) == 1
+    assert L.sage_smooth_quant_qk_rmsnorm_rope(by(q), by(k), 4096, 4096, 4096, 4096, 1e-6, by(same), 4096, 1 << 30,
+                                               None) == 1
     # fused path: bad out stride, bad scale, small workspace
     assert L.sage_attn_fwd(by(q), by(k), by(v), 0.1, 4096, 250, 128, 4096, 1 << 34, None) == 2
     assert L.sage_attn_fwd(by(q), by(k), by(v), -1.0, 4096, 256, 128, 4096, 1 << 34, None) == 1

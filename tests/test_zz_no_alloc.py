@@ -54,7 +54,7 @@ def test_noalloc_matches_allocating_entry_point(name):
 def test_noalloc_rejects_oversize_before_launch():
     build.build()
     L = _lib.lib()
-    qz = _lib.SageQuantizedC(*([4096] * 7))
+    qz = _lib.SageQuantizedC(*[4096 * (i + 1) for i in range(7)])   # distinct fake buffers
 
     def call(n, h, d):
         v = _lib.SageView(16, n, h, d, 3 * h * d, d)
@@ -65,6 +65,6 @@ def test_noalloc_rejects_oversize_before_launch():
     # beyond what sage_smooth_quant_qk accepts at all: its own status comes first
     assert call((1 << 22) + 1, 1, 64) == 3                 # SAGE_ERR_UNSUPPORTED, not WORKSPACE
     assert call(128, 1, 96) == 3                           # unsupported head dim
-    misaligned = _lib.SageQuantizedC(*([4096 + 4] + [4096] * 6))
+    misaligned = _lib.SageQuantizedC(*([4096 + 4] + [4096 * (i + 2) for i in range(6)]))
     v = _lib.SageView(16, 1024, 2, 128, 3 * 256, 128)
     assert L.sage_smooth_quant_qk_noalloc(ctypes.byref(v), ctypes.byref(v), ctypes.byref(misaligned), None) == 2

@@ -59,6 +59,7 @@ sage_status check_qz(const sage_quantized* qz, bool need_qk, bool need_v) {
   if (need_qk) {
     if (!q_block_ok(qz->q_block)) return SAGE_ERR_INVALID_ARG;
     if (!qz->q_codes || !qz->q_scales || !qz->k_codes || !qz->k_scales || !qz->k_mean) return SAGE_ERR_INVALID_ARG;
+    if (qz->q_codes == qz->k_codes) return SAGE_ERR_INVALID_ARG;   // one buffer for both code sets
     if (!aligned16(qz->q_codes) || !aligned16(qz->k_codes) || !aligned16(qz->q_scales) ||
         !aligned16(qz->k_scales) || !aligned16(qz->k_mean))
       return SAGE_ERR_ALIGNMENT;
