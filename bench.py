@@ -186,18 +186,20 @@ def run_gpu(args):
     default_path = args.v_format == "e4m3" and not args.smooth_v
     qz = sage.Quantized(n, h, d, dev, v_format=args.v_format, smooth_v=args.smooth_v)
     scratch = sage.quant_scratch(n, h, d, dev)
+    scratch2 = torch.empty(2 * scratch.numel(), dtype=torch.uint8, device=dev)   # sage_quant_qkv's
     status = sage.status_block(dev)
     out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, quant_v_fixup, attention;
-    # V smoothing adds colreduce+colfinal for the V mean.
-    launches_per_step = 8 + (2 if args.smooth_v else 0)
+    # sage_quant_qkv: colreduce (K sums and V maxima), colfinal (K mean and V scales), quant_qk,
+    # quant_v, quant_v_fixup; then the attention.  With a V option it runs the two stage calls:
+    # colreduce+colfinal (K), quant_qk, colreduce+colfinal (V), quant_v, quant_v_fixup, and V
+    # smoothing adds colreduce+colfinal for the V mean.
+    launches_per_step = 6 if default_path else 8 + (2 if args.smooth_v else 0)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        sage.sage_smooth_quant_qk(q, k, qz, scratch, stream)
-        sage.sage_quant_v(v, qz, scratch, stream)
+        sage.sage_quant_qkv(q, k, v, qz, scratch2, stream)
         if ev is not None:
             ev[1].record(stream)
         sage.sage_attn_fwd_quantized(qz, sm_scale, out, status, stream)

@@ -180,6 +180,17 @@ sage_status sage_smooth_quant_qk_noalloc(const sage_view* q, const sage_view* k,
 sage_status sage_quant_v(const sage_view* v, const sage_quantized* qz, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* K smoothing, qk_quantize and v_quantize in one call: the outputs of sage_smooth_quant_qk
+ * followed by sage_quant_v, bit for bit, for any options in qz.  With the default options
+ * (q_block 0 or 128, v_format 0, v_mean NULL) the K sums and the V maxima share one launch, and
+ * so do the K mean and the V scales: 5 launches instead of 7, the launches of the pages'
+ * framework_and_k_smoothing_estimate, qk_quantize and v_quantize stages together.  Other
+ * options run the two calls in turn.  q, k, v: views of one shape.  ws: 16-byte aligned device
+ * scratch of ws_bytes >= 2 * sage_quant_scratch_bytes(N, H, D), caller-owned, contents
+ * irrelevant.  Errors as for the two calls. */
+sage_status sage_quant_qkv(const sage_view* q, const sage_view* k, const sage_view* v, const sage_quantized* qz,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* Fused attention on quantised operands (the pages' attention_forward stage):
  *   s_ij = S_ij * q_scales[h][i/128] * k_scales[h][j/64] * sm_scale,  S = exact integer QK^T
  *   running row max m over 128-key tiles; p = exp(s - m); P8 = E4M3(448 p);
@@ -235,7 +246,7 @@ sage_status sage_smooth_quant_qk_rmsnorm_rope(const sage_view* q, const sage_vie
 /* The whole path: the Sage2 call whose stages "gb10-sampling-component-profile-1344x768-124f-
  * seed440420.json" times under attention_internal_p50_milliseconds.sage2 (K smoothing,
  * qk_quantize, v_quantize, attention_forward; total_excluding_external_layout), as
- * sage_smooth_quant_qk, sage_quant_v and sage_attn_fwd_quantized on buffers carved from ws
+ * sage_quant_qkv and sage_attn_fwd_quantized (6 launches) on buffers carved from ws
  * (>= sage_workspace_bytes, 256-byte aligned, caller-owned; the status block at its start must
  * be zeroed once by the caller before first use).  Arguments, layouts and errors as for those
  * three calls; a device timeout is reported through the status block at the start of ws. */

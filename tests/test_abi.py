@@ -13,7 +13,8 @@ EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_by
             "sage_smooth_quant_qk", "sage_quant_v", "sage_attn_fwd_quantized", "sage_attn_fwd",
             "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
             "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout", "sage_qk_rmsnorm_rope",
-            "sage_smooth_quant_qk_rmsnorm_rope", "sage_measure_mma_rate", "sage_get_device_status"}
+            "sage_smooth_quant_qk_rmsnorm_rope", "sage_measure_mma_rate", "sage_get_device_status",
+            "sage_quant_qkv"}
 
 
 @pytest.fixture(scope="module")
@@ -43,7 +44,7 @@ def test_workspace_sizes(L):
     np_ = 37888
     ws = L.sage_workspace_bytes(n, h, d)
     need = 2 * h * np_ * d * 2 + h * d * np_ + h * (np_ // 128) * 4 + h * (np_ // 64) * 4 + 2 * h * d * 4
-    need += (np_ // 128) * h * d * 4 + 256
+    need += 2 * (np_ // 128) * h * d * 4 + 256          # K and V column partials side by side
     assert need <= ws <= need + 16 * 256
     assert L.sage_quant_scratch_bytes(n, h, d) >= (np_ // 128) * h * d * 4
     assert L.sage_workspace_bytes(n, h, 96) == 0       # unsupported head_dim
@@ -131,6 +132,16 @@ def test_argument_validation_never_launches(L):
     assert fq(by(q), by(k), 4096, 4096, 4096, 4096, 1e-6, by(qz), 4096, 16, None) == 4
     assert fq(by(q), by(k), 4096, 4096, 4096, 4096, 1e-6, by(_qz(ptr=4100)), 4096, 1 << 30, None) == 2
     assert fq(by(_view(d=96)), by(_view(d=96)), 4096, 4096, 4096, 4096, 1e-6, by(qz), 4096, 1 << 30, None) == 3
+    # Q, K and V quantised in one call: the checks of both stage calls, and twice their scratch
+    qkv = L.sage_quant_qkv
+    assert qkv(by(q), by(k), by(_view(n=255)), by(qz), 4096, 1 << 30, None) == 1
+    assert qkv(by(q), by(k), by(_view(ptr=18)), by(qz), 4096, 1 << 30, None) == 2
+    assert qkv(by(q), by(k), by(v), by(_qz(ptr=4100)), 4096, 1 << 30, None) == 2
+    assert qkv(by(q), by(k), by(v), by(same), 4096, 1 << 30, None) == 1
+    one = int(L.sage_quant_scratch_bytes(256, 2, 128))
+    assert qkv(by(q), by(k), by(v), by(qz), 4096, one, None) == 4
+    assert qkv(by(q), by(k), by(v), by(qz), 0, 1 << 30, None) == 4
+    assert qkv(by(_view(d=96)), by(_view(d=96)), by(_view(d=96)), by(qz), 4096, 1 << 30, None) == 3
     assert L.sage_check_device_status(0, None, None) == 1
     assert L.sage_debug_wait_timeout(0, 1000, None) == 1
     assert L.sage_debug_wait_timeout(4096, 0, None) == 1

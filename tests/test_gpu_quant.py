@@ -41,6 +41,33 @@ def test_quant_bit_exact(name):
     _assert_same(_quantize(case), case["qz"])
 
 
+@pytest.mark.parametrize("name", CASES)
+def test_quant_qkv_one_call_bit_exact(name):
+    """sage_quant_qkv (K sums and V maxima in one launch, K mean and V scales in one) gives
+    the oracle's codes, scales and mean bit for bit, as the two stage calls do."""
+    case = gpu_case(name)
+    qz = sage.sage_quant_qkv(case["q"], case["k"], case["v"])
+    torch.cuda.synchronize()
+    _assert_same(qz, case["qz"])
+
+
+@pytest.mark.parametrize("opts", [dict(q_block=32), dict(v_format="int8"), dict(smooth_v=True),
+                                  dict(q_block=1, v_format="int8", smooth_v=True)])
+def test_quant_qkv_options_match_stage_calls(opts):
+    """With options, sage_quant_qkv gives exactly what sage_smooth_quant_qk + sage_quant_v give,
+    and its scratch contents do not matter."""
+    case = gpu_case("tails")
+    n, h, d = case["q"].shape
+    a = sage.sage_smooth_quant_qk(case["q"], case["k"], **opts)
+    sage.sage_quant_v(case["v"], a)
+    scratch = torch.full((2 * sage.quant_scratch(n, h, d).numel(),), 0xAB, dtype=torch.uint8, device="cuda")
+    b = sage.sage_quant_qkv(case["q"], case["k"], case["v"], scratch=scratch, **opts)
+    torch.cuda.synchronize()
+    for f in ("q_codes", "k_codes", "v_codes", "q_scales", "k_scales", "k_mean", "v_scales", "v_mean"):
+        x, y = getattr(a, f), getattr(b, f)
+        assert (x is None and y is None) or torch.equal(x, y), f
+
+
 def test_hnd_layout_gives_identical_codes():
     """Strided-NHD and HND-contiguous inputs holding the same values quantise identically
     (the layout invariance the strided-NHD page reports as max_abs_difference 0)."""

@@ -69,6 +69,7 @@ def lib():
             "sage_status_block_bytes": ([], S),
             "sage_smooth_quant_qk": ([VP, VP, QP, P, S, P], ctypes.c_int),
             "sage_quant_v": ([VP, QP, P, S, P], ctypes.c_int),
+            "sage_quant_qkv": ([VP, VP, VP, QP, P, S, P], ctypes.c_int),
             "sage_smooth_quant_qk_noalloc": ([VP, VP, QP, P], ctypes.c_int),
             "sage_attn_fwd_quantized": ([I, I, I, QP, F, P, I, I, P, P], ctypes.c_int),
             "sage_attn_fwd": ([VP, VP, VP, F, P, I, I, P, S, P], ctypes.c_int),
@@ -192,6 +193,21 @@ def sage_quant_v(v: torch.Tensor, qz: Quantized, scratch: Optional[torch.Tensor]
     vv, c = make_view(v), qz.c()
     _check(lib().sage_quant_v(ctypes.byref(vv), ctypes.byref(c), scratch.data_ptr(), scratch.numel(),
                               _stream(stream)), "sage_quant_v")
+    return qz
+
+
+def sage_quant_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, qz: Optional[Quantized] = None,
+                   scratch: Optional[torch.Tensor] = None, stream=None, q_block: int = 128, v_format: str = "e4m3",
+                   smooth_v: bool = False) -> Quantized:
+    """sage_smooth_quant_qk then sage_quant_v in one call (5 launches on the default options).
+    scratch: at least 2 * sage_quant_scratch_bytes bytes (made here when None)."""
+    n, h, d = q.shape
+    qz = qz or Quantized(n, h, d, q.device, q_block, v_format, smooth_v)
+    if scratch is None:
+        scratch = torch.empty(2 * int(lib().sage_quant_scratch_bytes(n, h, d)), dtype=torch.uint8, device=q.device)
+    vq, vk, vv, c = make_view(q), make_view(k), make_view(v), qz.c()
+    _check(lib().sage_quant_qkv(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), ctypes.byref(c),
+                                scratch.data_ptr(), scratch.numel(), _stream(stream)), "sage_quant_qkv")
     return qz
 
 

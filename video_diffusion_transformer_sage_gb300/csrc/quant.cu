@@ -53,9 +53,8 @@ __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
 // the chunk's tokens in ascending order in fp32; absmax mode keeps max |x|, or with kSubMean
 // max |fl32(x - mean[h][c])| (the maxima of smoothed V).  partials[chunk][h*D + c].
 template <bool kAbsMax, bool kSubMean = false>
-__global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
-                                                        int n, int h, int d, const float* __restrict__ mean,
-                                                        float* __restrict__ partials) {
+__device__ __forceinline__ void colreduce_block(const uint16_t* __restrict__ x, int64_t st, int64_t sh, int n, int h,
+                                                int d, const float* __restrict__ mean, float* __restrict__ partials) {
   const int vpr = d >> 3;  // 16-byte vectors per (token, head) row
   const int g = blockIdx.y * blockDim.x + threadIdx.x;
   if (g >= h * vpr) return;
@@ -92,14 +91,32 @@ __global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restri
   dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
+template <bool kAbsMax, bool kSubMean = false>
+__global__ void __launch_bounds__(128) colreduce_kernel(const uint16_t* __restrict__ x, int64_t st, int64_t sh,
+                                                        int n, int h, int d, const float* __restrict__ mean,
+                                                        float* __restrict__ partials) {
+  colreduce_block<kAbsMax, kSubMean>(x, st, sh, n, h, d, mean, partials);
+}
+
+// The K sums (z = 0) and the V maxima (z = 1) of the whole path in one launch.
+__global__ void __launch_bounds__(128) colreduce_kv_kernel(const uint16_t* __restrict__ k, int64_t kst, int64_t ksh,
+                                                           const uint16_t* __restrict__ v, int64_t vst, int64_t vsh,
+                                                           int n, int h, int d, float* __restrict__ part_k,
+                                                           float* __restrict__ part_v) {
+  if (blockIdx.z == 0)
+    colreduce_block<false>(k, kst, ksh, n, h, d, nullptr, part_k);
+  else
+    colreduce_block<true>(v, vst, vsh, n, h, d, nullptr, part_v);
+}
+
 // ---------------------------------------------------------------------------- finalise
 // 32 columns per CTA.  The chunk partials are split into 8 groups of G = ceil(nchunk / 8)
 // consecutive chunks; warp w folds group w in ascending chunk order (fp64 for sums), then
 // warp 0 folds the 8 group results in ascending group order.  Mean = fp32(total / N); in
 // absmax mode out = fl32(max / amax_div) (448 for E4M3 scales, 127 for INT8), IEEE division.
 template <bool kAbsMax>
-__global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__ partials, int nchunk, int cols,
-                                                       int n, float amax_div, float* __restrict__ out) {
+__device__ __forceinline__ void colfinal_block(const float* __restrict__ partials, int nchunk, int cols, int n,
+                                               float amax_div, float* __restrict__ out) {
   __shared__ double gsum[8][32];
   __shared__ float gmax[8][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -137,6 +154,23 @@ __global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__
     }
     out[col] = kAbsMax ? __fdiv_rn(m, amax_div) : static_cast<float>(t / static_cast<double>(n));
   }
+}
+
+template <bool kAbsMax>
+__global__ void __launch_bounds__(256) colfinal_kernel(const float* __restrict__ partials, int nchunk, int cols,
+                                                       int n, float amax_div, float* __restrict__ out) {
+  colfinal_block<kAbsMax>(partials, nchunk, cols, n, amax_div, out);
+}
+
+// The K mean (z = 0) and the E4M3 V scales (z = 1) of the whole path in one launch.
+__global__ void __launch_bounds__(256) colfinal_kv_kernel(const float* __restrict__ part_k,
+                                                          const float* __restrict__ part_v, int nchunk, int cols,
+                                                          int n, float* __restrict__ k_mean,
+                                                          float* __restrict__ v_scales) {
+  if (blockIdx.z == 0)
+    colfinal_block<false>(part_k, nchunk, cols, n, 0.0f, k_mean);
+  else
+    colfinal_block<true>(part_v, nchunk, cols, n, 448.0f, v_scales);
 }
 
 // ---------------------------------------------------------------------------- transform
@@ -717,6 +751,21 @@ cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool abs
     colreduce_kernel<true><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, nullptr, partials);
   else
     colreduce_kernel<false><<<grid, 128, 0, s>>>(x.data, x.st, x.sh, n, h, d, nullptr, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colreduce_kv(const StridedView& k, const StridedView& v, int n, int h, int d, float* part_k,
+                               float* part_v, cudaStream_t s) {
+  const int nchunk = (n + 127) / 128;
+  const int groups = h * (d / 8);
+  colreduce_kv_kernel<<<dim3(nchunk, (groups + 127) / 128, 2), 128, 0, s>>>(k.data, k.st, k.sh, v.data, v.st, v.sh,
+                                                                           n, h, d, part_k, part_v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colfinal_kv(const float* part_k, const float* part_v, int nchunk, int cols, int n, float* k_mean,
+                               float* v_scales, cudaStream_t s) {
+  colfinal_kv_kernel<<<dim3((cols + 31) / 32, 1, 2), 256, 0, s>>>(part_k, part_v, nchunk, cols, n, k_mean, v_scales);
   return cudaGetLastError();
 }
 

@@ -79,11 +79,13 @@ size_t scratch_bytes(int64_t n, int64_t h, int64_t d) {
 }
 
 // Carves the sage_attn_fwd workspace: status | q_codes | k_codes | v_codes | q_scales |
-// k_scales | k_mean | v_scales | scratch, each 256-byte aligned.
+// k_scales | k_mean | v_scales | scratch (K partials) | scratch_v (V partials), each 256-byte
+// aligned.
 struct Carve {
   void* status;
   sage_quantized qz;
   float* scratch;
+  float* scratch_v;
   size_t total;
 };
 Carve carve(void* base, int64_t n, int64_t h, int64_t d) {
@@ -107,6 +109,7 @@ Carve carve(void* base, int64_t n, int64_t h, int64_t d) {
   c.qz.v_format = 0;
   c.qz.v_mean = nullptr;
   c.scratch = reinterpret_cast<float*>(take(scratch_bytes(n, h, d)));
+  c.scratch_v = reinterpret_cast<float*>(take(scratch_bytes(n, h, d)));
   c.total = off;
   return c;
 }
@@ -252,6 +255,39 @@ sage_status sage_attn_fwd_quantized(int64_t n, int64_t h, int64_t d, const sage_
                                            static_cast<int32_t*>(status_block), static_cast<cudaStream_t>(stream)));
 }
 
+sage_status sage_quant_qkv(const sage_view* q, const sage_view* k, const sage_view* v, const sage_quantized* qz,
+                           void* ws, size_t ws_bytes, void* stream) {
+  sage_status st;
+  if ((st = sage::check_smooth_quant_qk_args(q, k, qz)) != SAGE_OK) return st;
+  if ((st = check_view(v)) != SAGE_OK) return st;
+  if (!same_shape(q, v)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_qz(qz, false, true)) != SAGE_OK) return st;
+  const int64_t n = q->n_tokens, h = q->n_heads, d = q->head_dim;
+  const size_t sb = scratch_bytes(n, h, d);
+  if (!ws || !aligned16(ws)) return ws ? SAGE_ERR_ALIGNMENT : SAGE_ERR_WORKSPACE;
+  if (ws_bytes < 2 * sb) return SAGE_ERR_WORKSPACE;
+  if (q_block_of(qz) != 128 || qz->v_format != 0 || qz->v_mean) {
+    // The options: the two stage calls, in turn (the first scratch region serves both).
+    if ((st = sage_smooth_quant_qk(q, k, qz, ws, sb, stream)) != SAGE_OK) return st;
+    return sage_quant_v(v, qz, ws, sb, stream);
+  }
+  // The default path: the kernels of the two stage calls, except that the K sums and the V
+  // maxima share one launch, and so do the K mean and the V scales (5 launches instead of 7).
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* part_k = static_cast<float*>(ws);
+  float* part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + sb);
+  const int nchunk = static_cast<int>((n + 127) / 128);
+  cudaError_t e = sage::launch_colreduce_kv(sv(k), sv(v), int(n), int(h), int(d), part_k, part_v, s);
+  if (e == cudaSuccess)
+    e = sage::launch_colfinal_kv(part_k, part_v, nchunk, int(h * d), int(n), qz->k_mean, qz->v_scales, s);
+  if (e == cudaSuccess)
+    e = sage::launch_quant_qk(sv(q), sv(k), qz->k_mean, int(n), int(h), int(d), 128, qz->q_codes, qz->q_scales,
+                              qz->k_codes, qz->k_scales, s);
+  if (e == cudaSuccess)
+    e = sage::launch_quant_v(sv(v), qz->v_scales, nullptr, 0, int(n), int(h), int(d), qz->v_codes, s);
+  return cuda_status(e);
+}
+
 sage_status sage_attn_fwd(const sage_view* q, const sage_view* k, const sage_view* v, float sm_scale, void* out,
                           int64_t ost, int64_t osh, void* ws, size_t ws_bytes, void* stream) {
   sage_status st;
@@ -265,9 +301,8 @@ sage_status sage_attn_fwd(const sage_view* q, const sage_view* k, const sage_vie
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SAGE_ERR_ALIGNMENT;
   Carve c = carve(ws, n, h, d);
   if (ws_bytes < c.total) return SAGE_ERR_WORKSPACE;
-  const size_t sb = scratch_bytes(n, h, d);
-  if ((st = sage_smooth_quant_qk(q, k, &c.qz, c.scratch, sb, stream)) != SAGE_OK) return st;
-  if ((st = sage_quant_v(v, &c.qz, c.scratch, sb, stream)) != SAGE_OK) return st;
+  // The two scratch regions are adjacent: 2 * scratch_bytes, as sage_quant_qkv takes them.
+  if ((st = sage_quant_qkv(q, k, v, &c.qz, c.scratch, 2 * scratch_bytes(n, h, d), stream)) != SAGE_OK) return st;
   return sage_attn_fwd_quantized(n, h, d, &c.qz, sm_scale, out, ost, osh, c.status, stream);
 }
 

@@ -37,6 +37,12 @@ sage_status check_smooth_quant_qk_args(const sage_view* q, const sage_view* k, c
 // Per-128-token column partials: sums, or maxima of |x| (of |fl32(x - mean)| when mean is set).
 cudaError_t launch_colreduce(const StridedView& x, int n, int h, int d, bool absmax, const float* mean,
                              float* partials, cudaStream_t s);
+// The whole path's K sums and V maxima in one launch (part_k, part_v as for launch_colreduce).
+cudaError_t launch_colreduce_kv(const StridedView& k, const StridedView& v, int n, int h, int d, float* part_k,
+                               float* part_v, cudaStream_t s);
+// The K mean and the E4M3 V scales (max / 448) from those partials in one launch.
+cudaError_t launch_colfinal_kv(const float* part_k, const float* part_v, int nchunk, int cols, int n, float* k_mean,
+                               float* v_scales, cudaStream_t s);
 // amax_div == 0: out = the column mean; otherwise out = fl32(column max / amax_div).
 cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, float amax_div, float* out,
                             cudaStream_t s);
