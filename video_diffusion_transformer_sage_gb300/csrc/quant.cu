@@ -243,20 +243,6 @@ __global__ void __launch_bounds__(256, 4) colsum_transform_kernel(const uint16_t
 }
 
 // ---------------------------------------------------------------------------- kernel Q
-template <int kThreads>
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) r = fmaxf(r, red[w]);
-  __syncthreads();
-  return r;
-}
-
 // Correctly rounded x / s from r = RN(1 / s): y = RN(x r) is within 2 ulp of x / s, the FMA
 // gives the exact remainder x - y s, and one FMA correction y + r (x - y s) rounds to
 // RN(x / s) (P. Markstein, "Computation of elementary functions on the IBM RISC

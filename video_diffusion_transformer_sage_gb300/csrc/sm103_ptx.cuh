@@ -283,12 +283,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// Two 16-bit halves into one word: lo in bits 0-15, hi in bits 16-31.
-__device__ __forceinline__ uint32_t pack_lo_hi16(uint32_t lo, uint32_t hi) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(d) : "r"(lo), "r"(hi));
-  return d;
-}
 
 // ------------------------------------------------------------------ misc math
 __device__ __forceinline__ float ex2_approx(float x) {
