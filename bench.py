@@ -490,10 +490,12 @@ def run_gpu(args):
     # and half as E4M3 MMAs (PV); the E4M3 rate is twice the 16-bit rate.  Its roofline is
     # the time of both halves at their own peaks.  The burst bf16 figure applies when the
     # timed loop ran at full SM clock without a power cap (as the burst GEMM did); the
-    # sustained figure (a GEMM held under the power cap, at lower clocks) otherwise.
+    # sustained figure (a GEMM held under the power cap, at lower clocks) otherwise.  A loop
+    # shorter than the sampler's period leaves no sample; such a short burst is held to the
+    # burst figure too (the larger, so the stricter, denominator).
     clocks = clk.summary()
-    full_clock = (clocks.get("sm_mhz") is not None and clocks["sm_mhz"] >= 0.97 * clocks["sm_max_mhz"]
-                  and "sw_power_cap" not in clocks["reasons"])
+    full_clock = (clocks.get("sm_mhz") is None
+                  or (clocks["sm_mhz"] >= 0.97 * clocks["sm_max_mhz"] and "sw_power_cap" not in clocks["reasons"]))
     p16 = bf16_burst if full_clock else bf16_sus
     p8 = 2 * p16
     composite = 1.0 / (0.5 / p16 + 0.5 / p8)

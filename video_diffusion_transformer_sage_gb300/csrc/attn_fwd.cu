@@ -56,15 +56,20 @@ namespace {
 
 constexpr int kBM = 128;   // query rows per tile
 // Register split of the 384-thread CTA, launched at 168 registers per thread (384 x 168 =
-// 64512): the role warpgroup (warps 0-3) drops to 56, the two softmax warpgroups rise to
-// 224.  128 x 56 + 256 x 224 = 64512, exactly the launch's total, so the rise can always be
-// granted.
-constexpr int kRegsLaunch = 168, kRegsRoles = 56, kRegsSoftmax = 224;
-static_assert(128 * kRegsRoles + 256 * kRegsSoftmax <= 384 * kRegsLaunch, "register split exceeds launch");
-// The INT8 P.V variant's producer (two V panels) and issuer (eight P.V MMAs) spill at 56; its
-// split is 72 / 208: 128 x 72 + 256 x 208 = 62464 <= 64512.
-constexpr int kRegsRolesPv16 = 72, kRegsSoftmaxPv16 = 208;
-static_assert(128 * kRegsRolesPv16 + 256 * kRegsSoftmaxPv16 <= 384 * kRegsLaunch, "register split exceeds launch");
+// 64512): the role warpgroup (warps 0-3) drops, the two softmax warpgroups rise.  Every split
+// below compiles without spills; among the splits that do, these measured fastest (D = 128:
+// 80 / 200, 21.90 ms against 21.97 for 56 / 224 on the video shape; D = 64: 72 / 216, 1.592
+// against 1.611 ms on strided64).  The INT8 P.V variant's producer (two V panels) and issuer
+// (eight P.V MMAs) spill at 56 and take 72 / 208.
+constexpr int kRegsLaunch = 168;
+template <int D, bool kPv16> constexpr int regs_roles() { return kPv16 ? 72 : (D == 128 ? 80 : 72); }
+template <int D, bool kPv16> constexpr int regs_softmax() { return kPv16 ? 208 : (D == 128 ? 200 : 216); }
+static_assert(128 * regs_roles<128, false>() + 256 * regs_softmax<128, false>() <= 384 * kRegsLaunch,
+              "register split exceeds launch");
+static_assert(128 * regs_roles<64, false>() + 256 * regs_softmax<64, false>() <= 384 * kRegsLaunch,
+              "register split exceeds launch");
+static_assert(128 * regs_roles<128, true>() + 256 * regs_softmax<128, true>() <= 384 * kRegsLaunch,
+              "register split exceeds launch");
 constexpr int kBN = 128;   // keys per tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
   if (warp < 4) {
-    regs_dec<(kPv16 ? kRegsRolesPv16 : kRegsRoles)>();
+    regs_dec<regs_roles<D, kPv16>()>();
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else {
-    regs_inc<(kPv16 ? kRegsSoftmaxPv16 : kRegsSoftmax)>();
+    regs_inc<regs_softmax<D, kPv16>()>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                     // TMEM lane quarter this warp may access
