@@ -43,7 +43,6 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
-#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -758,19 +757,12 @@ template <int D, bool kRowQ, bool kPv16, bool kMean>
 cudaError_t launch_variant(dim3 grid, const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& omap, const AttnParams& p, cudaStream_t s) {
   constexpr int kSmem = Cfg<D, kPv16>::kSmemBytes;
-  // The shared-memory limit is a per-device attribute of the function: set it once on each
-  // device (bit d of the mask), and on every call for device numbers past 63.
-  static std::atomic<uint64_t> attr_set{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // The shared-memory limit is an attribute of the function in the current context: set it on
+  // every call (a host-side call, no device synchronisation), so that a new context -- on
+  // another device, or after a cudaDeviceReset -- gets it too.
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kRowQ, kPv16, kMean>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = dev >= 0 && dev < 64 ? uint64_t(1) << dev : 0;
-  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kRowQ, kPv16, kMean>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set.fetch_or(bit, std::memory_order_acq_rel);
-  }
   attn_fwd_kernel<D, kRowQ, kPv16, kMean><<<grid, 384, kSmem, s>>>(qmap, kmap, vmap, omap, p);
   return cudaGetLastError();
 }
