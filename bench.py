@@ -459,6 +459,31 @@ def run_gpu(args):
                                "step_ms": round(v_quant + v_attn, 3)}
             del vz
 
+    # ---- unquantised attention on the tensor cores (sage_attn_dense_bf16_tc: bf16 operands, P
+    # rounded to bf16; V's transpose and the attention, 2 launches) at the same size and inputs,
+    # outside the timed region: 3 warm-up calls, then 10 calls with CUDA events around each.
+    dense_tc = None
+    if not args.no_variants:
+        dz_out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
+        dz_ws = sage.dense_workspace(n, h, d, dev)
+        for _ in range(3):
+            sage.sage_attn_dense_bf16_tc(q, k, v, sm_scale, dz_out, dz_ws, stream)
+        dev_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        torch.cuda.synchronize()
+        for a_, b_ in dev_:
+            a_.record(stream)
+            sage.sage_attn_dense_bf16_tc(q, k, v, sm_scale, dz_out, dz_ws, stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        code, where = sage.sage_check_device_status(dz_ws[:256], stream)
+        if code != 0:
+            raise RuntimeError(f"device status {code} at {where} (dense_tc)")
+        dt_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in dev_)
+        dense_tc = {"call": "sage_attn_dense_bf16_tc", "ms": round(dt_ms, 3),
+                    "tflops": round(flops / (dt_ms * 1e-3) / 1e12, 1), "launches": 2,
+                    "quantised_call_speedup": round(dt_ms / ms_per_step, 3)}
+        del dz_out, dz_ws
+
     # ---- the dense quality anchor (sage_attn_dense_bf16: unquantised, fp32 arithmetic on CUDA
     # cores), timed once after one warm-up call, beside the pages' dense figure -- context only.
     dense = None
@@ -503,6 +528,9 @@ def run_gpu(args):
         # INT8 P.V runs both contractions on fp16 operands, so the 16-bit peak is its roofline;
         # the E4M3 variant has the default path's composite roofline.
         vv_["roofline_frac"] = round(vv_["attention_tflops"] / (p16 if vname.startswith("int8") else composite), 4)
+    if dense_tc is not None:
+        # Both contractions on bf16 operands: the bf16 peak bounds it.
+        dense_tc["roofline_frac_of_bf16_peak"] = round(dense_tc["tflops"] / p16, 4)
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
     # INT8 P.V runs both contractions on 16-bit operands: the bf16 peak is its roofline.
@@ -546,6 +574,7 @@ def run_gpu(args):
                      "mma_ceiling_mode": mix_mode},
         "mma_ceiling": mma_ceiling,
         "dense_anchor": dense,
+        "dense_tc": dense_tc,
         "kernels_ms": {"quantise_all_avg": round(quant_avg, 4), "attention_avg": round(attn_avg, 3),
                        "quantise_gbs_algorithmic": round(quant_bytes / (quant_avg * 1e-3) / 1e9, 1),
                        "quantise_hbm_frac": round(quant_bytes / (quant_avg * 1e-3) / 1e9 / hbm, 4)},

@@ -262,6 +262,29 @@ sage_status sage_attn_dense_bf16(const sage_view* q, const sage_view* k, const s
                                  float sm_scale, void* out, int64_t out_stride_token,
                                  int64_t out_stride_head, void* stream);
 
+/* Bytes of workspace sage_attn_dense_bf16_tc needs: a 256-byte device status block and V
+ * transposed, H * D * N_pad bf16 values (N_pad = N rounded up to 128), 256-byte aligned.
+ * 0 for a shape the library does not take. */
+size_t sage_dense_workspace_bytes(int64_t n_tokens, int64_t n_heads, int64_t head_dim);
+
+/* The same dense attention on the tensor cores, for timing the quantised path against
+ * unquantised attention on the same GPU (the pages time their dense path:
+ * "gb10-sampling-component-profile-1344x768-124f-seed440420.json",
+ * quality_gates.sol_fully_dense_tau_minus_100_p50_milliseconds).  Flash-attention schedule of the fused kernel: 128-key tiles,
+ * S = q k^T from bf16 operands with fp32 accumulation; m the running row max of S;
+ * p = exp2(S * sm_scale * log2 e - m); P = bf16_rn(p); l = sum of the unrounded p;
+ * O = sum P v with fp32 accumulation (rescaled by exp2(m_old - m_new) when m rises);
+ * out = bf16_rn(O / l).  Rounding P to bf16 makes it less exact than sage_attn_dense_bf16:
+ * per element |out - exact| <= 2^-8 max_t |v[t][h][c]| plus fp32 rounding.
+ * Views, output and errors as for sage_attn_dense_bf16.  ws: caller-owned, 256-byte aligned,
+ * >= sage_dense_workspace_bytes (sage_workspace_bytes is enough); the status block at its
+ * start must be zeroed once by the caller before first use, and reports a device timeout
+ * (read it with sage_check_device_status).  Two launches: V's transpose into ws, then the
+ * attention. */
+sage_status sage_attn_dense_bf16_tc(const sage_view* q, const sage_view* k, const sage_view* v,
+                                    float sm_scale, void* out, int64_t out_stride_token,
+                                    int64_t out_stride_head, void* ws, size_t ws_bytes, void* stream);
+
 /* Test hook: the integer S = Qc Kc^T (the QK^T product inside attention_forward of the call
  * above) of head `head`, query rows [i0, i0 + 128 * row_tiles)
  * and keys [j0, j0 + 128 * col_tiles), produced by the same tensor-core QK^T code path

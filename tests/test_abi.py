@@ -14,7 +14,7 @@ EXPECTED = {"sage_status_string", "sage_quant_scratch_bytes", "sage_workspace_by
             "sage_attn_dense_bf16", "sage_debug_qk_int32", "sage_check_device_status",
             "sage_smooth_quant_qk_noalloc", "sage_debug_wait_timeout", "sage_qk_rmsnorm_rope",
             "sage_smooth_quant_qk_rmsnorm_rope", "sage_measure_mma_rate", "sage_get_device_status",
-            "sage_quant_qkv"}
+            "sage_quant_qkv", "sage_dense_workspace_bytes", "sage_attn_dense_bf16_tc"}
 
 
 @pytest.fixture(scope="module")
@@ -97,6 +97,18 @@ def test_argument_validation_never_launches(L):
     assert L.sage_attn_fwd(by(q), by(k), by(v), 0.1, 4096, 256, 128, 4100, 1 << 34, None) == 2
     assert L.sage_attn_fwd_quantized(256, 2, 128, by(qz), 0.1, 4096, 256, 128, 0, None) == 1
     assert L.sage_attn_dense_bf16(by(q), by(k), by(_view(h=3)), 0.1, 4096, 256, 128, None) == 1
+    # tensor-core dense path: the dense path's checks, then its workspace (status block + V^T)
+    dt = L.sage_attn_dense_bf16_tc
+    need = L.sage_dense_workspace_bytes(256, 2, 128)
+    assert need == 256 + 2 * 128 * 256 * 2
+    assert L.sage_dense_workspace_bytes(256, 2, 96) == 0
+    assert dt(by(q), by(k), by(_view(h=3)), 0.1, 4096, 256, 128, 4096, need, None) == 1
+    assert dt(by(q), by(k), by(v), 0.1, 4096, 250, 128, 4096, need, None) == 2
+    assert dt(by(q), by(k), by(v), -1.0, 4096, 256, 128, 4096, need, None) == 1
+    assert dt(by(q), by(k), by(v), 0.1, 4096, 256, 128, 4096, need - 1, None) == 4
+    assert dt(by(q), by(k), by(v), 0.1, 4096, 256, 128, 0, need, None) == 4
+    assert dt(by(q), by(k), by(v), 0.1, 4096, 256, 128, 4352 + 16, need, None) == 2
+    assert dt(by(_view(d=96)), by(_view(d=96)), by(_view(d=96)), 0.1, 4096, 256, 128, 4096, need, None) == 3
     # debug tiles outside N_pad
     assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 0, 128, 0, 2, 1, 4096, 4096, None) == 1
     assert L.sage_debug_qk_int32(256, 2, 128, by(qz), 2, 0, 0, 1, 1, 4096, 4096, None) == 1

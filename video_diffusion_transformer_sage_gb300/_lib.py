@@ -74,6 +74,8 @@ def lib():
             "sage_attn_fwd_quantized": ([I, I, I, QP, F, P, I, I, P, P], ctypes.c_int),
             "sage_attn_fwd": ([VP, VP, VP, F, P, I, I, P, S, P], ctypes.c_int),
             "sage_attn_dense_bf16": ([VP, VP, VP, F, P, I, I, P], ctypes.c_int),
+            "sage_dense_workspace_bytes": ([I, I, I], S),
+            "sage_attn_dense_bf16_tc": ([VP, VP, VP, F, P, I, I, P, S, P], ctypes.c_int),
             "sage_debug_qk_int32": ([I, I, I, QP, I, I, I, I, I, P, P, P], ctypes.c_int),
             "sage_check_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "sage_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
@@ -250,6 +252,30 @@ def sage_attn_dense_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_s
     vq, vk, vv = make_view(q), make_view(k), make_view(v)
     _check(lib().sage_attn_dense_bf16(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), sm_scale,
                                       out.data_ptr(), ost, osh, _stream(stream)), "sage_attn_dense_bf16")
+    return out
+
+
+def dense_workspace(n: int, h: int, d: int, device="cuda") -> torch.Tensor:
+    """Workspace for sage_attn_dense_bf16_tc; its leading status block starts zeroed."""
+    need = int(lib().sage_dense_workspace_bytes(n, h, d))
+    ws = torch.empty(need + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + need]
+    ws[:256].zero_()
+    return ws
+
+
+def sage_attn_dense_bf16_tc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sm_scale: Optional[float] = None,
+                            out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    n, h, d = q.shape
+    sm_scale = 1.0 / math.sqrt(d) if sm_scale is None else sm_scale
+    out, ost, osh = _out_args(out, n, h, d, q.device)
+    ws = dense_workspace(n, h, d, q.device) if ws is None else ws
+    vq, vk, vv = make_view(q), make_view(k), make_view(v)
+    _check(lib().sage_attn_dense_bf16_tc(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv), sm_scale,
+                                         out.data_ptr(), ost, osh, ws.data_ptr(), ws.numel(), _stream(stream)),
+           "sage_attn_dense_bf16_tc")
     return out
 
 

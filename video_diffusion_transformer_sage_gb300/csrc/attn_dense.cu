@@ -8,6 +8,9 @@
 // transposed ([D][64] fp32) so that lane j reads key j without bank conflicts, and V as
 // [64][D] fp32.  Lane j scores keys j and j + 32 for its warp's 8 rows; P is broadcast
 // with warp shuffles into the O accumulation, where lane owns channels lane + 32 i.
+//
+// Also here: the V transpose of the tensor-core dense path (attn_fwd.cu, attn_dense_tc_kernel),
+// whose P.V takes V with the keys of each channel contiguous.
 #include <cuda_bf16.h>
 
 #include "sage_internal.h"
@@ -104,7 +107,56 @@ __global__ void __launch_bounds__(256) attn_dense_kernel(const uint16_t* __restr
   }
 }
 
+// V^T for the tensor-core dense path: vt[h][c][t] = v[t][h][c] (bf16 bits), t < N_pad, zero for
+// t >= N.  CTA = (head, 128 tokens): the tokens' rows are read as 16-byte vectors (4 tokens x 8
+// channels per work item), each channel's 128 tokens gathered in shared memory as 64 bf16 pairs
+// (the earlier token in the low half), then written as 16-byte runs of 8 tokens.
+template <int D>
+__global__ void __launch_bounds__(256) transpose_v_kernel(const uint16_t* __restrict__ v, int64_t st, int64_t sh,
+                                                          int n, int npad, uint16_t* __restrict__ vt) {
+  constexpr int VPR = D / 8;
+  __shared__ uint32_t tile[D][64 + 1];
+  const int hh = blockIdx.x, t_base = blockIdx.y * 128;
+  for (int it = threadIdx.x; it < VPR * 32; it += 256) {
+    const int c8 = it % VPR, tg = it / VPR;
+    uint4 raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t_base + tg * 4 + u;
+      raw[u] = t < n ? *reinterpret_cast<const uint4*>(v + static_cast<int64_t>(t) * st + hh * sh + c8 * 8)
+                     : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t h16[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w = (&raw[u].x)[j >> 1];
+        h16[u] = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+      }
+      tile[c8 * 8 + j][tg * 2] = h16[0] | (h16[1] << 16);
+      tile[c8 * 8 + j][tg * 2 + 1] = h16[2] | (h16[3] << 16);
+    }
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < D * 16; o += 256) {
+    const int c = o / 16, seg = o % 16;
+    const uint4 w = make_uint4(tile[c][seg * 4], tile[c][seg * 4 + 1], tile[c][seg * 4 + 2], tile[c][seg * 4 + 3]);
+    *reinterpret_cast<uint4*>(vt + (static_cast<int64_t>(hh) * D + c) * npad + t_base + seg * 8) = w;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_v(const StridedView& v, int n, int h, int d, uint16_t* vt, cudaStream_t s) {
+  const int npad = static_cast<int>((n + 127) / 128 * 128);
+  const dim3 grid(h, npad / 128);
+  if (d == 128)
+    transpose_v_kernel<128><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, n, npad, vt);
+  else
+    transpose_v_kernel<64><<<grid, 256, 0, s>>>(v.data, v.st, v.sh, n, npad, vt);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_dense(const StridedView& q, const StridedView& k, const StridedView& v, int n, int h,
                               int d, float sm_scale, void* out, int64_t ost, int64_t osh, cudaStream_t s) {

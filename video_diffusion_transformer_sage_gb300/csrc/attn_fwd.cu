@@ -147,10 +147,14 @@ __device__ __forceinline__ float block_max64(const uint32_t* s) {
   return fmaxf(fmax3(a, b, c), d);
 }
 
-// S[tmem d_col] = Q_tile(sq) . K_tile(sk)^T over D channels: D/16 MMAs of 128x128x16.
-template <int D>
+// kind::f16 operand format bf16 (code 1) for A and B; the default code 0 is fp16.
+constexpr uint32_t kIdescBf16 = (1u << 7) | (1u << 10);
+
+// S[tmem d_col] = Q_tile(sq) . K_tile(sk)^T over D channels: D/16 MMAs of 128x128x16 (fp16
+// operands, or bf16 with kBf16).
+template <int D, bool kBf16 = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
-  constexpr uint32_t idesc = idesc_f32acc(kBM, kBN);
+  constexpr uint32_t idesc = idesc_f32acc(kBM, kBN) | (kBf16 ? kIdescBf16 : 0u);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * Cfg<D>::kPanelBytes + (kk & 3) * 32;
@@ -159,10 +163,11 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
 }
 
 // O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3), or with kPv16 8 MMAs of
-// 128 x D x 16 on fp16 codes (P: 16 keys per 8 TMEM columns; V: two 64-key panels).
-template <int D, bool kPv16>
+// 128 x D x 16 on 16-bit values, fp16 codes or with kBf16 bf16 (P: 16 keys per 8 TMEM
+// columns; V: two 64-key panels).
+template <int D, bool kPv16, bool kBf16 = false>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
-  constexpr uint32_t idesc = idesc_f32acc(kBM, D);
+  constexpr uint32_t idesc = idesc_f32acc(kBM, D) | (kBf16 ? kIdescBf16 : 0u);
   if (kPv16) {
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
@@ -188,6 +193,12 @@ __device__ __forceinline__ void p_codes_f16(const float pp[4], uint64_t magic2, 
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(w23) : "r"(h23), "r"(0x64006400u));
 }
 
+// Four probabilities p_k as two bf16x2 words (round to nearest even), the lower key in the low half.
+__device__ __forceinline__ void p_bf16(const float pp[4], uint32_t& w01, uint32_t& w23) {
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w01) : "f"(pp[1]), "f"(pp[0]));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w23) : "f"(pp[3]), "f"(pp[2]));
+}
+
 // One 128-key tile j of the online softmax for the calling thread's row (= TMEM lane):
 //   reads S from TMEM; forms the tile max on raw S per 64-key half (c >= 0 and rounding is
 //   monotone, so max_k fl(S_k c) = fl(c max_k S_k)); writes P = E4M3(448 p) with
@@ -199,7 +210,8 @@ __device__ __forceinline__ void p_codes_f16(const float pp[4], uint64_t magic2, 
 //   once P.V of tile j - 1 has finished with them (pv_done, phase (j - 1) & 1).  Returns false
 //   if that wait expired.
 // kTail: keys >= kvalid are excluded from the max and get p = 0.
-template <int D, bool kTail, bool kPv16>
+// kDense (with kPv16): unquantised attention, P = bf16_rn(p) with p = exp2(S c - m_new) itself.
+template <int D, bool kTail, bool kPv16, bool kDense = false>
 __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint32_t tP, float c0, float c1, int kvalid,
                                              bool first, float& m, float& l, uint64_t* s_free, uint64_t* pv_done,
                                              int j, uint64_t limit) {
@@ -233,8 +245,8 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint32_t 
   const bool rise = !first && (m_new > m);
   const float alpha = rise ? ex2_approx(m - m_new) : 1.0f;
   m = m_new;
-  // p' = 448 p = exp2(S c + log2(448) - m) (127 p with kPv16), two keys per fp32x2 FMA.
-  constexpr float kLog2P = kPv16 ? kLog2_127 : kLog2_448;
+  // p' = 448 p = exp2(S c + log2(448) - m) (127 p with kPv16, p with kDense), two keys per fp32x2 FMA.
+  constexpr float kLog2P = kDense ? 0.0f : (kPv16 ? kLog2_127 : kLog2_448);
   const uint64_t bias2 = f2_pack(kLog2P - m_new, kLog2P - m_new);
   const uint64_t magic2 = f2_pack(kRintMagic, kRintMagic);
   // Partial sums of p': one per (32-key chunk, key pair parity), so no add waits on more than
@@ -265,7 +277,9 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint32_t 
         l2[cch][0] = f2_add(l2[cch][0], f2_pack(pp[0], pp[1]));
         l2[cch][1] = f2_add(l2[cch][1], f2_pack(pp[2], pp[3]));
       }
-      if (kPv16)
+      if (kDense)
+        p_bf16(pp, pw[2 * w], pw[2 * w + 1]);
+      else if (kPv16)
         p_codes_f16(pp, magic2, pw[2 * w], pw[2 * w + 1]);
       else
         pw[w] = pack_h2(e4m3x2(pp[0], pp[1]), e4m3x2(pp[2], pp[3]));
@@ -322,11 +336,14 @@ __device__ __forceinline__ bool softmax_step(uint32_t tS, uint32_t tO, uint32_t 
 // was: the per-row lookup alone measured 0.7 % slower there.
 // kMean: V was smoothed, the epilogue adds p.v_mean (a separate instantiation keeps the
 // default epilogue free of the extra loads).
-template <int D, bool kRowQ, bool kPv16, bool kMean>
-__global__ void __launch_bounds__(384, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-                    const AttnParams p) {
+// kDense (with kPv16, not kRowQ / kMean): unquantised attention on bf16 Q, K and V.  Q and K come
+// straight from the caller's [N][H][D] views through 3-D tensor maps (rows past N read as
+// zeros), V from its transpose [H][D][N_pad]; there are no Q, K or V scales (c = sm_scale log2 e,
+// out = O / l), P is bf16 and both MMAs take bf16 operands.
+template <int D, bool kRowQ, bool kPv16, bool kMean, bool kDense>
+__device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                          const CUtensorMap& omap, const AttnParams& p) {
+  static_assert(!kDense || (kPv16 && !kRowQ && !kMean), "the dense path is the 16-bit P.V schedule alone");
   using C = Cfg<D, kPv16>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_skip;
@@ -389,8 +406,12 @@ __global__ void __launch_bounds__(384, 1)
         const int qrow = hh * p.npad + q0;
         mbar_arrive_expect_tx(q_full, 2 * C::kQTileBytes);
         for (int t = 0; t < 2; ++t)
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_2d(sQ + t * C::kQTileBytes + pn * C::kPanelBytes, &qmap, q_full, pn * 64, qrow + t * kBM);
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            if (kDense)
+              tma_load_3d(sQ + t * C::kQTileBytes + pn * C::kPanelBytes, &qmap, q_full, pn * 64, hh, q0 + t * kBM);
+            else
+              tma_load_2d(sQ + t * C::kQTileBytes + pn * C::kPanelBytes, &qmap, q_full, pn * 64, qrow + t * kBM);
+          }
         for (int j = 0; j < ntiles; ++j) {
           const int s = j % C::kStages;
           if (j >= C::kStages && !mbar_wait(kv_empty + s, ((j / C::kStages) - 1) & 1, limit)) {
@@ -400,8 +421,12 @@ __global__ void __launch_bounds__(384, 1)
           if (s_abort) break;
           uint8_t* sk = sKV + s * C::kStageBytes;
           mbar_arrive_expect_tx(kv_full + s, C::kStageBytes);
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_2d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh * p.npad + j * kBN);
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            if (kDense)
+              tma_load_3d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh, j * kBN);
+            else
+              tma_load_2d(sk + pn * C::kPanelBytes, &kmap, kv_full + s, pn * 64, hh * p.npad + j * kBN);
+          }
           if (kPv16) {
             for (int pn = 0; pn < 2; ++pn)
               tma_load_2d(sk + C::kKTileBytes + pn * C::kVPanelBytes, &vmap, kv_full + s, j * kBN + pn * 64, hh * D);
@@ -422,9 +447,9 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) record_error(p.status, kWhereQFull, &s_abort);
         if (ok) {
           tc_fence_after();
-          issue_qk<D>(colS[0], sq, skv);
+          issue_qk<D, kDense>(colS[0], sq, skv);
           tc_commit(s_full + 0);
-          issue_qk<D>(colS[1], sq + C::kQTileBytes, skv);
+          issue_qk<D, kDense>(colS[1], sq + C::kQTileBytes, skv);
           tc_commit(s_full + 1);
         }
         // Separate P columns: S_t of tile j + 1 is issued as soon as the softmax has read S_t of tile
@@ -445,7 +470,7 @@ __global__ void __launch_bounds__(384, 1)
                 break;
               }
               tc_fence_after();
-              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              issue_qk<D, kDense>(colS[t], sq + t * C::kQTileBytes, sk_next);
               tc_commit(s_full + t);
             }
             if (t < 2) break;
@@ -457,7 +482,7 @@ __global__ void __launch_bounds__(384, 1)
               break;
             }
             tc_fence_after();
-            issue_pv<D, kPv16>(colO[t], colP[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            issue_pv<D, kPv16, kDense>(colO[t], colP[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
             tc_commit(pv_done + t);
           }
           if (t < 2) break;
@@ -473,7 +498,7 @@ __global__ void __launch_bounds__(384, 1)
               break;
             }
             tc_fence_after();
-            issue_pv<D, kPv16>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            issue_pv<D, kPv16, kDense>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
             tc_commit(pv_done + t);
             if (t == 1) tc_commit(kv_empty + s);
             if (j + 1 < ntiles) {
@@ -489,7 +514,7 @@ __global__ void __launch_bounds__(384, 1)
                 break;
               }
               tc_fence_after();
-              issue_qk<D>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              issue_qk<D, kDense>(colS[t], sq + t * C::kQTileBytes, sk_next);
               tc_commit(s_full + t);
             }
           }
@@ -512,7 +537,9 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tP = C::kSepP ? tmem + lane_base + (t == 0 ? C::kColP0 : C::kColP1) : tS;
     const int nbk = p.npad / 64;
     float qscale;
-    if (kRowQ) {
+    if (kDense) {
+      qscale = 1.0f;
+    } else if (kRowQ) {
       // The scale of this thread's own row (its block of 2^q_shift rows); none past the padding.
       qscale = row < p.npad ? p.q_scales[hh * (p.npad >> p.q_shift) + (row >> p.q_shift)] : 0.0f;
     } else {
@@ -520,13 +547,13 @@ __global__ void __launch_bounds__(384, 1)
       qscale = qblk < nbq ? p.q_scales[hh * nbq + qblk] : 0.0f;
     }
     const float cq = qscale * p.sm_scale_log2;
-    const float* ks = p.k_scales + hh * nbk;
+    const float* ks = kDense ? nullptr : p.k_scales + hh * nbk;
     float m = -INFINITY, l = 0.0f;
-    float ksn0 = ks[0], ksn1 = ks[1];   // k scales of the next tile, loaded one tile ahead
+    float ksn0 = kDense ? 1.0f : ks[0], ksn1 = kDense ? 1.0f : ks[1];   // k scales of the next tile, loaded one tile ahead
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const float ks0 = ksn0, ks1 = ksn1;
-      if (j + 1 < ntiles) {
+      if (!kDense && j + 1 < ntiles) {
         ksn0 = ks[2 * j + 2];
         ksn1 = ks[2 * j + 3];
       }
@@ -540,9 +567,10 @@ __global__ void __launch_bounds__(384, 1)
       const int kvalid = min(kBN, p.n - j * kBN);
       const bool stepped =
           kvalid == kBN
-              ? softmax_step<D, false, kPv16>(tS, tO, tP, c0, c1, kBN, j == 0, m, l, s_free + t, pv_done + t, j, limit)
-              : softmax_step<D, true, kPv16>(tS, tO, tP, c0, c1, kvalid, j == 0, m, l, s_free + t, pv_done + t, j,
-                                             limit);
+              ? softmax_step<D, false, kPv16, kDense>(tS, tO, tP, c0, c1, kBN, j == 0, m, l, s_free + t, pv_done + t,
+                                                      j, limit)
+              : softmax_step<D, true, kPv16, kDense>(tS, tO, tP, c0, c1, kvalid, j == 0, m, l, s_free + t, pv_done + t,
+                                                     j, limit);
       if (!stepped) {
         if (lane == 0) record_error(p.status, kWherePvDone, &s_abort);
         ok = false;
@@ -554,8 +582,8 @@ __global__ void __launch_bounds__(384, 1)
     if (ok && warp_wait(pv_done + t, (ntiles - 1) & 1, limit)) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      const float* vs = p.v_scales + hh * D;
-      const float* vm = p.v_mean + hh * D;
+      const float* vs = kDense ? nullptr : p.v_scales + hh * D;
+      const float* vm = kMean ? p.v_mean + hh * D : nullptr;
       uint16_t* orow = p.out + static_cast<int64_t>(row) * p.ost + static_cast<int64_t>(hh) * p.osh;
       // With the output map, the rows go through Q tile t's shared memory (every Q.K^T that read it
       // was issued before this tile's last P.V, so it has completed) in the map's 128-byte
@@ -577,8 +605,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int k = v8 * 8 + u * 2;
-              float a = __uint_as_float(o[k]) * vs[c + k] * inv_l;
-              float b = __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
+              float a = kDense ? __uint_as_float(o[k]) * inv_l : __uint_as_float(o[k]) * vs[c + k] * inv_l;
+              float b = kDense ? __uint_as_float(o[k + 1]) * inv_l : __uint_as_float(o[k + 1]) * vs[c + k + 1] * inv_l;
               if (kMean) {
                 a += vm[c + k];
                 b += vm[c + k + 1];
@@ -620,6 +648,22 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+template <int D, bool kRowQ, bool kPv16, bool kMean>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                    const AttnParams p) {
+  attn_body<D, kRowQ, kPv16, kMean, false>(qmap, kmap, vmap, omap, p);
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    attn_dense_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                         const AttnParams p) {
+  attn_body<D, false, true, false, true>(qmap, kmap, vmap, omap, p);
 }
 
 // --------------------------------------------------------------------------- debug: S tiles
@@ -738,6 +782,27 @@ bool make_out_map(CUtensorMap* m, void* out, int n, int h, int d, int64_t ost, i
   return r == CUDA_SUCCESS;
 }
 
+// A bf16 [N][H][D] view with the caller's token and head strides (elements) as a 3-D map
+// {D, H, N}, 128-byte swizzled boxes of 64 channels x 1 head x 128 rows: in shared memory the
+// same panel layout as a 128-row tile of codes.  A stride of a dimension of extent 1 is never
+// stepped, so any valid value stands in for it.  False if the map cannot be built (the strides
+// must be multiples of 8 elements).
+bool make_view_map(CUtensorMap* m, const void* base, int n, int h, int d, int64_t st, int64_t sh) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  if (h == 1 && sh <= 0) sh = d;
+  if (n == 1 && st <= 0) st = static_cast<int64_t>(h) * d;
+  if (st <= 0 || sh <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(st) * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Row-major [rows][inner] matrix, 128-byte swizzled boxes of box_rows x box_inner elements.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
               uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
@@ -818,6 +883,37 @@ cudaError_t launch_attn_fwd_t(int n, int h, const sage_quantized& qz, int q_bloc
 }
 
 template <int D>
+cudaError_t launch_attn_dense_tc_t(const StridedView& q, const StridedView& k, const uint16_t* vt, int n, int h,
+                                   float sm_scale, void* out, int64_t ost, int64_t osh, int32_t* status,
+                                   cudaStream_t s) {
+  using C = Cfg<D, true>;
+  const int npad = static_cast<int>(pad128(n));
+  CUtensorMap qmap, kmap, vmap, omap;
+  if (!make_view_map(&qmap, q.data, n, h, D, q.st, q.sh) || !make_view_map(&kmap, k.data, n, h, D, k.st, k.sh) ||
+      !make_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vt, npad, static_cast<uint64_t>(h) * D, 64, D))
+    return cudaErrorInvalidValue;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.n = n;
+  p.npad = npad;
+  p.h = h;
+  p.sm_scale_log2 = sm_scale * kLog2e;
+  p.out = static_cast<uint16_t*>(out);
+  p.ost = ost;
+  p.osh = osh;
+  memset(&omap, 0, sizeof(omap));
+  p.tma_out = (D == 128 && make_out_map(&omap, out, n, h, D, ost, osh)) ? 1 : 0;
+  p.status = status;
+  p.wait_limit_ns = kWaitLimitNs;
+  cudaError_t e = cudaFuncSetAttribute(attn_dense_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((npad + 2 * kBM - 1) / (2 * kBM), h);
+  attn_dense_tc_kernel<D><<<grid, 384, C::kSmemBytes, s>>>(qmap, kmap, vmap, omap, p);
+  return cudaGetLastError();
+}
+
+template <int D>
 cudaError_t launch_debug_qk_t(int n, int h, const sage_quantized& qz, int head, int i0, int j0, int row_tiles,
                               int col_tiles, int32_t* out, int32_t* status, cudaStream_t s) {
   using C = Cfg<D, false>;
@@ -840,6 +936,12 @@ cudaError_t launch_attn_fwd(int n, int h, int d, const sage_quantized& qz, int q
                             int64_t ost, int64_t osh, int32_t* status, cudaStream_t s) {
   return d == 128 ? launch_attn_fwd_t<128>(n, h, qz, q_block, sm_scale, out, ost, osh, status, s)
                   : launch_attn_fwd_t<64>(n, h, qz, q_block, sm_scale, out, ost, osh, status, s);
+}
+
+cudaError_t launch_attn_dense_tc(const StridedView& q, const StridedView& k, const uint16_t* vt, int n, int h, int d,
+                                 float sm_scale, void* out, int64_t ost, int64_t osh, int32_t* status, cudaStream_t s) {
+  return d == 128 ? launch_attn_dense_tc_t<128>(q, k, vt, n, h, sm_scale, out, ost, osh, status, s)
+                  : launch_attn_dense_tc_t<64>(q, k, vt, n, h, sm_scale, out, ost, osh, status, s);
 }
 
 cudaError_t launch_debug_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t s) {

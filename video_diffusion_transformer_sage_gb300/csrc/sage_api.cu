@@ -319,6 +319,32 @@ sage_status sage_attn_dense_bf16(const sage_view* q, const sage_view* k, const s
                                              static_cast<cudaStream_t>(stream)));
 }
 
+size_t sage_dense_workspace_bytes(int64_t n, int64_t h, int64_t d) {
+  if (check_shape(n, h, d) != SAGE_OK) return 0;
+  return kStatusBytes + up256(static_cast<size_t>(h) * d * pad128(n) * 2);
+}
+
+sage_status sage_attn_dense_bf16_tc(const sage_view* q, const sage_view* k, const sage_view* v, float sm_scale,
+                                    void* out, int64_t ost, int64_t osh, void* ws, size_t ws_bytes, void* stream) {
+  sage_status st;
+  if ((st = check_view(q)) != SAGE_OK || (st = check_view(k)) != SAGE_OK || (st = check_view(v)) != SAGE_OK)
+    return st;
+  if (!same_shape(q, k) || !same_shape(q, v)) return SAGE_ERR_INVALID_ARG;
+  if ((st = check_out(out, ost, osh)) != SAGE_OK) return st;
+  if (!(sm_scale > 0.0f)) return SAGE_ERR_INVALID_ARG;
+  const int64_t n = q->n_tokens, h = q->n_heads, d = q->head_dim;
+  if (!ws) return SAGE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SAGE_ERR_ALIGNMENT;
+  if (ws_bytes < sage_dense_workspace_bytes(n, h, d)) return SAGE_ERR_WORKSPACE;
+  auto* status = static_cast<int32_t*>(ws);
+  auto* vt = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + kStatusBytes);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = sage::launch_transpose_v(sv(v), int(n), int(h), int(d), vt, s);
+  if (e == cudaSuccess)
+    e = sage::launch_attn_dense_tc(sv(q), sv(k), vt, int(n), int(h), int(d), sm_scale, out, ost, osh, status, s);
+  return cuda_status(e);
+}
+
 sage_status sage_debug_qk_int32(int64_t n, int64_t h, int64_t d, const sage_quantized* qz, int64_t head, int64_t i0,
                                 int64_t j0, int64_t row_tiles, int64_t col_tiles, int32_t* out, void* status_block,
                                 void* stream) {

@@ -85,6 +85,9 @@ cudaError_t launch_debug_qk(int n, int h, int d, const sage_quantized& qz, int h
                             int col_tiles, int32_t* out, int32_t* status, cudaStream_t s);
 
 cudaError_t launch_debug_wait_timeout(int32_t* status, uint64_t limit_ns, cudaStream_t s);
+// The tensor-core dense path: Q, K as bf16 views, V transposed to vt [H][D][N_pad] bf16.
+cudaError_t launch_attn_dense_tc(const StridedView& q, const StridedView& k, const uint16_t* vt, int n, int h, int d,
+                                 float sm_scale, void* out, int64_t ost, int64_t osh, int32_t* status, cudaStream_t s);
 
 // mma_rate.cu: `ctas` CTAs each issue `iters` rounds of the tensor-core MMAs of `mode` (0-4).
 cudaError_t launch_mma_rate(int mode, int iters, int ctas, int32_t* status, uint64_t limit_ns, cudaStream_t s);
@@ -92,5 +95,7 @@ cudaError_t launch_mma_rate(int mode, int iters, int ctas, int32_t* status, uint
 // attn_dense.cu
 cudaError_t launch_attn_dense(const StridedView& q, const StridedView& k, const StridedView& v, int n, int h,
                               int d, float sm_scale, void* out, int64_t ost, int64_t osh, cudaStream_t s);
+// vt[h][c][t] = v[t][h][c] for t < N_pad (zero for t >= N): the V operand of the tensor-core dense path.
+cudaError_t launch_transpose_v(const StridedView& v, int n, int h, int d, uint16_t* vt, cudaStream_t s);
 
 }  // namespace sage

@@ -86,6 +86,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// 3-D tiled load of one box, completion signalled on `bar` as transaction bytes (the whole box,
+// elements outside the tensor filled with zeros).  x is the innermost coordinate (elements, its
+// byte offset a multiple of 16).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // 3-D tiled store of one box from shared memory (laid out as the map's swizzle says), tracked
 // by bulk groups (bulk_commit / bulk_wait_read).  x is the innermost coordinate (elements, its
 // byte offset a multiple of 16); no coordinate may be negative.  Elements outside the tensor
