@@ -81,3 +81,28 @@ def test_dense_tc_close_to_fp32_dense_path():
     f32 = sage.sage_attn_dense_bf16(case["q"], case["k"], case["v"]).float()
     torch.cuda.synchronize()
     assert float((tc - f32).norm() / f32.norm()) <= 4e-3
+
+
+EDGE = [(1, 1, 128), (1, 2, 64), (100, 1, 128), (127, 1, 128), (129, 3, 64), (255, 2, 128), (257, 1, 64)]
+
+
+@pytest.mark.parametrize("n,h,d", EDGE)
+def test_dense_tc_edge_shapes(n, h, d):
+    """Fewer tokens than one 128-row box (the tensor maps' boxes reach past N and read zeros),
+    one key past a tile boundary, a second Q tile wholly in the padding, odd head counts."""
+    inp = synth.make_inputs(synth.custom(n, h, d, "qkv", seed=7 * n + h + d, n_outlier=1))
+    st = inp.storage.to("cuda")
+    hd = h * d
+    q, k, v = (st[:, i * hd:(i + 1) * hd].view(n, h, d) for i in range(3))
+    sm = 1.0 / math.sqrt(d)
+    ws = sage.dense_workspace(n, h, d)
+    out = sage.sage_attn_dense_bf16_tc(q, k, v, sm, ws=ws)
+    torch.cuda.synchronize()
+    assert sage.sage_check_device_status(ws[:256]) == (0, 0)
+    got = out.float().cpu().numpy().astype(np.float64)
+    if n == 1:
+        # softmax over one key: P = 1 exactly, so the output is that key's V
+        assert torch.equal(out.cpu(), inp.v)
+    rows = list(range(n))
+    ex = oracle.attn_exact(inp.q, inp.k, inp.v, sm, rows)
+    assert (np.abs(got - ex) - _bound(inp, rows, sm)).max() <= 0.0
