@@ -155,10 +155,11 @@ constexpr uint32_t kIdescBf16 = (1u << 7) | (1u << 10);
 template <int D, bool kBf16 = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, kBN) | (kBf16 ? kIdescBf16 : 0u);
+  const uint32_t ql = sdesc_lo(sq), kl = sdesc_lo(sk);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * Cfg<D>::kPanelBytes + (kk & 3) * 32;
-    mma_f16_ss(d_tmem, sdesc_k_sw128(sq + off), sdesc_k_sw128(sk + off), idesc, kk > 0 ? 1u : 0u);
+    const uint32_t off16 = ((kk >> 2) * Cfg<D>::kPanelBytes + (kk & 3) * 32) >> 4;
+    mma_f16_ss(d_tmem, sdesc_of_lo(ql + off16), sdesc_of_lo(kl + off16), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -168,15 +169,17 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t 
 template <int D, bool kPv16, bool kBf16 = false>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, D) | (kBf16 ? kIdescBf16 : 0u);
+  const uint32_t vl = sdesc_lo(sv);
   if (kPv16) {
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
-      mma_f16_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + (kk >> 2) * Cfg<D, true>::kVPanelBytes + (kk & 3) * 32),
-                 idesc, (first && kk == 0) ? 0u : 1u);
+      mma_f16_ts(o_tmem, p_tmem + kk * 8,
+                 sdesc_of_lo(vl + (((kk >> 2) * Cfg<D, true>::kVPanelBytes + (kk & 3) * 32) >> 4)), idesc,
+                 (first && kk == 0) ? 0u : 1u);
   } else {
 #pragma unroll
     for (int kk = 0; kk < kBN / 32; ++kk)
-      mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_k_sw128(sv + kk * 32), idesc, (first && kk == 0) ? 0u : 1u);
+      mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_of_lo(vl + ((kk * 32) >> 4)), idesc, (first && kk == 0) ? 0u : 1u);
   }
 }
 

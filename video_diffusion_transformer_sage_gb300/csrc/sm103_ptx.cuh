@@ -211,6 +211,16 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same descriptor in two 32-bit words: the high word is one constant for every operand
+// (stride byte offset, version, swizzle), the low word holds the start address and the leading
+// byte offset.  Shared-window addresses are below 2^18, so the low word of base + off (off a
+// multiple of 16) is the low word of base plus off / 16: no carry leaves the 14-bit start address.
+constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+__device__ __forceinline__ uint64_t sdesc_of_lo(uint32_t lo) {
+  return (static_cast<uint64_t>(kSdescHi) << 32) | lo;
+}
+
 // Instruction descriptor: fp32 accumulator, A/B format code 0 (fp16 for kind::f16, E4M3 for
 // kind::f8f6f4), both operands K-major, dense, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_f32acc(int m, int n) {
