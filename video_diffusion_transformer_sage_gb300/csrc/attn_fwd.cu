@@ -152,24 +152,28 @@ constexpr uint32_t kIdescBf16 = (1u << 7) | (1u << 10);
 
 // S[tmem d_col] = Q_tile(sq) . K_tile(sk)^T over D channels: D/16 MMAs of 128x128x16 (fp16
 // operands, or bf16 with kBf16).
+// ql, kl: the descriptor low words (sdesc_lo) of the Q and K tiles.
 template <int D, bool kBf16 = false>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
+__device__ __forceinline__ void issue_qk_lo(uint32_t d_tmem, uint32_t ql, uint32_t kl) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, kBN) | (kBf16 ? kIdescBf16 : 0u);
-  const uint32_t ql = sdesc_lo(sq), kl = sdesc_lo(sk);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off16 = ((kk >> 2) * Cfg<D>::kPanelBytes + (kk & 3) * 32) >> 4;
     mma_f16_ss(d_tmem, sdesc_of_lo(ql + off16), sdesc_of_lo(kl + off16), idesc, kk > 0 ? 1u : 0u);
   }
 }
+template <int D, bool kBf16 = false>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sq, uint32_t sk) {
+  issue_qk_lo<D, kBf16>(d_tmem, sdesc_lo(sq), sdesc_lo(sk));
+}
 
 // O[tmem] (+)= P[tmem] . V_tile(sv): 4 MMAs of 128 x D x 32 (E4M3), or with kPv16 8 MMAs of
 // 128 x D x 16 on 16-bit values, fp16 codes or with kBf16 bf16 (P: 16 keys per 8 TMEM
 // columns; V: two 64-key panels).
+// vl: the descriptor low word (sdesc_lo) of the V tile.
 template <int D, bool kPv16, bool kBf16 = false>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, bool first) {
+__device__ __forceinline__ void issue_pv_lo(uint32_t o_tmem, uint32_t p_tmem, uint32_t vl, bool first) {
   constexpr uint32_t idesc = idesc_f32acc(kBM, D) | (kBf16 ? kIdescBf16 : 0u);
-  const uint32_t vl = sdesc_lo(sv);
   if (kPv16) {
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
@@ -446,26 +450,33 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
         const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
         const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
         const uint32_t colP[2] = {tmem + (C::kSepP ? C::kColP0 : C::kColS0), tmem + (C::kSepP ? C::kColP1 : C::kColS1)};
+        // Descriptor low words: Q tile t at q_lo + t * kQLo, ring stage s's K tile at kv_lo + s * kStageLo,
+        // its V tile kVLo further.
+        const uint32_t q_lo = sdesc_lo(sq), kv_lo = sdesc_lo(skv);
+        constexpr uint32_t kQLo = C::kQTileBytes >> 4, kStageLo = C::kStageBytes >> 4, kVLo = C::kKTileBytes >> 4;
         bool ok = mbar_wait(q_full, 0, limit) && mbar_wait(kv_full, 0, limit);
         if (!ok) record_error(p.status, kWhereQFull, &s_abort);
         if (ok) {
           tc_fence_after();
-          issue_qk<D, kDense>(colS[0], sq, skv);
+          issue_qk_lo<D, kDense>(colS[0], q_lo, kv_lo);
           tc_commit(s_full + 0);
-          issue_qk<D, kDense>(colS[1], sq + C::kQTileBytes, skv);
+          issue_qk_lo<D, kDense>(colS[1], q_lo + kQLo, kv_lo);
           tc_commit(s_full + 1);
         }
+        // Ring stage of tile j (s) and of tile j + 1 (sn) with the kv_full phase of tile j + 1,
+        // advanced once per tile.
+        int s = 0, sn = 1 % C::kStages;
+        uint32_t phn = 0;
         // Separate P columns: S_t of tile j + 1 is issued as soon as the softmax has read S_t of tile
         // j (s_free), P.V of tile j once P_t is written (p_full).  A softmax writes P_t of tile j + 1
         // only after P.V of tile j is done, so it never runs two tiles ahead of these waits.
         for (int j = 0; C::kSepP && ok && j < ntiles; ++j) {
-          const int s = j % C::kStages;
           if (j + 1 < ntiles) {
-            if (!mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+            if (!mbar_wait(kv_full + sn, phn, limit)) {
               record_error(p.status, kWhereKvFull, &s_abort);
               break;
             }
-            const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+            const uint32_t k_next = kv_lo + sn * kStageLo;
             int t = 0;
             for (; t < 2; ++t) {
               if (!mbar_wait(s_free + t, j & 1, limit)) {
@@ -473,7 +484,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
                 break;
               }
               tc_fence_after();
-              issue_qk<D, kDense>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              issue_qk_lo<D, kDense>(colS[t], q_lo + t * kQLo, k_next);
               tc_commit(s_full + t);
             }
             if (t < 2) break;
@@ -485,15 +496,19 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
               break;
             }
             tc_fence_after();
-            issue_pv<D, kPv16, kDense>(colO[t], colP[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            issue_pv_lo<D, kPv16, kDense>(colO[t], colP[t], kv_lo + s * kStageLo + kVLo, j == 0);
             tc_commit(pv_done + t);
           }
           if (t < 2) break;
           tc_commit(kv_empty + s);
+          s = sn;
+          if (++sn == C::kStages) {
+            sn = 0;
+            phn ^= 1u;
+          }
         }
         for (int j = 0; !C::kSepP && ok && j < ntiles; ++j) {
-          const int s = j % C::kStages;
-          const uint32_t sk_next = skv + ((j + 1) % C::kStages) * C::kStageBytes;
+          const uint32_t k_next = kv_lo + sn * kStageLo;
           for (int t = 0; t < 2 && ok; ++t) {
             if (!mbar_wait(p_full + t, j & 1, limit)) {
               record_error(p.status, kWherePFull, &s_abort);
@@ -501,11 +516,11 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
               break;
             }
             tc_fence_after();
-            issue_pv<D, kPv16, kDense>(colO[t], colS[t], skv + s * C::kStageBytes + C::kKTileBytes, j == 0);
+            issue_pv_lo<D, kPv16, kDense>(colO[t], colS[t], kv_lo + s * kStageLo + kVLo, j == 0);
             tc_commit(pv_done + t);
             if (t == 1) tc_commit(kv_empty + s);
             if (j + 1 < ntiles) {
-              if (t == 0 && !mbar_wait(kv_full + (j + 1) % C::kStages, ((j + 1) / C::kStages) & 1, limit)) {
+              if (t == 0 && !mbar_wait(kv_full + sn, phn, limit)) {
                 record_error(p.status, kWhereKvFull, &s_abort);
                 ok = false;
                 break;
@@ -517,9 +532,14 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
                 break;
               }
               tc_fence_after();
-              issue_qk<D, kDense>(colS[t], sq + t * C::kQTileBytes, sk_next);
+              issue_qk_lo<D, kDense>(colS[t], q_lo + t * kQLo, k_next);
               tc_commit(s_full + t);
             }
+          }
+          s = sn;
+          if (++sn == C::kStages) {
+            sn = 0;
+            phn ^= 1u;
           }
         }
         // Drain: every MMA issued above has finished before the CTA frees its tensor memory.
