@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(256) colfinal_kv_kernel(const float* __restric
                                                           const float* __restrict__ part_v, int nchunk, int cols,
                                                           int n, float* __restrict__ k_mean,
                                                           float* __restrict__ v_scales) {
+  grid_dep_wait();   // launched as a dependent of the column pass (small calls)
+  grid_dep_launch();
   if (blockIdx.z == 0)
     colfinal_block<false>(part_k, nchunk, cols, n, 0.0f, k_mean);
   else
@@ -681,6 +683,8 @@ __global__ void __launch_bounds__(256) quant_v_fixup_kernel(const uint16_t* __re
                                                             const float* __restrict__ v_scales,
                                                             const float* __restrict__ v_mean, int n, int npad,
                                                             void* __restrict__ v_codes) {
+  grid_dep_wait();   // launched as a dependent of quant_v (small calls)
+  grid_dep_launch();
   const int hh = blockIdx.x;
   bool sub = false;
   for (int c = threadIdx.x; c < D; c += 256) sub = sub || subnormal_scale(v_scales[hh * D + c]);
@@ -710,8 +714,10 @@ cudaError_t launch_quant_v_t(const StridedView& v, const float* v_scales, const 
                                                                      v_codes);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  quant_v_fixup_kernel<D, kI8, kMean><<<h, 256, 0, s>>>(v.data, v.st, v.sh, v_scales, v_mean, n, npad, v_codes);
-  return cudaGetLastError();
+  // The fix-up (one CTA per head, nearly always exiting at once) launches as a dependent of
+  // quant_v in small calls, which hides its launch.
+  return launch_dependent(dependent_launches(n, h, D), quant_v_fixup_kernel<D, kI8, kMean>, dim3(h), dim3(256), 0, s,
+                          v.data, v.st, v.sh, v_scales, v_mean, n, npad, v_codes);
 }
 
 template <int D>
@@ -751,8 +757,9 @@ cudaError_t launch_colreduce_kv(const StridedView& k, const StridedView& v, int 
 
 cudaError_t launch_colfinal_kv(const float* part_k, const float* part_v, int nchunk, int cols, int n, float* k_mean,
                                float* v_scales, cudaStream_t s) {
-  colfinal_kv_kernel<<<dim3((cols + 31) / 32, 1, 2), 256, 0, s>>>(part_k, part_v, nchunk, cols, n, k_mean, v_scales);
-  return cudaGetLastError();
+  // A dependent of the column pass in small calls, which hides its launch.
+  return launch_dependent(dependent_launches(n, 1, cols), colfinal_kv_kernel, dim3((cols + 31) / 32, 1, 2), dim3(256), 0,
+                          s, part_k, part_v, nchunk, cols, n, k_mean, v_scales);
 }
 
 cudaError_t launch_colfinal(const float* partials, int nchunk, int cols, int n, float amax_div, float* out,

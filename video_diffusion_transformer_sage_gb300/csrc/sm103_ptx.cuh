@@ -72,6 +72,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// ------------------------------------------------------------------ dependent launches
+// A kernel launched with programmatic stream serialization may start while the kernel before it
+// in the stream drains.  grid_dep_wait blocks until that kernel has completed and its memory
+// operations are visible (a no-op in a kernel launched without the attribute);
+// grid_dep_launch lets the next such kernel launch once every CTA of this one has issued it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
