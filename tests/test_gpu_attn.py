@@ -156,6 +156,30 @@ def test_deterministic_and_layout_invariant():
     assert len(digests) == 1
 
 
+@pytest.mark.parametrize("name", ["tiny", "tails"])
+def test_back_to_back_calls_on_alternating_inputs(name):
+    """Calls queued back to back on one stream, sharing one workspace, with two input sets in
+    turn: every output equals its input set's reference bit for bit.  Small calls launch some of
+    their kernels as dependents of the kernel before them; nothing of one call may be read or
+    overwritten out of order by the next."""
+    case = gpu_case(name)
+    n, h, d = case["q"].shape
+    other = [torch.flip(t, dims=[0]).contiguous() for t in (case["q"], case["k"], case["v"])]
+    sets = [(case["q"], case["k"], case["v"]), tuple(other)]
+    refs = []
+    for qkv in sets:
+        refs.append(sage.sage_attn_fwd(*qkv))
+        torch.cuda.synchronize()
+    ws = sage.workspace(n, h, d)
+    outs = [torch.empty((n, h, d), dtype=torch.bfloat16, device="cuda") for _ in range(24)]
+    for i, o in enumerate(outs):
+        sage.sage_attn_fwd(*sets[i % 2], out=o, ws=ws)
+    torch.cuda.synchronize()
+    assert sage.sage_check_device_status(ws[:256]) == (0, 0)
+    for i, o in enumerate(outs):
+        assert torch.equal(o, refs[i % 2]), i
+
+
 def test_status_clean_after_runs():
     case = gpu_case("tiny")
     n, h, d = case["q"].shape
