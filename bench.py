@@ -571,7 +571,11 @@ def run_gpu(args):
                      "frac_of_bf16_peak": round(achieved / p16, 4),
                      "frac_of_mma_ceiling": (round(achieved / mma_ceiling["tflops"][mix_mode], 4)
                                              if mma_ceiling else None),
-                     "mma_ceiling_mode": mix_mode},
+                     "mma_ceiling_mode": mix_mode,
+                     # against the measured dense E4M3 (kind::f8f6f4) instruction rate, 128x256x32
+                     # from shared memory: what the whole contraction would take at the FP8 rate
+                     "frac_of_measured_e4m3_rate": (round(achieved / mma_ceiling["tflops"]["e4m3_ss_128x256x32"], 4)
+                                                    if mma_ceiling else None)},
         "mma_ceiling": mma_ceiling,
         "dense_anchor": dense,
         "dense_tc": dense_tc,
