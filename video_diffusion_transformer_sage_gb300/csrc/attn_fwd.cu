@@ -58,16 +58,25 @@ constexpr int kBM = 128;   // query rows per tile
 // 64512): the role warpgroup (warps 0-3) drops, the two softmax warpgroups rise.  Every split
 // below compiles without spills; among the splits that do, these measured fastest (D = 128:
 // 80 / 200, 21.90 ms against 21.97 for 56 / 224 on the video shape; D = 64: 72 / 216, 1.592
-// against 1.611 ms on strided64).  The INT8 P.V variant's producer (two V panels) and issuer
-// (eight P.V MMAs) spill at 56 and take 72 / 208.
+// against 1.611 ms on strided64).  The 16-bit P.V schedule's producer (two V panels) and issuer
+// (eight P.V MMAs) spill at 56: the INT8 P.V variant takes 80 / 208 at D = 128 (24.95 ms against
+// 25.31 for 72 / 208) and 72 / 208 at D = 64; the dense bf16 kernel 72 / 216 (25.28 against 25.38).
 constexpr int kRegsLaunch = 168;
-template <int D, bool kPv16> constexpr int regs_roles() { return kPv16 ? 72 : (D == 128 ? 80 : 72); }
-template <int D, bool kPv16> constexpr int regs_softmax() { return kPv16 ? 208 : (D == 128 ? 200 : 216); }
+template <int D, bool kPv16, bool kDense = false> constexpr int regs_roles() {
+  return kDense ? 72 : (kPv16 ? (D == 128 ? 80 : 72) : (D == 128 ? 80 : 72));
+}
+template <int D, bool kPv16, bool kDense = false> constexpr int regs_softmax() {
+  return kDense ? 216 : (kPv16 ? 208 : (D == 128 ? 200 : 216));
+}
 static_assert(128 * regs_roles<128, false>() + 256 * regs_softmax<128, false>() <= 384 * kRegsLaunch,
               "register split exceeds launch");
 static_assert(128 * regs_roles<64, false>() + 256 * regs_softmax<64, false>() <= 384 * kRegsLaunch,
               "register split exceeds launch");
 static_assert(128 * regs_roles<128, true>() + 256 * regs_softmax<128, true>() <= 384 * kRegsLaunch,
+              "register split exceeds launch");
+static_assert(128 * regs_roles<64, true>() + 256 * regs_softmax<64, true>() <= 384 * kRegsLaunch,
+              "register split exceeds launch");
+static_assert(128 * regs_roles<128, true, true>() + 256 * regs_softmax<128, true, true>() <= 384 * kRegsLaunch,
               "register split exceeds launch");
 constexpr int kBN = 128;   // keys per tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
@@ -403,7 +412,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
   if (warp < 4) {
-    regs_dec<regs_roles<D, kPv16>()>();
+    regs_dec<regs_roles<D, kPv16, kDense>()>();
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -548,7 +557,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& qmap, const CUtenso
       }
     }
   } else {
-    regs_inc<regs_softmax<D, kPv16>()>();
+    regs_inc<regs_softmax<D, kPv16, kDense>()>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                     // TMEM lane quarter this warp may access
